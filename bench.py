@@ -1,0 +1,442 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode step (copy-on-write copy + slot-mapped append
++ paged decode attention with its split-K merge) on synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--partition P] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is the step's algorithmic bytes (KV gathered
+through the block tables + q + out + tables + lens, the append's rows and the
+block copies) over the device time of exactly K steps (CUDA events, inputs
+resident in HBM), summed over ranks and divided by the slowest rank's time.
+``e2e`` is the same metric through the public API with every step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  ``roofline`` is the decode kernel's achieved bandwidth against the
+measured HBM copy peak.  ``cpu_baseline`` times the float64 oracle on a
+bounded sample of the same workload.  ``--impl reference`` times that oracle
+alone, as the reference arm.
+
+With ``--gpus N`` (torchrun) every rank runs its own replica of the workload
+on its own GPU (the path has no exchange step; no collective touches the
+data), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak) and µs/step, 1 GPU"
+DEFAULT_WORKLOAD = "llama7b_mha"
+KERNEL_SOURCES = ["paged_kv_cache_10_gb300/csrc/pkv_decode_impl.cuh", "paged_kv_cache_10_gb300/csrc/pkv_device.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """dram read+write bytes per decode launch from the committed ncu summary,
+    valid only for the kernel sources it was taken on."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kh = kernel_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == kh:
+            return float(parts[2])
+    return None
+
+
+def step_bytes(step) -> dict:
+    """Algorithmic bytes of one step of a DecodeStep."""
+    wl = step.wl
+    ke = wl.kv_elem_bytes()
+    qe = 2
+    lens = step.seq_lens.astype(np.int64)
+    kv = int(lens.sum()) * 2 * wl.Hkv * wl.D * ke
+    q_out = 2 * wl.S * wl.Hq * wl.D * qe
+    tables = int(((lens + wl.b - 1) // wl.b).sum()) * 4 + wl.S * 4
+    decode = kv + q_out + tables
+    n_app = int((step.slots >= 0).sum())
+    in_e = 2
+    append = n_app * 2 * wl.Hkv * wl.D * (in_e + ke) + wl.S * 8
+    block_bytes = wl.Hkv * wl.b * wl.D * ke
+    copy = len(step.pairs) * (2 * 2 * block_bytes + 8)
+    return {"kv": kv, "decode": decode, "append": append, "copy": copy, "total": decode + append + copy}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, stamped on arrival."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.samples = []
+        self.proc = None
+        ident = []
+        try:
+            ident = ["-i", "GPU-" + str(torch.cuda.get_device_properties(device).uuid)]
+        except Exception:
+            ident = []
+        cmd = ["nvidia-smi", *ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.monotonic(), float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[3][i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def aggregate(value_bytes: float, seconds: float, group=None):
+    """Whole-job bytes (sum over ranks) and time (max over ranks)."""
+    import torch.distributed as dist
+    if group is None and not (dist.is_available() and dist.is_initialized()):
+        return value_bytes, seconds
+    t = torch.tensor([value_bytes, seconds], dtype=torch.float64)
+    if dist.get_backend(group) == "nccl":
+        t = t.cuda()
+    b = t[0:1].clone()
+    s = t[1:2].clone()
+    dist.all_reduce(b, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX, group=group)
+    return float(b.item()), float(s.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------- oracle timing
+def oracle_rows_step(wl, step, rows, pools):
+    """The float64 oracle on rows of the workload: their append and their
+    decode (plus the copy-on-write copies of the step).  ``pools`` = (k, v)
+    numpy pools updated in place (idempotent)."""
+    import oracle
+    kp, vp = pools
+    if len(step.pairs):
+        oracle.copy_blocks(kp, vp, wl.kv_dtype, step.pairs)
+    sl = np.full(wl.S, -1, np.int64)
+    sl[rows] = step.slots[rows]
+    oracle.append(wl.k_new, wl.v_new, wl.in_dtype, sl, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
+    oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.q_dtype, kp, vp, wl.kv_dtype,
+                        np.ascontiguousarray(step.tables[rows]), np.ascontiguousarray(step.seq_lens[rows]),
+                        wl.scale, wl.k_scale, wl.v_scale)
+
+
+def rows_bytes(step, rows) -> int:
+    wl = step.wl
+    ke = wl.kv_elem_bytes()
+    lens = step.seq_lens[rows].astype(np.int64)
+    kv = int(lens.sum()) * 2 * wl.Hkv * wl.D * ke
+    other = 2 * len(rows) * wl.Hq * wl.D * 2 + int(((lens + 15) // 16).sum()) * 4
+    app = int((step.slots[rows] >= 0).sum()) * 2 * wl.Hkv * wl.D * (2 + ke)
+    return kv + other + app
+
+
+def cpu_baseline(wl, step, budget_s=15.0):
+    import oracle
+    pools = (wl.k_pool.copy(), wl.v_pool.copy())
+    t = time.perf_counter()
+    oracle_rows_step(wl, step, np.array([0]), pools)
+    one = max(time.perf_counter() - t, 1e-3)
+    n = int(max(1, min(wl.S, budget_s / one)))
+    rows = np.arange(n)
+    t = time.perf_counter()
+    oracle_rows_step(wl, step, rows, pools)
+    dt = time.perf_counter() - t
+    return {"value": rows_bytes(step, rows) / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {wl.S} sequences of {wl.name} (all heads): their append + float64 decode, "
+                      f"{dt:.1f} s"}
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = workloads.NAMED[args.workload]()
+    step = DecodeStep(wl, device=dev, partition_tokens=args.partition)
+    nbytes = step_bytes(step)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    working_set = nbytes["total"]
+    flush = working_set < 4 * l2
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if flush else None
+
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    t_load0 = time.monotonic()
+    for i in range(K):
+        if flush:
+            flush_buf.zero_()
+        a, b, c = ev[i]
+        a.record(stream)
+        step.copy()
+        step.append()
+        b.record(stream)
+        step.decode()
+        c.record(stream)
+    torch.cuda.synchronize()
+    t_load1 = time.monotonic()
+    barrier()
+    if flush:
+        step_ms = [a.elapsed_time(c) for a, _, c in ev]
+        total_ms = sum(step_ms)
+    else:
+        total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
+    # extend the load window (same steps, untimed) if it was too short for clock samples
+    if sampler and t_load1 - t_load0 < 1.0:
+        t_ext = time.monotonic()
+        while time.monotonic() - t_ext < 1.5:
+            for _ in range(20):
+                step.run()
+            torch.cuda.synchronize()
+        t_load1 = time.monotonic()
+
+    tot_bytes, tot_s = aggregate(nbytes["total"] * K, total_ms / 1e3)
+    value = tot_bytes / tot_s / 1e9
+
+    # ---- end to end through the public API from pinned host buffers
+    h = {
+        "q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(), "v": step.v_new.cpu().pin_memory(),
+        "slots": step.d_slots.cpu().pin_memory(), "pairs": step.d_pairs.cpu().pin_memory(),
+        "tables": step.d_tables.cpu().pin_memory(), "lens": step.d_lens.cpu().pin_memory(),
+    }
+    d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_h.numel() * out_h.element_size()
+    Ke = max(1, min(K, 200))
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        if flush:
+            flush_buf.zero_()
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        if len(step.pairs):
+            from paged_kv_cache_10_gb300 import pagedkv as pk
+            pk.copy_blocks(step.k_cache, step.v_cache, step.desc, d["pairs"])
+        step.append(k=d["k"], v=d["v"], slots=d["slots"])
+        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"])
+        out_h.copy_(step.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if flush:
+        # the flushes are not part of the step: subtract their measured cost
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(Ke):
+            flush_buf.zero_()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms -= f0.elapsed_time(f1)
+    e2e_bytes, e2e_s = aggregate(nbytes["total"] * Ke, e2e_ms / 1e3)
+
+    from paged_kv_cache_10_gb300 import pagedkv as pk
+    assert pk.get_device_error() == 0, "device error word set during the benchmark"
+
+    if rank != 0:
+        return None
+    clocks = sampler.summary(t_load0, t_load1) if sampler else None
+    if sampler:
+        sampler.stop()
+    peak, peak_kind = measured_peaks()
+    dec_ms = statistics.mean(decode_ms)
+    achieved = nbytes["decode"] / (dec_ms / 1e3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    ms_per_step = total_ms / K
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "tokens_per_s": round(world * wl.S / (tot_s / K), 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"e4m3": "e4m3 KV, bf16 q"}.get(wl.kv_dtype, wl.kv_dtype) + ", fp32 accumulate",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D,
+            "block_size": wl.b, "kv_dtype": wl.kv_dtype, "num_blocks": wl.NB, "max_seq_len": step.max_seq_len,
+            "mean_seq_len": float(step.seq_lens.mean()), "partition_tokens": step.effective_partition(),
+            "cow_pairs": int(len(step.pairs)), "appended_tokens": int((step.slots >= 0).sum()),
+            "bytes_per_step": nbytes, "l2": ("flushed between steps (2x L2 write)" if flush else
+                                             f"inputs larger than L2 ({working_set / 2**20:.0f} MiB vs "
+                                             f"{l2 / 2**20:.0f} MiB), no flush"),
+            "parallelism": f"replicas x{world}",
+        },
+        "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": K * step.kernel_launches(),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "decode_kernel (+ merge_kernel when split)", "mean_launch_us": round(dec_ms * 1e3, 2),
+                     "algorithmic_bytes_per_launch": nbytes["decode"]},
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, step)
+    return line
+
+
+# ----------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.pagedkv import Allocator, apply_setup
+
+    oracle.build()
+    wl = workloads.NAMED[args.workload]()
+
+    class HostStep:  # the host bookkeeping of the step, through the C++ allocator
+        pass
+
+    st = HostStep()
+    st.wl = wl
+    a = Allocator(wl.NB, wl.b, wl.free_order)
+    apply_setup(a, wl.setup)
+    appending = np.full(wl.S, -1, np.int64)
+    appending[np.asarray(wl.step_seqs)] = np.asarray(wl.step_seqs)
+    st.slots, st.pairs = a.append_batch(appending)
+    st.tables, st.seq_lens = a.export(np.arange(wl.S), wl.max_blocks)
+    pools = (wl.k_pool.copy(), wl.v_pool.copy())
+    K, W = args.steps, args.warmup
+    # one sequence (all heads) per step, rotating through the batch
+    for i in range(W):
+        oracle_rows_step(wl, st, np.array([i % wl.S]), pools)
+    nbytes, t = 0, 0.0
+    for i in range(K):
+        rows = np.array([(W + i) % wl.S])
+        t0 = time.perf_counter()
+        oracle_rows_step(wl, st, rows, pools)
+        t += time.perf_counter() - t0
+        nbytes += rows_bytes(st, rows)
+    value = nbytes / t / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(1e3 * t / K, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv,
+                   "head_size": wl.D, "kv_dtype": wl.kv_dtype},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"one sequence of {wl.name} (all heads) per step, rotating: its append + "
+                                   f"float64 decode"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--partition", type=int, default=None, help="tokens per split-K partition (0 = auto)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

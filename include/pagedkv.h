@@ -1,0 +1,279 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 paged KV cache library (libpagedkv.so).
+ *
+ * The library implements the data-parallel hot path of PagedAttention
+ * decoding, as described by the web pages on vLLM's PagedAttention:
+ *
+ *  [P1] "vLLM 高性能大语言模型推理引擎深度技术评估与分布式架构展望", sections
+ *       "PagedAttention 内存管理与核心数据结构" (KV split into fixed-size
+ *       physical blocks), "逻辑块到物理块的映射转换" (block tables; the kernel
+ *       walks the physical-block mapping and gathers K/V in place), and
+ *       "束搜索与并行采样的三大调度原语" (fork / append with copy-on-write / free).
+ *  [P2] openEuler essay on vLLM, section "PagedAttention：把操作系统的分页搬上
+ *       GPU" (block table indirection; split of long contexts into
+ *       partitions, grid (heads, seqs, partitions)).
+ *  [P3] "vLLM：大语言模型推理与服务库", section 4.2 (physical block, block table,
+ *       block pool with an O(1) free list), 4.3 (allocate on demand when the
+ *       last block is full, then update the table and write the KV) and 4.4
+ *       (PagedAttention kernel: inputs q, k_cache, v_cache, block_tables,
+ *       context lengths; q.K -> softmax -> weighted sum of V; 16-byte
+ *       vectorised coalesced loads, shared-memory staging).
+ *  [P4] "vLLM 深度解析：从 PagedAttention 到生产部署", sections "PagedAttention
+ *       的解法" (block table example) and "Prefix Caching 与 Copy-on-Write".
+ *
+ * Conventions for every call below.
+ *  - Device pointers are CUDA global-memory addresses owned by the caller
+ *    (typically torch tensors).  The library never allocates or frees device
+ *    memory and keeps no pointer after a call returns.
+ *  - Every device pointer must be 16-byte aligned.
+ *  - GPU calls are asynchronous on the given stream (0 = legacy default
+ *    stream) and return after enqueueing; ordering between calls is the
+ *    stream order the caller chooses.
+ *  - Arguments are validated on the host before any launch: a bad shape,
+ *    size, null pointer or misalignment returns PKV_ERR_INVALID and launches
+ *    nothing; a valid but unimplemented combination returns
+ *    PKV_ERR_UNSUPPORTED.  A failed launch returns PKV_ERR_CUDA.
+ *  - Data-dependent errors found on the device (a block id outside the
+ *    pool, a slot outside the pool, a seq_len beyond the block table) never
+ *    trap: the kernel skips the offending access and ORs a bit into a device
+ *    error word that pkv_get_device_error() reads and clears.
+ *  - No C++ exception crosses this interface.
+ *
+ * KV pool layout (part of the ABI).  K and V are two separate pools, each
+ *     [num_blocks][num_kv_heads][block_size][head_size]
+ * row-major in the cache element type, so the (block, kv head) tile is one
+ * contiguous run of block_size*head_size elements (4 KiB for bf16 at
+ * head_size 128) and one token of one head is a contiguous head_size row.
+ * Token position t of a sequence lives in physical block
+ * block_tables[seq][t / block_size] at offset t % block_size.
+ * A slot is physical_block * block_size + offset.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,      /* bad argument; nothing launched / state unchanged */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (dtype, head_size, group) */
+    PKV_ERR_OOM = 3,          /* host allocator has no free block; state unchanged */
+    PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    PKV_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+    PKV_ERR_NOT_FOUND = 6     /* unknown sequence id (host allocator) */
+} pkv_status;
+
+typedef enum {
+    PKV_F16 = 0,       /* IEEE binary16 */
+    PKV_BF16 = 1,      /* bfloat16 */
+    PKV_FP8_E4M3 = 2   /* OCP E4M3FN, per-tensor scale: value = code * scale */
+} pkv_dtype;
+
+/* Bits of the device error word (pkv_get_device_error). */
+#define PKV_DEVERR_BLOCK_ID   0x1u  /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SEQ_LEN    0x2u  /* seq_len < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEVERR_SLOT       0x4u  /* slot >= num_blocks * block_size */
+#define PKV_DEVERR_COPY_PAIR  0x8u  /* copy pair id outside [0, num_blocks) */
+#define PKV_DEVERR_TIMEOUT    0x10u /* an internal pipeline wait gave up */
+
+/* Description of one KV pool pair (K pool and V pool share it). */
+typedef struct {
+    int32_t num_blocks;    /* NB >= 1 */
+    int32_t block_size;    /* b; only 16 is implemented */
+    int32_t num_kv_heads;  /* Hkv >= 1 */
+    int32_t head_size;     /* D; 64 or 128 */
+    int32_t kv_dtype;      /* pkv_dtype of the pool elements */
+    float k_scale;         /* fp8 only: stored key = code * k_scale (> 0); ignored otherwise */
+    float v_scale;         /* fp8 only: stored value = code * v_scale (> 0) */
+} pkv_cache_desc;
+
+/* ------------------------------------------------------------------ GPU */
+
+/*
+ * Slot-mapped append of this step's new keys and values into the paged pool
+ * ([P3] 4.3 step 2: allocate a block when the last is full -> update the
+ * block table -> write the KV; [P1] prefill/decode paragraph: each decode
+ * step appends the new token's KV vector).
+ *
+ * k, v: device [num_tokens][num_kv_heads][head_size] in in_dtype.  in_dtype
+ *   equals the cache dtype, or for an fp8 cache is PKV_BF16 or PKV_F16.
+ * slot_mapping: device int64 [num_tokens]; slot < 0 skips the token (padding).
+ *   Token t is written to block slot / b at offset slot % b of every KV
+ *   head.  For an fp8 cache each element is stored as the E4M3 code nearest
+ *   (ties to even, saturating at +-448) to binary32(x) / k_scale (v_scale).
+ *   Two tokens with the same slot race (which one lands is unspecified).
+ * k_cache, v_cache: device pools in the layout above, written in place.
+ * A slot >= num_blocks * b sets PKV_DEVERR_SLOT and that token is skipped.
+ * num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_paged_kv_append(const void* k, const void* v, int32_t in_dtype, int32_t num_tokens,
+                               const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                               const pkv_cache_desc* desc, void* stream);
+
+/*
+ * Block copy behind copy-on-write ([P4] "Prefix Caching 与 Copy-on-Write":
+ * a block shared by several sequences is copied only when one of them is
+ * about to modify it; [P1] append primitive).
+ *
+ * pairs: device int32 [num_pairs][2] = (src, dst).  Every byte of K[src]
+ *   and V[src] (all KV heads, all b slots) is copied to K[dst] and V[dst].
+ *   The dst ids must be distinct and no dst may be a src of another pair
+ *   (the host allocator only produces such sets); otherwise the result is
+ *   unspecified.  An id outside [0, num_blocks) sets PKV_DEVERR_COPY_PAIR
+ *   and skips the pair.  Enqueue before pkv_paged_kv_append of the same
+ *   step so the appended token lands in the private copy.
+ * num_pairs == 0 is a no-op.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* desc,
+                           const int32_t* pairs, int32_t num_pairs, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_attention_decode needs for these sizes
+ * (split-K partials: per (seq, query head, partition) a running max, a sum
+ * and a normalised head_size-vector, all fp32).  partition_tokens = 0 asks
+ * for the size the automatic choice can need (its largest case).
+ * Returns 0 on invalid sizes.
+ */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                  int32_t max_seq_len, int32_t partition_tokens);
+
+/*
+ * Decode (single-query) attention over the paged pool ([P3] 4.4: inputs q,
+ * k_cache, v_cache, block_tables, context lengths; per query walk the block
+ * table, q.K -> softmax -> weighted sum of V; [P1] "逻辑块到物理块的映射转换"
+ * step 4; [P2] partitions of long contexts).
+ *
+ * For every sequence s and query head i (KV head h = i / (num_q_heads /
+ * num_kv_heads)):
+ *     out[s][i] = sum_{t < seq_lens[s]} softmax_t(scale * q[s][i] . K_t) V_t
+ * with K_t, V_t read from block block_tables[s][t / b], offset t % b, head h
+ * (for fp8 pools multiplied by k_scale / v_scale).  Accumulation is fp32;
+ * out is rounded once to q_dtype.  seq_lens[s] == 0 gives a zero row.
+ *
+ * q: device [num_seqs][num_q_heads][head_size] in q_dtype (PKV_F16 or
+ *   PKV_BF16; for f16/bf16 pools it must equal the pool dtype).
+ * block_tables: device int32 [num_seqs][max_blocks_per_seq]; entries past a
+ *   sequence's last block are never read.
+ * seq_lens: device int32 [num_seqs]; max_seq_len (host) must be >= every
+ *   entry (it sizes the launch).  An entry that is negative or beyond
+ *   min(max_blocks_per_seq * b, max_seq_len rounded up to whole partitions)
+ *   sets PKV_DEVERR_SEQ_LEN and is clamped into that range.
+ * out: device [num_seqs][num_q_heads][head_size] in q_dtype.
+ * partition_tokens: tokens per split-K partition (a positive multiple of
+ *   the block size), or 0 to let the library choose from the sizes and the
+ *   SM count.  When a sequence spans more than one partition its partials go
+ *   to the workspace and a log-sum-exp merge kernel finishes the row.
+ * workspace: device buffer of at least
+ *   pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_size,
+ *   max_seq_len, partition_tokens) bytes (may be NULL when that is 0);
+ *   otherwise PKV_ERR_WORKSPACE.
+ * Implemented: block_size 16; head_size 64 or 128; num_q_heads / num_kv_heads
+ *   in {1, 2, 4, 8}; pools f16, bf16 or fp8 E4M3.
+ */
+pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t num_seqs,
+                                      int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                      const pkv_cache_desc* desc, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                      int32_t max_seq_len, float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t partition_tokens, void* stream);
+
+/*
+ * Partition size the automatic choice (partition_tokens = 0) would use for
+ * these sizes on the current device, or a negative pkv_status on error.
+ */
+int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_size, int32_t max_seq_len);
+
+/*
+ * Reads and clears the device error word of the current device (the OR of
+ * PKV_DEVERR_* bits set by every kernel since the last call).  Synchronises
+ * the given stream first.  *flags receives the bits.
+ */
+pkv_status pkv_get_device_error(uint32_t* flags, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* pkv_status_string(int32_t status);
+
+/* Library version, "major.minor.patch". */
+const char* pkv_version(void);
+
+/* -------------------------------------------------------- host allocator */
+
+/*
+ * Host-side block allocator: plain C++, host memory only (it hands out block
+ * ids; the caller owns the device pool they index).
+ *
+ * [P3] 4.2 "Block Pool": a pool split into fixed-size blocks, a free list,
+ *   O(1) allocate (take the last free id; fail when empty) and O(1) free.
+ * [P3] 4.3: a sequence gets a new block only when its last block is full.
+ * [P1] "束搜索与并行采样的三大调度原语": fork copies the parent's block table
+ *   (same physical ids, reference count +1); append on a shared block uses
+ *   copy-on-write; free decrements reference counts and returns blocks
+ *   whose count reaches zero to the free list at once.
+ * [P4] "Prefix Caching 与 Copy-on-Write": shared blocks carry a reference
+ *   count > 1 and are copied only when modified.
+ *
+ * Readings: the free list is a stack; copy-on-write happens when the block
+ * the next token goes to is partial AND shared; a sequence's blocks are
+ * released last block first.  Every call either succeeds completely or
+ * returns an error with the allocator unchanged.  The handle is not
+ * thread-safe: one thread at a time per handle.
+ */
+typedef struct pkv_alloc pkv_alloc;
+
+/* free_order: NULL (ids 0..num_blocks-1, so block num_blocks-1 is taken
+ * first) or a permutation of 0..num_blocks-1 whose LAST entry is taken
+ * first.  Returns NULL on invalid arguments. */
+pkv_alloc* pkv_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order);
+void pkv_alloc_destroy(pkv_alloc* a);
+
+/* New sequence holding num_tokens >= 0 tokens (ceil(num_tokens / b) blocks). */
+pkv_status pkv_alloc_seq_new(pkv_alloc* a, int64_t seq_id, int32_t num_tokens);
+/* child gets parent's table and length; every block's count +1. */
+pkv_status pkv_alloc_fork(pkv_alloc* a, int64_t parent_id, int64_t child_id);
+/* Reserve the slot for one more token of seq_id.  *slot receives it.  When
+ * the token would go into a partial block shared with another sequence, a
+ * private block is allocated, the table is repointed, and (*cow_src,
+ * *cow_dst) receive the pair to pass to pkv_copy_blocks; otherwise both are
+ * -1.  cow_src / cow_dst may be NULL only if the caller does not care. */
+pkv_status pkv_alloc_append_slot(pkv_alloc* a, int64_t seq_id, int64_t* slot, int32_t* cow_src,
+                                 int32_t* cow_dst);
+/* Grow seq_id by num_tokens tokens without returning slots (prefill of new
+ * tokens).  PKV_ERR_INVALID if that would write into a shared partial block. */
+pkv_status pkv_alloc_seq_extend(pkv_alloc* a, int64_t seq_id, int32_t num_tokens);
+/* Release every block of seq_id and forget it. */
+pkv_status pkv_alloc_free(pkv_alloc* a, int64_t seq_id);
+
+/* One decode step for a batch: append_slot for seq_ids[0..n) in order.
+ * slots[i] receives row i's slot (or -1 where seq_ids[i] < 0: padding row);
+ * pairs receives the copy-on-write pairs ([*num_pairs][2], capacity
+ * pairs_cap >= n).  All or nothing: on any error the allocator is restored
+ * to its state before the call. */
+pkv_status pkv_alloc_append_batch(pkv_alloc* a, const int64_t* seq_ids, int32_t n, int64_t* slots,
+                                  int32_t* pairs, int32_t pairs_cap, int32_t* num_pairs);
+/* Export padded block tables and lengths for a batch: tables is
+ * [n][max_blocks] (unused entries -1), seq_lens [n]; a row whose seq_id is
+ * negative gets length 0.  PKV_ERR_INVALID if a table does not fit. */
+pkv_status pkv_alloc_export(const pkv_alloc* a, const int64_t* seq_ids, int32_t n, int32_t* tables,
+                            int32_t max_blocks, int32_t* seq_lens);
+
+pkv_status pkv_alloc_block_table(const pkv_alloc* a, int64_t seq_id, int32_t* out, int32_t cap,
+                                 int32_t* n);
+pkv_status pkv_alloc_seq_len(const pkv_alloc* a, int64_t seq_id, int64_t* n);
+/* Reference count of a block (0 = free), or -1 for an id outside the pool. */
+int32_t pkv_alloc_refcount(const pkv_alloc* a, int32_t block);
+int32_t pkv_alloc_num_free(const pkv_alloc* a);
+int32_t pkv_alloc_num_seqs(const pkv_alloc* a);
+/* Fault injection for tests: the k-th block allocation from now (k >= 1)
+ * fails as if the pool were empty; k <= 0 disables. */
+void pkv_alloc_fail_after(pkv_alloc* a, int64_t k);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

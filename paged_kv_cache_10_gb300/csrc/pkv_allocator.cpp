@@ -1,0 +1,321 @@
+// pkv_allocator.cpp -- host block allocator (free list, reference counts,
+// fork / append with copy-on-write / free).  Host memory only.
+//
+// "vLLM：大语言模型推理与服务库" section 4.2 ("Block Pool"): the pool is split
+// into fixed-size blocks tracked by a free list; allocation takes the last
+// free id in O(1) and fails when none is left; freeing pushes the id back.
+// Section 4.3: a sequence receives a block only when its last block is full.
+// "vLLM 高性能大语言模型推理引擎深度技术评估与分布式架构展望", section
+// "束搜索与并行采样的三大调度原语": fork shares the parent's physical blocks;
+// append gives the writer a private copy of a shared block (copy-on-write);
+// free drops reference counts and returns zero-count blocks immediately.
+// "vLLM 深度解析：从 PagedAttention 到生产部署", "Prefix Caching 与
+// Copy-on-Write": shared blocks have reference count > 1 and are copied only
+// when modified.
+//
+// Every public call is all-or-nothing: failures leave the state unchanged
+// (OOM returns a status instead of throwing).
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pagedkv.h"
+
+namespace {
+
+struct Seq {
+    std::vector<int32_t> blocks;
+    int64_t len = 0;
+};
+
+}  // namespace
+
+struct pkv_alloc {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    std::vector<int32_t> free_stack;  // allocation pops the back
+    std::vector<int32_t> ref;
+    std::unordered_map<int64_t, Seq> seqs;
+    int64_t fail_countdown = 0;  // >0: the fail_countdown-th allocation fails
+
+    bool can_take() {
+        if (fail_countdown > 0) {
+            if (fail_countdown == 1) {
+                fail_countdown = 0;
+                return false;
+            }
+        }
+        return !free_stack.empty();
+    }
+    // Only call after can_take() returned true.
+    int32_t take() {
+        if (fail_countdown > 0) --fail_countdown;
+        int32_t id = free_stack.back();
+        free_stack.pop_back();
+        ref[id] = 1;
+        return id;
+    }
+    // Exact inverse of take() for rollback.
+    void untake(int32_t id) {
+        ref[id] = 0;
+        free_stack.push_back(id);
+    }
+    void release(int32_t id) {
+        if (--ref[id] == 0) free_stack.push_back(id);
+    }
+};
+
+namespace {
+
+// Record of one append_slot, enough to undo it exactly.
+struct AppendUndo {
+    int64_t seq;
+    int kind;  // 0: wrote in place, 1: took a fresh block, 2: copy-on-write
+    int32_t src, dst;
+};
+
+pkv_status append_one(pkv_alloc* a, int64_t seq_id, int64_t* slot, int32_t* cs, int32_t* cd,
+                      AppendUndo* undo) {
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    Seq& s = it->second;
+    const int64_t pos = s.len;
+    const int32_t off = static_cast<int32_t>(pos % a->block_size);
+    int32_t src = -1, dst = -1;
+    int kind = 0;
+    if (off == 0) {
+        if (!a->can_take()) return PKV_ERR_OOM;
+        s.blocks.push_back(a->take());
+        kind = 1;
+    } else {
+        const int32_t last = s.blocks.back();
+        if (a->ref[last] > 1) {
+            if (!a->can_take()) return PKV_ERR_OOM;
+            dst = a->take();
+            a->ref[last] -= 1;
+            s.blocks.back() = dst;
+            src = last;
+            kind = 2;
+        }
+    }
+    s.len = pos + 1;
+    *slot = static_cast<int64_t>(s.blocks.back()) * a->block_size + off;
+    if (cs) *cs = src;
+    if (cd) *cd = dst;
+    if (undo) *undo = AppendUndo{seq_id, kind, src, dst};
+    return PKV_OK;
+}
+
+void undo_append(pkv_alloc* a, const AppendUndo& u) {
+    Seq& s = a->seqs[u.seq];
+    s.len -= 1;
+    if (u.kind == 1) {
+        a->untake(s.blocks.back());
+        s.blocks.pop_back();
+    } else if (u.kind == 2) {
+        s.blocks.back() = u.src;
+        a->ref[u.src] += 1;
+        a->untake(u.dst);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_alloc* pkv_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order) {
+    if (num_blocks <= 0 || block_size <= 0) return nullptr;
+    pkv_alloc* a = new (std::nothrow) pkv_alloc();
+    if (!a) return nullptr;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ref.assign(num_blocks, 0);
+    a->free_stack.resize(num_blocks);
+    if (free_order) {
+        std::vector<char> seen(num_blocks, 0);
+        for (int32_t i = 0; i < num_blocks; ++i) {
+            int32_t id = free_order[i];
+            if (id < 0 || id >= num_blocks || seen[id]) {
+                delete a;
+                return nullptr;
+            }
+            seen[id] = 1;
+            a->free_stack[i] = id;
+        }
+    } else {
+        for (int32_t i = 0; i < num_blocks; ++i) a->free_stack[i] = i;
+    }
+    return a;
+}
+
+void pkv_alloc_destroy(pkv_alloc* a) { delete a; }
+
+pkv_status pkv_alloc_seq_new(pkv_alloc* a, int64_t seq_id, int32_t num_tokens) {
+    if (!a || num_tokens < 0) return PKV_ERR_INVALID;
+    if (a->seqs.count(seq_id)) return PKV_ERR_INVALID;
+    const int64_t need = (static_cast<int64_t>(num_tokens) + a->block_size - 1) / a->block_size;
+    if (need > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+    Seq s;
+    s.blocks.reserve(need);
+    for (int64_t i = 0; i < need; ++i) {
+        if (!a->can_take()) {
+            for (auto it = s.blocks.rbegin(); it != s.blocks.rend(); ++it) a->untake(*it);
+            return PKV_ERR_OOM;
+        }
+        s.blocks.push_back(a->take());
+    }
+    s.len = num_tokens;
+    a->seqs.emplace(seq_id, std::move(s));
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_fork(pkv_alloc* a, int64_t parent_id, int64_t child_id) {
+    if (!a) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(parent_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    if (a->seqs.count(child_id)) return PKV_ERR_INVALID;
+    Seq child = it->second;
+    for (int32_t id : child.blocks) a->ref[id] += 1;
+    a->seqs.emplace(child_id, std::move(child));
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_append_slot(pkv_alloc* a, int64_t seq_id, int64_t* slot, int32_t* cow_src,
+                                 int32_t* cow_dst) {
+    if (!a || !slot) return PKV_ERR_INVALID;
+    return append_one(a, seq_id, slot, cow_src, cow_dst, nullptr);
+}
+
+pkv_status pkv_alloc_seq_extend(pkv_alloc* a, int64_t seq_id, int32_t num_tokens) {
+    if (!a || num_tokens < 0) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    Seq& s = it->second;
+    if (num_tokens == 0) return PKV_OK;
+    if (s.len % a->block_size != 0 && a->ref[s.blocks.back()] > 1) return PKV_ERR_INVALID;
+    const int64_t have = static_cast<int64_t>(s.blocks.size());
+    const int64_t need = (s.len + num_tokens + a->block_size - 1) / a->block_size - have;
+    if (need > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+    for (int64_t i = 0; i < need; ++i) {
+        if (!a->can_take()) {
+            while (static_cast<int64_t>(s.blocks.size()) > have) {
+                a->untake(s.blocks.back());
+                s.blocks.pop_back();
+            }
+            return PKV_ERR_OOM;
+        }
+        s.blocks.push_back(a->take());
+    }
+    s.len += num_tokens;
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_free(pkv_alloc* a, int64_t seq_id) {
+    if (!a) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    const std::vector<int32_t>& bl = it->second.blocks;
+    for (auto r = bl.rbegin(); r != bl.rend(); ++r) a->release(*r);
+    a->seqs.erase(it);
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_append_batch(pkv_alloc* a, const int64_t* seq_ids, int32_t n, int64_t* slots,
+                                  int32_t* pairs, int32_t pairs_cap, int32_t* num_pairs) {
+    if (!a || n < 0 || (n > 0 && (!seq_ids || !slots)) || !num_pairs) return PKV_ERR_INVALID;
+    if (pairs_cap < n || (n > 0 && !pairs)) return PKV_ERR_INVALID;
+    // A sequence may appear at most once per batch.
+    {
+        std::unordered_map<int64_t, int> seen;
+        for (int32_t i = 0; i < n; ++i)
+            if (seq_ids[i] >= 0 && seen[seq_ids[i]]++) return PKV_ERR_INVALID;
+    }
+    std::vector<AppendUndo> undo;
+    undo.reserve(n);
+    int32_t np = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        if (seq_ids[i] < 0) {
+            slots[i] = -1;
+            continue;
+        }
+        int32_t cs = -1, cd = -1;
+        AppendUndo u{};
+        pkv_status st = append_one(a, seq_ids[i], &slots[i], &cs, &cd, &u);
+        if (st != PKV_OK) {
+            for (auto r = undo.rbegin(); r != undo.rend(); ++r) undo_append(a, *r);
+            return st;
+        }
+        undo.push_back(u);
+        if (cs >= 0) {
+            pairs[2 * np] = cs;
+            pairs[2 * np + 1] = cd;
+            ++np;
+        }
+    }
+    *num_pairs = np;
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_export(const pkv_alloc* a, const int64_t* seq_ids, int32_t n, int32_t* tables,
+                            int32_t max_blocks, int32_t* seq_lens) {
+    if (!a || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !tables || !seq_lens)))
+        return PKV_ERR_INVALID;
+    for (int32_t i = 0; i < n; ++i) {
+        if (seq_ids[i] < 0) continue;
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+        if (static_cast<int64_t>(it->second.blocks.size()) > max_blocks) return PKV_ERR_INVALID;
+        if (it->second.len > INT32_MAX) return PKV_ERR_INVALID;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
+        for (int32_t j = 0; j < max_blocks; ++j) row[j] = -1;
+        seq_lens[i] = 0;
+        if (seq_ids[i] < 0) continue;
+        const Seq& s = a->seqs.find(seq_ids[i])->second;
+        std::memcpy(row, s.blocks.data(), s.blocks.size() * sizeof(int32_t));
+        seq_lens[i] = static_cast<int32_t>(s.len);
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_block_table(const pkv_alloc* a, int64_t seq_id, int32_t* out, int32_t cap,
+                                 int32_t* n) {
+    if (!a || !n || cap < 0) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    const auto& bl = it->second.blocks;
+    *n = static_cast<int32_t>(bl.size());
+    if (static_cast<int64_t>(bl.size()) > cap || (!out && !bl.empty())) return PKV_ERR_INVALID;
+    if (!bl.empty()) std::memcpy(out, bl.data(), bl.size() * sizeof(int32_t));
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_seq_len(const pkv_alloc* a, int64_t seq_id, int64_t* n) {
+    if (!a || !n) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    *n = it->second.len;
+    return PKV_OK;
+}
+
+int32_t pkv_alloc_refcount(const pkv_alloc* a, int32_t block) {
+    if (!a || block < 0 || block >= a->num_blocks) return -1;
+    return a->ref[block];
+}
+
+int32_t pkv_alloc_num_free(const pkv_alloc* a) {
+    return a ? static_cast<int32_t>(a->free_stack.size()) : -1;
+}
+
+int32_t pkv_alloc_num_seqs(const pkv_alloc* a) {
+    return a ? static_cast<int32_t>(a->seqs.size()) : -1;
+}
+
+void pkv_alloc_fail_after(pkv_alloc* a, int64_t k) {
+    if (a) a->fail_countdown = k > 0 ? k : 0;
+}
+
+}  // extern "C"

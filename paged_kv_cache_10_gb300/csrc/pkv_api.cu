@@ -1,0 +1,221 @@
+// pkv_api.cu -- C ABI entry points for decode attention, the device error
+// word, status strings.  Argument meaning, layout, ownership and error
+// behaviour are specified in include/pagedkv.h.
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_decode_impl.cuh"
+
+namespace pkv {
+
+// Device error word: the OR of PKV_DEVERR_* bits reported by the kernels.
+__device__ unsigned int g_device_error = 0;
+
+unsigned int* error_word() {
+    static unsigned int* ptrs[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned int*>(p);
+    }
+    return ptrs[dev];
+}
+
+cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st) {
+    const int64_t rows = static_cast<int64_t>(p.S) * p.Hq;
+    const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
+    if (q_dtype == PKV_BF16) {
+        if (p.D == 128)
+            merge_kernel<128, BF16><<<grid, 256, 0, st>>>(p);
+        else
+            merge_kernel<64, BF16><<<grid, 256, 0, st>>>(p);
+    } else {
+        if (p.D == 128)
+            merge_kernel<128, F16><<<grid, 256, 0, st>>>(p);
+        else
+            merge_kernel<64, F16><<<grid, 256, 0, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+int num_sms() {
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+// Smallest partition the automatic choice uses (sizes the P = 0 workspace).
+constexpr int kAutoMinPartition = 256;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tokens per split-K partition when the caller passes 0.  Enough CTAs for a
+// few waves of resident CTAs keep the SMs evenly loaded when sequence
+// lengths differ; beyond that, splitting only adds partial-result traffic.
+int auto_partition(int S, int Hkv, int max_seq_len) {
+    const int64_t units = static_cast<int64_t>(S) * Hkv;
+    const int64_t want = static_cast<int64_t>(num_sms()) * 2 * 4;
+    int64_t parts = ceil_div(want, units > 0 ? units : 1);
+    if (parts < 1) parts = 1;
+    int64_t P = ceil_div(ceil_div(max_seq_len > 0 ? max_seq_len : 1, parts), kBlockSize) * kBlockSize;
+    if (P < kAutoMinPartition) P = kAutoMinPartition;
+    return static_cast<int>(P);
+}
+
+size_t workspace_bytes(int64_t S, int64_t Hq, int64_t D, int64_t max_seq_len, int64_t P) {
+    const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
+    if (NP <= 1) return 0;
+    // m, l and o rows, each region 256-byte aligned
+    const int64_t rows = S * Hq * NP;
+    const int64_t ml = ceil_div(rows * 4, 256) * 256;
+    return static_cast<size_t>(2 * ml + rows * D * 4);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                             int32_t max_seq_len, int32_t partition_tokens) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_seq_len < 0 || partition_tokens < 0)
+        return 0;
+    if (partition_tokens % kBlockSize) return 0;
+    const int64_t P = partition_tokens > 0 ? partition_tokens : kAutoMinPartition;
+    return workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len, P);
+}
+
+extern "C" int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                             int32_t head_size, int32_t max_seq_len) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_size <= 0 || max_seq_len < 0)
+        return -static_cast<int32_t>(PKV_ERR_INVALID);
+    return auto_partition(num_seqs, num_kv_heads, max_seq_len);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t num_seqs,
+                                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                                 const pkv_cache_desc* d, const int32_t* block_tables,
+                                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                                 int32_t max_seq_len, float scale, void* out, void* workspace,
+                                                 size_t ws_bytes, int32_t partition_tokens, void* stream) {
+    // ---- validation (host, before any launch)
+    if (!d || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        partition_tokens < 0)
+        return PKV_ERR_INVALID;
+    if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->head_size <= 0 || d->block_size <= 0)
+        return PKV_ERR_INVALID;
+    if (d->kv_dtype < PKV_F16 || d->kv_dtype > PKV_FP8_E4M3) return PKV_ERR_INVALID;
+    if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return PKV_ERR_INVALID;
+    if (num_q_heads % d->num_kv_heads) return PKV_ERR_INVALID;
+    if (!(scale == scale)) return PKV_ERR_INVALID;
+    if (d->kv_dtype == PKV_FP8_E4M3 && !(d->k_scale > 0.f && d->v_scale > 0.f)) return PKV_ERR_INVALID;
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * d->block_size)
+        return PKV_ERR_INVALID;
+    if (partition_tokens % kBlockSize) return PKV_ERR_INVALID;
+    if (d->kv_dtype != PKV_FP8_E4M3 && q_dtype != d->kv_dtype) return PKV_ERR_UNSUPPORTED;
+    if (d->block_size != kBlockSize || (d->head_size != 64 && d->head_size != 128)) return PKV_ERR_UNSUPPORTED;
+    const int G = num_q_heads / d->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || d->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PKV_ERR_INVALID;
+
+    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len);
+    const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
+    if (NP > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    const size_t need = workspace_bytes(num_seqs, num_q_heads, d->head_size, max_seq_len, P);
+    if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
+
+    unsigned int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+
+    DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.S = num_seqs;
+    p.Hq = num_q_heads;
+    p.Hkv = d->num_kv_heads;
+    p.D = d->head_size;
+    p.NB = d->num_blocks;
+    p.MB = max_blocks_per_seq;
+    p.P = P;
+    p.NP = static_cast<int32_t>(NP);
+    const float log2e = 1.4426950408889634f;
+    p.qk_scale = scale * log2e * (d->kv_dtype == PKV_FP8_E4M3 ? d->k_scale : 1.f);
+    p.v_scale = d->kv_dtype == PKV_FP8_E4M3 ? d->v_scale : 1.f;
+    p.err = err;
+    if (need > 0) {
+        const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads * NP;
+        const int64_t ml = ceil_div(rows * 4, 256) * 256;
+        unsigned char* w = static_cast<unsigned char*>(workspace);
+        p.part_m = reinterpret_cast<float*>(w);
+        p.part_l = reinterpret_cast<float*>(w + ml);
+        p.part_o = reinterpret_cast<float*>(w + 2 * ml);
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (d->kv_dtype == PKV_F16)
+        e = launch_decode_f16(p, G, st);
+    else if (d->kv_dtype == PKV_BF16)
+        e = launch_decode_bf16(p, G, st);
+    else if (q_dtype == PKV_BF16)
+        e = launch_decode_fp8_bf16q(p, G, st);
+    else
+        e = launch_decode_fp8_f16q(p, G, st);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    if (NP > 1) {
+        e = launch_merge(p, q_dtype, st);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+extern "C" pkv_status pkv_get_device_error(uint32_t* flags, void* stream) {
+    if (!flags) return PKV_ERR_INVALID;
+    unsigned int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(err, 0, sizeof(unsigned int), st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PKV_ERR_CUDA;
+    *flags = v;
+    return PKV_OK;
+}
+
+extern "C" const char* pkv_status_string(int32_t status) {
+    switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported combination";
+    case PKV_ERR_OOM: return "out of blocks";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_NOT_FOUND: return "unknown sequence";
+    default: return "unknown status";
+    }
+}
+
+extern "C" const char* pkv_version(void) { return "0.1.0"; }

@@ -1,0 +1,12 @@
+// pkv_decode_fp8.cu -- decode attention instantiations for fp8 E4M3 pools
+// (bf16 or f16 q).
+#include "pkv_decode_impl.cuh"
+
+namespace pkv {
+cudaError_t launch_decode_fp8_bf16q(const DecodeParams& p, int G, cudaStream_t st) {
+    return launch_decode_family<E4M3, BF16>(p, G, st);
+}
+cudaError_t launch_decode_fp8_f16q(const DecodeParams& p, int G, cudaStream_t st) {
+    return launch_decode_family<E4M3, F16>(p, G, st);
+}
+}  // namespace pkv

@@ -1,0 +1,326 @@
+"""ctypes binding of ``libpagedkv.so`` (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels or its C++ allocator;
+this module converts torch tensors to pointers, picks the stream and turns
+status codes into exceptions.  It never falls back to another
+implementation: if the library is missing it raises.
+
+Names follow the C ABI in ``include/pagedkv.h`` without the ``pkv_`` prefix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_WORKSPACE, ERR_NOT_FOUND = range(7)
+F16, BF16, FP8_E4M3 = 0, 1, 2
+DTYPE_CODE = {"f16": F16, "bf16": BF16, "e4m3": FP8_E4M3}
+DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+EXPORTED = [
+    "pkv_paged_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
+    "pkv_paged_attention_decode", "pkv_decode_auto_partition", "pkv_get_device_error",
+    "pkv_status_string", "pkv_version", "pkv_alloc_create", "pkv_alloc_destroy",
+    "pkv_alloc_seq_new", "pkv_alloc_fork", "pkv_alloc_append_slot", "pkv_alloc_seq_extend",
+    "pkv_alloc_free", "pkv_alloc_append_batch", "pkv_alloc_export", "pkv_alloc_block_table",
+    "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
+    "pkv_alloc_fail_after",
+]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+class OutOfBlocks(PagedKVError):
+    pass
+
+
+class _CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
+
+
+@dataclass
+class CacheDesc:
+    num_blocks: int
+    num_kv_heads: int
+    head_size: int
+    kv_dtype: str = "bf16"
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    block_size: int = 16
+
+    def c(self) -> _CacheDesc:
+        return _CacheDesc(self.num_blocks, self.block_size, self.num_kv_heads, self.head_size,
+                          DTYPE_CODE[self.kv_dtype], self.k_scale, self.v_scale)
+
+
+_lib = None
+
+
+def lib():
+    """Loads the library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with paged_kv_cache_10_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, u32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint32)
+    D = ctypes.POINTER(_CacheDesc)
+    sig = {
+        "pkv_paged_kv_append": (i32, [P, P, i32, i32, P, P, P, D, P]),
+        "pkv_copy_blocks": (i32, [P, P, D, P, i32, P]),
+        "pkv_decode_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32]),
+        "pkv_paged_attention_decode": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, ctypes.c_float,
+                                             P, P, ctypes.c_size_t, i32, P]),
+        "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32]),
+        "pkv_get_device_error": (i32, [u32p, P]),
+        "pkv_status_string": (ctypes.c_char_p, [i32]),
+        "pkv_version": (ctypes.c_char_p, []),
+        "pkv_alloc_create": (P, [i32, i32, P]),
+        "pkv_alloc_destroy": (None, [P]),
+        "pkv_alloc_seq_new": (i32, [P, i64, i32]),
+        "pkv_alloc_fork": (i32, [P, i64, i64]),
+        "pkv_alloc_append_slot": (i32, [P, i64, P, P, P]),
+        "pkv_alloc_seq_extend": (i32, [P, i64, i32]),
+        "pkv_alloc_free": (i32, [P, i64]),
+        "pkv_alloc_append_batch": (i32, [P, P, i32, P, P, i32, P]),
+        "pkv_alloc_export": (i32, [P, P, i32, P, i32, P]),
+        "pkv_alloc_block_table": (i32, [P, i64, P, i32, P]),
+        "pkv_alloc_seq_len": (i32, [P, i64, P]),
+        "pkv_alloc_refcount": (i32, [P, i32]),
+        "pkv_alloc_num_free": (i32, [P]),
+        "pkv_alloc_num_seqs": (i32, [P]),
+        "pkv_alloc_fail_after": (None, [P, i64]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return lib().pkv_version().decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status == ERR_OOM:
+        raise OutOfBlocks(status, what)
+    if status != OK:
+        raise PagedKVError(status, what)
+
+
+def _dev_ptr(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+_TORCH_CODE = {torch.float16: F16, torch.bfloat16: BF16}
+
+
+def _dtype_code(t: torch.Tensor, declared: str | None) -> int:
+    if declared is not None:
+        return DTYPE_CODE[declared]
+    if t.dtype not in _TORCH_CODE:
+        raise TypeError(f"cannot infer element type from {t.dtype}; pass it explicitly")
+    return _TORCH_CODE[t.dtype]
+
+
+# ------------------------------------------------------------------- GPU ops
+def paged_kv_append(k, v, slot_mapping, k_cache, v_cache, desc: CacheDesc, in_dtype: str | None = None,
+                    stream=None) -> None:
+    """k, v: [T, Hkv, D]; slot_mapping: int64 [T] (device)."""
+    T = int(slot_mapping.shape[0])
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    st = lib().pkv_paged_kv_append(_dev_ptr(k, "k"), _dev_ptr(v, "v"), _dtype_code(k, in_dtype), T,
+                                   _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(k_cache, "k_cache"),
+                                   _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()), _stream(stream))
+    _check(st, "paged_kv_append")
+
+
+def copy_blocks(k_cache, v_cache, desc: CacheDesc, pairs, num_pairs: int | None = None, stream=None) -> None:
+    """pairs: int32 [n, 2] (device) of (src, dst)."""
+    n = int(pairs.shape[0]) if num_pairs is None else int(num_pairs)
+    if pairs.dtype != torch.int32:
+        raise TypeError("pairs must be int32")
+    st = lib().pkv_copy_blocks(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
+                               _dev_ptr(pairs, "pairs") if n > 0 else None, n, _stream(stream))
+    _check(st, "copy_blocks")
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: int, max_seq_len: int,
+                           partition_tokens: int = 0) -> int:
+    return int(lib().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len, partition_tokens))
+
+
+def decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len) -> int:
+    r = int(lib().pkv_decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len))
+    if r < 0:
+        _check(-r, "decode_auto_partition")
+    return r
+
+
+def paged_attention_decode(q, k_cache, v_cache, desc: CacheDesc, block_tables, seq_lens, max_seq_len: int,
+                           scale: float, out, workspace=None, partition_tokens: int = 0,
+                           q_dtype: str | None = None, stream=None) -> None:
+    """q, out: [S, Hq, D]; block_tables: int32 [S, MB]; seq_lens: int32 [S] (device)."""
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = lib().pkv_paged_attention_decode(_dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
+                                          _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+                                          ctypes.byref(desc.c()), _dev_ptr(block_tables, "block_tables"),
+                                          int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
+                                          int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes,
+                                          int(partition_tokens), _stream(stream))
+    _check(st, "paged_attention_decode")
+
+
+def get_device_error(stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib().pkv_get_device_error(ctypes.byref(flags), _stream(stream)), "get_device_error")
+    return int(flags.value)
+
+
+# ------------------------------------------------------------ host allocator
+def _np_ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Allocator:
+    """Host block allocator (C++): free list, reference counts, fork / append
+    with copy-on-write / free."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16, free_order=None):
+        self._order = None
+        ptr = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            ptr = _np_ptr(self._order)
+        self._h = lib().pkv_alloc_create(int(num_blocks), int(block_size), ptr)
+        if not self._h:
+            raise PagedKVError(ERR_INVALID, "alloc_create")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if self._h:
+            lib().pkv_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def seq_new(self, seq: int, num_tokens: int) -> None:
+        _check(lib().pkv_alloc_seq_new(self._h, seq, num_tokens), "alloc_seq_new")
+
+    def fork(self, parent: int, child: int) -> None:
+        _check(lib().pkv_alloc_fork(self._h, parent, child), "alloc_fork")
+
+    def append_slot(self, seq: int):
+        slot, cs, cd = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pkv_alloc_append_slot(self._h, seq, ctypes.byref(slot), ctypes.byref(cs), ctypes.byref(cd)),
+               "alloc_append_slot")
+        return slot.value, (None if cs.value < 0 else (cs.value, cd.value))
+
+    def extend(self, seq: int, num_tokens: int) -> None:
+        _check(lib().pkv_alloc_seq_extend(self._h, seq, num_tokens), "alloc_seq_extend")
+
+    def free(self, seq: int) -> None:
+        _check(lib().pkv_alloc_free(self._h, seq), "alloc_free")
+
+    def append_batch(self, seq_ids):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        slots = np.empty(n, np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int32)
+        npairs = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_append_batch(self._h, _np_ptr(ids), n, _np_ptr(slots), _np_ptr(pairs), max(n, 1),
+                                            ctypes.byref(npairs)), "alloc_append_batch")
+        return slots, pairs[: npairs.value].copy()
+
+    def export(self, seq_ids, max_blocks: int):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        tables = np.empty((n, max_blocks), np.int32)
+        lens = np.empty(n, np.int32)
+        _check(lib().pkv_alloc_export(self._h, _np_ptr(ids), n, _np_ptr(tables), max_blocks, _np_ptr(lens)),
+               "alloc_export")
+        return tables, lens
+
+    def block_table(self, seq: int):
+        n = ctypes.c_int32(0)
+        cap = self.num_blocks
+        out = np.empty(max(cap, 1), np.int32)
+        _check(lib().pkv_alloc_block_table(self._h, seq, _np_ptr(out), cap, ctypes.byref(n)), "alloc_block_table")
+        return out[: n.value].tolist()
+
+    def seq_len(self, seq: int) -> int:
+        n = ctypes.c_int64(0)
+        _check(lib().pkv_alloc_seq_len(self._h, seq, ctypes.byref(n)), "alloc_seq_len")
+        return n.value
+
+    def refcount(self, block: int) -> int:
+        return int(lib().pkv_alloc_refcount(self._h, block))
+
+    def num_free(self) -> int:
+        return int(lib().pkv_alloc_num_free(self._h))
+
+    def num_seqs(self) -> int:
+        return int(lib().pkv_alloc_num_seqs(self._h))
+
+    def fail_after(self, k: int) -> None:
+        lib().pkv_alloc_fail_after(self._h, int(k))
+
+
+def apply_setup(alloc: Allocator, ops) -> None:
+    """Runs an allocator script of ("new", seq, n) / ("fork", parent, child) /
+    ("extend", seq, n) / ("free", seq) operations."""
+    for op in ops:
+        if op[0] == "new":
+            alloc.seq_new(op[1], op[2])
+        elif op[0] == "fork":
+            alloc.fork(op[1], op[2])
+        elif op[0] == "extend":
+            alloc.extend(op[1], op[2])
+        elif op[0] == "free":
+            alloc.free(op[1])
+        else:
+            raise ValueError(f"unknown allocator op {op[0]!r}")

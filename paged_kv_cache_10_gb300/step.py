@@ -1,0 +1,99 @@
+"""One decode step of the paged KV cache through the C ABI.
+
+Host side (C++ allocator): ``append_batch`` reserves one slot per sequence
+(copy-on-write pairs where a sequence writes into a shared partial block),
+``export`` writes the padded block tables and lengths.  Device side, in
+stream order: ``copy_blocks`` (only when there are pairs) ->
+``paged_kv_append`` -> ``paged_attention_decode`` (+ its merge kernel when a
+sequence spans several partitions).
+
+Re-running the device part is idempotent (the same slots get the same
+values, the same copies are made), which is what timing loops rely on.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import pagedkv as pk
+
+_STORE = {"f16": torch.uint16, "bf16": torch.uint16, "e4m3": torch.uint8}
+
+
+def _to_dev(a: np.ndarray, device) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.uint16)
+    return torch.from_numpy(a).to(device)
+
+
+class DecodeStep:
+    """Device state and launch sequence of one workload's decode step."""
+
+    def __init__(self, wl, device="cuda", partition_tokens=None, alloc: pk.Allocator | None = None):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.kv_dtype,
+                                 k_scale=wl.k_scale, v_scale=wl.v_scale, block_size=wl.b)
+        self.partition_tokens = wl.partition_tokens if partition_tokens is None else partition_tokens
+        # -- host allocator: prefill script, then this step's appends
+        self.alloc = alloc or pk.Allocator(wl.NB, wl.b, wl.free_order)
+        pk.apply_setup(self.alloc, wl.setup)
+        rows = np.arange(wl.S, dtype=np.int64)
+        appending = np.full(wl.S, -1, np.int64)
+        appending[np.asarray(wl.step_seqs, dtype=np.int64)] = np.asarray(wl.step_seqs, dtype=np.int64)
+        self.slots, self.pairs = self.alloc.append_batch(appending)
+        self.max_blocks = wl.max_blocks
+        self.tables, self.seq_lens = self.alloc.export(rows, self.max_blocks)
+        self.max_seq_len = int(self.seq_lens.max()) if wl.S else 0
+        # -- device buffers
+        dev = self.device
+        self.k_cache = _to_dev(wl.k_pool, dev)
+        self.v_cache = _to_dev(wl.v_pool, dev)
+        self.q = _to_dev(wl.q, dev)
+        self.k_new = _to_dev(wl.k_new, dev)
+        self.v_new = _to_dev(wl.v_new, dev)
+        self.d_slots = torch.from_numpy(self.slots).to(dev)
+        self.d_pairs = torch.from_numpy(np.ascontiguousarray(self.pairs)).to(dev)
+        self.d_tables = torch.from_numpy(self.tables).to(dev)
+        self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
+        self.out = torch.empty((wl.S, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
+        ws = pk.decode_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
+        self.launches = 0
+
+    def effective_partition(self) -> int:
+        if self.partition_tokens:
+            return self.partition_tokens
+        return pk.decode_auto_partition(self.wl.S, self.wl.Hq, self.wl.Hkv, self.wl.D, self.max_seq_len)
+
+    def kernel_launches(self) -> int:
+        """Number of kernels one ``run`` enqueues."""
+        n = 2  # append + decode
+        if len(self.pairs):
+            n += 1
+        P = self.effective_partition()
+        if self.max_seq_len > P:
+            n += 1  # merge
+        return n
+
+    # -- device work (stream order)
+    def copy(self, stream=None):
+        if len(self.pairs):
+            pk.copy_blocks(self.k_cache, self.v_cache, self.desc, self.d_pairs, stream=stream)
+
+    def append(self, stream=None, k=None, v=None, slots=None):
+        pk.paged_kv_append(self.k_new if k is None else k, self.v_new if v is None else v,
+                           self.d_slots if slots is None else slots, self.k_cache, self.v_cache, self.desc,
+                           in_dtype=self.wl.in_dtype, stream=stream)
+
+    def decode(self, stream=None, q=None, tables=None, lens=None, out=None):
+        pk.paged_attention_decode(self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
+                                  self.d_tables if tables is None else tables,
+                                  self.d_lens if lens is None else lens, self.max_seq_len, self.wl.scale,
+                                  self.out if out is None else out, workspace=self.workspace,
+                                  partition_tokens=self.partition_tokens, q_dtype=self.wl.q_dtype, stream=stream)
+
+    def run(self, stream=None):
+        self.copy(stream)
+        self.append(stream)
+        self.decode(stream)

@@ -1,0 +1,96 @@
+"""The C ABI library builds, loads without a GPU and exports every symbol the
+header declares; host-side validation rejects bad arguments before touching
+the device.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_cache_10_gb300 import build, pagedkv
+    build.build()
+    return pagedkv
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(pk):
+    syms = declared_symbols()
+    assert "pkv_paged_attention_decode" in syms and "pkv_paged_kv_append" in syms and "pkv_copy_blocks" in syms
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    missing = [s for s in syms if not hasattr(lib, s)]
+    assert not missing
+    assert sorted(pk.EXPORTED) == sorted(s for s in syms if s in pk.EXPORTED)
+    assert set(syms) <= set(pk.EXPORTED)
+
+
+def test_status_strings_and_version(pk):
+    assert pk.status_string(0) == "ok"
+    assert "workspace" in pk.status_string(5)
+    assert pk.status_string(99) == "unknown status"
+    assert re.match(r"^\d+\.\d+\.\d+$", pk.version())
+
+
+def test_workspace_size_arithmetic(pk):
+    # one partition: no workspace
+    assert pk.decode_workspace_bytes(64, 32, 128, 512, 512) == 0
+    # S*Hq*NP rows of m and l (256-byte aligned regions) plus D floats each
+    S, Hq, D, L, P = 8, 64, 128, 32768, 512
+    rows = S * Hq * (L // P)
+    ml = -(-rows * 4 // 256) * 256
+    assert pk.decode_workspace_bytes(S, Hq, D, L, P) == 2 * ml + rows * D * 4
+    # auto sizes for its smallest partition (256 tokens), covering any choice it makes
+    assert pk.decode_workspace_bytes(S, Hq, D, L, 0) == pk.decode_workspace_bytes(S, Hq, D, L, 256)
+    assert pk.decode_workspace_bytes(S, Hq, D, L, 100) == 0  # not a multiple of the block size
+
+
+def test_validation_rejects_before_any_launch(pk):
+    L = pk.lib()
+    d = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="bf16").c()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+    # head_size 96 is unsupported
+    d96 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=96, kv_dtype="bf16").c()
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 4, fake, fake, ctypes.byref(d96), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_UNSUPPORTED
+    # group of 3 query heads per KV head is unsupported; 5 heads over 2 is invalid
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 6, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_UNSUPPORTED
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 5, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_INVALID
+    # q dtype must match a 16-bit pool
+    assert L.pkv_paged_attention_decode(fake, 0, 2, 4, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_UNSUPPORTED
+    # max_seq_len beyond the table, partition not a multiple of 16, misaligned pointer
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 4, fake, fake, ctypes.byref(d), fake, 4, fake, 65,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_INVALID
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 4, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 24, None) == pk.ERR_INVALID
+    assert L.pkv_paged_attention_decode(fake + 2, 1, 2, 4, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_INVALID
+    # workspace required for a split launch
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 4, fake, fake, ctypes.byref(d), fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 16, None) == pk.ERR_WORKSPACE
+    # null descriptor, negative sizes
+    assert L.pkv_paged_attention_decode(fake, 1, 2, 4, fake, fake, None, fake, 4, fake, 64,
+                                        0.1, fake, None, 0, 0, None) == pk.ERR_INVALID
+    assert L.pkv_paged_kv_append(fake, fake, 1, -1, fake, fake, fake, ctypes.byref(d), None) == pk.ERR_INVALID
+    # append: bf16 input into an f16 pool is unsupported; misaligned slot_mapping invalid
+    d16 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="f16").c()
+    assert L.pkv_paged_kv_append(fake, fake, 1, 4, fake, fake, fake, ctypes.byref(d16), None) == pk.ERR_UNSUPPORTED
+    assert L.pkv_paged_kv_append(fake, fake, 1, 4, fake + 4, fake, fake, ctypes.byref(d), None) == pk.ERR_INVALID
+    # fp8 pool needs positive scales
+    d8 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="e4m3", k_scale=0.0).c()
+    assert L.pkv_copy_blocks(fake, fake, ctypes.byref(d8), fake, 1, None) == pk.ERR_INVALID
+    # empty work is a no-op that needs no device
+    assert L.pkv_copy_blocks(fake, fake, ctypes.byref(d), None, 0, None) == pk.OK
+    assert L.pkv_paged_kv_append(None, None, 1, 0, None, None, None, ctypes.byref(d), None) == pk.OK

@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py without a GPU: the multi-rank aggregation
+(whole-job bytes summed over ranks, time = slowest rank) over a gloo process
+group of two CPU ranks, and the algorithmic byte count of a step."""
+import os
+import socket
+
+import numpy as np
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    b, s = bench.aggregate(1000.0 * (rank + 1), 0.5 + rank)
+    q.put((rank, b, s))
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for _, b, s in res:
+        assert b == 3000.0 and s == 1.5
+
+
+def test_single_process_aggregate_is_identity():
+    import bench
+    assert bench.aggregate(12.0, 3.0) == (12.0, 3.0)
+
+
+def test_step_bytes_counts_the_gathered_kv():
+    import bench
+
+    class WL:
+        S, Hq, Hkv, D, b = 2, 8, 2, 128, 16
+        def kv_elem_bytes(self):
+            return 2
+
+    class Step:
+        wl = WL()
+        seq_lens = np.array([17, 40], np.int32)
+        slots = np.array([5, -1], np.int64)
+        pairs = np.zeros((1, 2), np.int32)
+
+    nb = bench.step_bytes(Step())
+    assert nb["kv"] == (17 + 40) * 2 * 2 * 128 * 2
+    assert nb["decode"] == nb["kv"] + 2 * 2 * 8 * 128 * 2 + (2 + 3) * 4 + 2 * 4
+    assert nb["append"] == 1 * 2 * 2 * 128 * (2 + 2) + 2 * 8
+    assert nb["copy"] == 1 * (2 * 2 * (2 * 16 * 128 * 2) + 8)
+    assert nb["total"] == nb["decode"] + nb["append"] + nb["copy"]

@@ -1,0 +1,154 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Append and copy-on-write must match bit for bit (whole pools compared);
+attention within max-abs 2e-3 (fp16) / 1e-2 (bf16, fp8 KV judged on the
+dequantised values).  Small cases span several blocks, partitions and warps
+with ragged tails; the five named workloads run at full size with the
+launch configuration the benchmark uses, checked on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity_util import TOL, check_step, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_10_gb300 import build, pagedkv
+    build.build()
+    pagedkv.lib()
+    return pagedkv
+
+
+def run(wl, partition=None):
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    st = DecodeStep(wl, device="cuda", partition_tokens=partition)
+    st.run()
+    torch.cuda.synchronize()
+    return st
+
+
+EDGE_LENS = [1, 15, 16, 17, 31, 33, 100, 255, 511, 512, 513, 1000]
+
+CASES = [
+    # (kv dtype, q dtype, head size)
+    ("f16", "f16", 64),
+    ("bf16", "bf16", 128),
+    ("e4m3", "bf16", 128),
+    ("f16", "f16", 128),
+    ("bf16", "bf16", 64),
+    ("e4m3", "f16", 64),
+]
+
+
+@pytest.mark.parametrize("kv,qd,D", CASES)
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("partition", [0, 16, 64, 512])
+def test_small_cases_match_oracle(lib, kv, qd, D, G, partition):
+    from paged_kv_cache_10_gb300 import workloads
+    Hkv = 2
+    wl = workloads.custom(f"edge_{kv}_{D}_{G}", 7 + G + D, EDGE_LENS, Hkv * G, Hkv, D, kv_dtype=kv,
+                          q_dtype=qd, partition_tokens=partition)
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_step(st)
+    assert err <= TOL[kv], (err, mx)
+
+
+def test_zero_length_rows_and_padding_slots(lib):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.custom("zeros", 3, [0, 5, 0, 40], 8, 2, 128, kv_dtype="bf16")
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, _ = check_step(st)
+    assert err <= TOL["bf16"]
+    out = host_bits(st.out)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert st.slots[0] == -1 and st.slots[2] == -1
+
+
+@pytest.mark.parametrize("P", [16, 48, 160, 0])
+def test_split_and_unsplit_agree(lib, P):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.custom("split", 11, [700, 1300, 64, 2049], 32, 8, 128, kv_dtype="bf16", partition_tokens=P)
+    a = run(wl)
+    b = run(wl, partition=2064)  # one partition for every row
+    ea, _ = check_step(a)
+    eb, _ = check_step(b)
+    assert ea <= TOL["bf16"] and eb <= TOL["bf16"]
+    import oracle
+    fa = oracle.dequantize(host_bits(a.out), "bf16")
+    fb = oracle.dequantize(host_bits(b.out), "bf16")
+    # the two reductions differ only in fp32 rounding before the final bf16 rounding
+    assert np.max(np.abs(fa - fb) / np.maximum(np.abs(fb), 1e-2)) <= 2 ** -7
+
+
+@pytest.mark.parametrize("name,rows", [
+    ("tiny_fp16", None),
+    ("llama7b_mha", list(range(0, 64, 4))),
+    ("llama3_8b_gqa", list(range(0, 256, 9))),
+    ("longctx_fp8", [0, 5]),
+    ("prefix_share", list(range(0, 128, 5))),
+])
+def test_named_workloads_full_size(lib, name, rows):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.NAMED[name]()
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    if name == "prefix_share":
+        assert len(st.pairs) >= 50  # copy-on-write really happens
+    err, mx = check_step(st, rows=rows)
+    assert err <= TOL[wl.kv_dtype], (name, err, mx)
+    del st
+    torch.cuda.empty_cache()
+
+
+def test_literal_prefix_share_has_no_copy(lib):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.prefix_share(literal=True, pairs=16)
+    st = run(wl)
+    assert len(st.pairs) == 0
+    err, _ = check_step(st)
+    assert err <= TOL["bf16"]
+
+
+def test_device_errors_are_reported_not_trapped(lib):
+    """Out-of-range ids set bits in the device error word; the kernels skip
+    the access and the context stays usable."""
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.custom("errs", 5, [20, 40], 4, 2, 128, kv_dtype="bf16")
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    st = DecodeStep(wl, device="cuda")
+    assert lib.get_device_error() == 0
+    # a block id outside the pool in row 1
+    bad = st.d_tables.clone()
+    bad[1, 1] = wl.NB + 5
+    st.decode(tables=bad)
+    assert lib.get_device_error() & lib.DEVERR_BLOCK_ID
+    # a seq_len beyond the block table
+    lens = st.d_lens.clone()
+    lens[0] = st.max_blocks * 16 + 7
+    st.decode(lens=lens)
+    assert lib.get_device_error() & lib.DEVERR_SEQ_LEN
+    # a slot outside the pool; -1 is padding and silent
+    slots = torch.tensor([wl.NB * 16 + 3, -1], dtype=torch.int64, device="cuda")
+    st.append(slots=slots)
+    assert lib.get_device_error() == lib.DEVERR_SLOT
+    # a copy pair outside the pool
+    pairs = torch.tensor([[0, wl.NB]], dtype=torch.int32, device="cuda")
+    lib.copy_blocks(st.k_cache, st.v_cache, st.desc, pairs)
+    assert lib.get_device_error() == lib.DEVERR_COPY_PAIR
+    # the context still works: a clean step matches the oracle
+    st2 = run(wl)
+    assert lib.get_device_error() == 0
+    err, _ = check_step(st2)
+    assert err <= TOL["bf16"]
+
+
+def test_library_is_loaded_from_the_tree(lib):
+    import os
+    maps = open("/proc/self/maps").read()
+    assert os.path.realpath(lib.LIB_PATH) in maps
