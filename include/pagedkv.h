@@ -190,6 +190,18 @@ int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t
                                   int32_t head_size, int32_t max_seq_len);
 
 /*
+ * Decode kernel selection for subsequent pkv_paged_attention_decode calls
+ * (process-wide): 0 = automatic (tensor-core kernel when num_q_heads /
+ * num_kv_heads >= 2 and head_size == 128, CUDA-core kernel otherwise),
+ * 1 = always the CUDA-core kernel, 2 = always the tensor-core kernel (a call
+ * it cannot serve then returns PKV_ERR_UNSUPPORTED).  Both compute the same
+ * function; the switch exists so each can be tested and timed.
+ * PKV_ERR_INVALID for another value.
+ */
+pkv_status pkv_set_decode_path(int32_t path);
+int32_t pkv_get_decode_path(void);
+
+/*
  * Reads and clears the device error word of the current device (the OR of
  * PKV_DEVERR_* bits set by every kernel since the last call).  Synchronises
  * the given stream first.  *flags receives the bits.

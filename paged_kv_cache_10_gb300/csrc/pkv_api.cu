@@ -1,8 +1,11 @@
 // pkv_api.cu -- C ABI entry points for decode attention, the device error
 // word, status strings.  Argument meaning, layout, ownership and error
 // behaviour are specified in include/pagedkv.h.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pkv_decode_impl.cuh"
 
@@ -56,6 +59,38 @@ int num_sms() {
 
 namespace {
 
+std::atomic<int> g_decode_path{0};  // 0 auto, 1 CUDA cores, 2 tensor cores
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D view of a pool as [NB*Hkv*16 rows][D] elements, 128-byte inner box of
+// 16 rows, 128-byte swizzle (matches swz128() in the kernel).
+bool encode_pool_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t rows, int D) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * elem_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(kBlockSize)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Smallest partition the automatic choice uses (sizes the P = 0 workspace).
 constexpr int kAutoMinPartition = 256;
 
@@ -89,6 +124,14 @@ size_t workspace_bytes(int64_t S, int64_t Hq, int64_t D, int64_t max_seq_len, in
 }  // namespace pkv
 
 using namespace pkv;
+
+extern "C" pkv_status pkv_set_decode_path(int32_t path) {
+    if (path < 0 || path > 2) return PKV_ERR_INVALID;
+    g_decode_path.store(path);
+    return PKV_OK;
+}
+
+extern "C" int32_t pkv_get_decode_path(void) { return g_decode_path.load(); }
 
 extern "C" size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                              int32_t max_seq_len, int32_t partition_tokens) {
@@ -174,16 +217,39 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
         p.part_o = reinterpret_cast<float*>(w + 2 * ml);
     }
 
+    // Tensor-core kernel for grouped-query heads at head_size 128; CUDA
+    // cores otherwise (one query row per KV head is not a dense tile).
+    const int64_t pool_rows = static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * kBlockSize;
+    const bool mma_ok = d->head_size == 128 && G >= 2 && pool_rows <= 0x7fffffff;
+    const int path = g_decode_path.load();
+    if (path == 2 && !mma_ok) return PKV_ERR_UNSUPPORTED;
+    const bool use_mma = mma_ok && path != 1;
+
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (d->kv_dtype == PKV_F16)
+    if (use_mma) {
+        CUtensorMap tk, tv;
+        const int eb = d->kv_dtype == PKV_FP8_E4M3 ? 1 : 2;
+        if (!encode_pool_map(&tk, k_cache, eb, pool_rows, d->head_size) ||
+            !encode_pool_map(&tv, v_cache, eb, pool_rows, d->head_size))
+            return PKV_ERR_CUDA;
+        if (d->kv_dtype == PKV_F16)
+            e = launch_decode_mma_f16(p, G, tk, tv, st);
+        else if (d->kv_dtype == PKV_BF16)
+            e = launch_decode_mma_bf16(p, G, tk, tv, st);
+        else if (q_dtype == PKV_BF16)
+            e = launch_decode_mma_fp8_bf16q(p, G, tk, tv, st);
+        else
+            e = launch_decode_mma_fp8_f16q(p, G, tk, tv, st);
+    } else if (d->kv_dtype == PKV_F16) {
         e = launch_decode_f16(p, G, st);
-    else if (d->kv_dtype == PKV_BF16)
+    } else if (d->kv_dtype == PKV_BF16) {
         e = launch_decode_bf16(p, G, st);
-    else if (q_dtype == PKV_BF16)
+    } else if (q_dtype == PKV_BF16) {
         e = launch_decode_fp8_bf16q(p, G, st);
-    else
+    } else {
         e = launch_decode_fp8_f16q(p, G, st);
+    }
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     if (NP > 1) {
         e = launch_merge(p, q_dtype, st);

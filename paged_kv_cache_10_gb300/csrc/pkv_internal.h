@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pagedkv.h"
@@ -42,6 +43,18 @@ cudaError_t launch_decode_f16(const DecodeParams& p, int G, cudaStream_t st);
 cudaError_t launch_decode_bf16(const DecodeParams& p, int G, cudaStream_t st);
 cudaError_t launch_decode_fp8_bf16q(const DecodeParams& p, int G, cudaStream_t st);
 cudaError_t launch_decode_fp8_f16q(const DecodeParams& p, int G, cudaStream_t st);
+
+// Tensor-core launchers for grouped-query attention (G in {2, 4, 8},
+// head_size 128); tk / tv map the K / V pools as 2-D [NB*Hkv*16 rows][128]
+// tensors with a 128-byte inner box and the 128-byte swizzle.
+cudaError_t launch_decode_mma_f16(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  cudaStream_t st);
+cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   cudaStream_t st);
+cudaError_t launch_decode_mma_fp8_bf16q(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                                        cudaStream_t st);
+cudaError_t launch_decode_mma_fp8_f16q(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       cudaStream_t st);
 
 // Log-sum-exp merge of split-K partials into out (q dtype).
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);

@@ -27,7 +27,7 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT =
 EXPORTED = [
     "pkv_paged_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
     "pkv_paged_attention_decode", "pkv_decode_auto_partition", "pkv_get_device_error",
-    "pkv_status_string", "pkv_version", "pkv_alloc_create", "pkv_alloc_destroy",
+    "pkv_status_string", "pkv_version", "pkv_set_decode_path", "pkv_get_decode_path", "pkv_alloc_create", "pkv_alloc_destroy",
     "pkv_alloc_seq_new", "pkv_alloc_fork", "pkv_alloc_append_slot", "pkv_alloc_seq_extend",
     "pkv_alloc_free", "pkv_alloc_append_batch", "pkv_alloc_export", "pkv_alloc_block_table",
     "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
@@ -87,6 +87,8 @@ def lib():
                                              P, P, ctypes.c_size_t, i32, P]),
         "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32]),
         "pkv_get_device_error": (i32, [u32p, P]),
+        "pkv_set_decode_path": (i32, [i32]),
+        "pkv_get_decode_path": (i32, []),
         "pkv_status_string": (ctypes.c_char_p, [i32]),
         "pkv_version": (ctypes.c_char_p, []),
         "pkv_alloc_create": (P, [i32, i32, P]),
@@ -207,6 +209,33 @@ def paged_attention_decode(q, k_cache, v_cache, desc: CacheDesc, block_tables, s
                                           int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes,
                                           int(partition_tokens), _stream(stream))
     _check(st, "paged_attention_decode")
+
+
+PATH_AUTO, PATH_CUDA_CORES, PATH_TENSOR_CORES = 0, 1, 2
+
+
+def set_decode_path(path: int) -> None:
+    _check(lib().pkv_set_decode_path(int(path)), "set_decode_path")
+
+
+def get_decode_path() -> int:
+    return int(lib().pkv_get_decode_path())
+
+
+class decode_path:
+    """Context manager selecting the decode kernel (see pkv_set_decode_path)."""
+
+    def __init__(self, path: int):
+        self.path = path
+
+    def __enter__(self):
+        self.prev = get_decode_path()
+        set_decode_path(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        set_decode_path(self.prev)
+        return False
 
 
 def get_device_error(stream=None) -> int:

@@ -47,15 +47,69 @@ CASES = [
 @pytest.mark.parametrize("kv,qd,D", CASES)
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("partition", [0, 16, 64, 512])
-def test_small_cases_match_oracle(lib, kv, qd, D, G, partition):
+@pytest.mark.parametrize("path", [0, 1])
+def test_small_cases_match_oracle(lib, kv, qd, D, G, partition, path):
+    """path 0: automatic choice (tensor cores for G >= 2 at D = 128);
+    path 1: the CUDA-core kernel for every case."""
     from paged_kv_cache_10_gb300 import workloads
+    if path == 1 and (G == 1 or D != 128):
+        pytest.skip("automatic choice already is the CUDA-core kernel")
     Hkv = 2
     wl = workloads.custom(f"edge_{kv}_{D}_{G}", 7 + G + D, EDGE_LENS, Hkv * G, Hkv, D, kv_dtype=kv,
                           q_dtype=qd, partition_tokens=partition)
-    st = run(wl)
+    with lib.decode_path(path):
+        st = run(wl)
     assert lib.get_device_error() == 0
     err, mx = check_step(st)
     assert err <= TOL[kv], (err, mx)
+
+
+@pytest.mark.parametrize("kv,qd", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "bf16")])
+def test_tensor_core_and_cuda_core_kernels_agree(lib, kv, qd):
+    from paged_kv_cache_10_gb300 import workloads
+    import oracle
+    wl = workloads.custom("paths", 21, [1, 16, 17, 300, 1029], 32, 8, 128, kv_dtype=kv, q_dtype=qd)
+    with lib.decode_path(2):
+        a = run(wl)
+    with lib.decode_path(1):
+        b = run(wl)
+    ea, _ = check_step(a)
+    eb, _ = check_step(b)
+    assert ea <= TOL[kv] and eb <= TOL[kv]
+    fa = oracle.dequantize(host_bits(a.out), qd)
+    fb = oracle.dequantize(host_bits(b.out), qd)
+    assert np.max(np.abs(fa - fb)) <= TOL[kv]
+
+
+def test_tensor_core_path_rejects_what_it_cannot_serve(lib):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.custom("mha", 22, [40], 4, 4, 128, kv_dtype="bf16")  # G = 1
+    with lib.decode_path(2):
+        with pytest.raises(lib.PagedKVError):
+            run(wl)
+
+
+def test_stale_nan_bytes_past_the_sequence_end_are_ignored(lib):
+    """Slots past a sequence's last token may hold anything (here NaN bit
+    patterns); neither kernel may let them reach the output."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.custom("nan", 23, [5, 21, 16], 16, 2, 128, kv_dtype="bf16")
+    for path in (1, 2):
+        st = DecodeStep(wl, device="cuda")
+        for s in range(wl.S):
+            L = int(st.seq_lens[s])
+            last = int(st.tables[s, (L - 1) // 16])
+            off = L % 16
+            if off:
+                st.k_cache[last, :, off:] = 0x7FC0  # bf16 quiet NaN
+                st.v_cache[last, :, off:] = 0x7FC0
+        with lib.decode_path(path):
+            st.run()
+        torch.cuda.synchronize()
+        got = host_bits(st.out)
+        import oracle
+        assert np.all(np.isfinite(oracle.dequantize(got, "bf16"))), path
 
 
 def test_zero_length_rows_and_padding_slots(lib):
@@ -82,8 +136,10 @@ def test_split_and_unsplit_agree(lib, P):
     import oracle
     fa = oracle.dequantize(host_bits(a.out), "bf16")
     fb = oracle.dequantize(host_bits(b.out), "bf16")
-    # the two reductions differ only in fp32 rounding before the final bf16 rounding
-    assert np.max(np.abs(fa - fb) / np.maximum(np.abs(fb), 1e-2)) <= 2 ** -7
+    # the two reductions differ in summation order and, on the tensor-core
+    # path, in where P is rounded to bf16 (relative to a partition's running
+    # max): a few bf16 ulps of the outputs, far inside the tolerance
+    assert np.max(np.abs(fa - fb)) <= 4e-3
 
 
 @pytest.mark.parametrize("name,rows", [
