@@ -183,6 +183,35 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t nu
                                       size_t workspace_bytes, int32_t partition_tokens, void* stream);
 
 /*
+ * Decode attention that allocates nothing and needs no workspace argument.
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot hand the library a device buffer -- a plug-in inside a framework
+ * that owns all device memory and exposes no allocator, or a latency-
+ * critical loop that must not call cudaMalloc (which can synchronise the
+ * device).  Arguments and results are those of pkv_paged_attention_decode
+ * without workspace / workspace_bytes.
+ *
+ * The split-K scratch is a 32 MiB array inside the library (held on every
+ * GPU that loads it until the process exits).  A call whose scratch need,
+ * pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len,
+ * P) for the partition size P actually used, exceeds 32 MiB returns
+ * PKV_ERR_WORKSPACE and launches nothing.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress); make that first
+ * call before any stream capture.  No cudaMalloc, cudaFree or allocating
+ * routine is called.  All calls share the one array and it keeps whatever
+ * the last call left there; nothing in it needs to start at zero (every
+ * partial the merge reads is written first in the same call).  Calls whose
+ * kernels may overlap on the GPU (different streams without ordering) race
+ * on the array and give undefined results.
+ */
+pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, int32_t num_seqs,
+                                              int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                              const pkv_cache_desc* desc, const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                              int32_t max_seq_len, float scale, void* out,
+                                              int32_t partition_tokens, void* stream);
+
+/*
  * Partition size the automatic choice (partition_tokens = 0) would use for
  * these sizes on the current device, or a negative pkv_status on error.
  */

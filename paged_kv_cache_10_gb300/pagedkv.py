@@ -26,7 +26,7 @@ DEVERR_BLOCK_ID, DEVERR_SEQ_LEN, DEVERR_SLOT, DEVERR_COPY_PAIR, DEVERR_TIMEOUT =
 
 EXPORTED = [
     "pkv_paged_kv_append", "pkv_copy_blocks", "pkv_decode_workspace_bytes",
-    "pkv_paged_attention_decode", "pkv_decode_auto_partition", "pkv_get_device_error",
+    "pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc", "pkv_decode_auto_partition", "pkv_get_device_error",
     "pkv_status_string", "pkv_version", "pkv_set_decode_path", "pkv_get_decode_path", "pkv_alloc_create", "pkv_alloc_destroy",
     "pkv_alloc_seq_new", "pkv_alloc_fork", "pkv_alloc_append_slot", "pkv_alloc_seq_extend",
     "pkv_alloc_free", "pkv_alloc_append_batch", "pkv_alloc_export", "pkv_alloc_block_table",
@@ -85,6 +85,8 @@ def lib():
         "pkv_decode_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32]),
         "pkv_paged_attention_decode": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, ctypes.c_float,
                                              P, P, ctypes.c_size_t, i32, P]),
+        "pkv_paged_attention_decode_noalloc": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, ctypes.c_float,
+                                                     P, i32, P]),
         "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32]),
         "pkv_get_device_error": (i32, [u32p, P]),
         "pkv_set_decode_path": (i32, [i32]),
@@ -236,6 +238,24 @@ class decode_path:
     def __exit__(self, *exc):
         set_decode_path(self.prev)
         return False
+
+
+def paged_attention_decode_noalloc(q, k_cache, v_cache, desc: CacheDesc, block_tables, seq_lens,
+                                   max_seq_len: int, scale: float, out, partition_tokens: int = 0,
+                                   q_dtype: str | None = None, stream=None) -> None:
+    """Decode attention for callers that cannot supply a workspace: the
+    library's built-in 32 MiB scratch array is used instead (see the C
+    declaration for its limits and sharing rules)."""
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    st = lib().pkv_paged_attention_decode_noalloc(_dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
+                                                  _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+                                                  ctypes.byref(desc.c()), _dev_ptr(block_tables, "block_tables"),
+                                                  int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
+                                                  int(max_seq_len), float(scale), _dev_ptr(out, "out"),
+                                                  int(partition_tokens), _stream(stream))
+    _check(st, "paged_attention_decode_noalloc")
 
 
 def get_device_error(stream=None) -> int:
