@@ -41,13 +41,23 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode-attention KV GB/s (% of GB300 HBM peak) and µs/step, 1 GPU"
 DEFAULT_WORKLOAD = "llama7b_mha"
-KERNEL_SOURCES = ["paged_kv_cache_10_gb300/csrc/pkv_decode_impl.cuh", "paged_kv_cache_10_gb300/csrc/pkv_device.cuh"]
+_CSRC = "paged_kv_cache_10_gb300/csrc/"
+# Sources of the decode kernel a workload runs (CUDA-core kernel for one
+# query head per KV head or head_size 64; tensor-core kernel for GQA at 128).
+KERNEL_SOURCES = {
+    "cuda_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh"],
+    "tensor_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh"],
+}
 
 
 # ------------------------------------------------------------------ helpers
-def kernel_hash() -> str:
+def decode_kernel_kind(wl) -> str:
+    return "tensor_core" if (wl.Hq // wl.Hkv >= 2 and wl.D == 128) else "cuda_core"
+
+
+def kernel_hash(kind: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kind]:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -60,13 +70,13 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kind: str):
     """dram read+write bytes per decode launch from the committed ncu summary,
     valid only for the kernel sources it was taken on."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    kh = kernel_hash()
+    kh = kernel_hash(kind)
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == kh:
@@ -324,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     dec_ms = statistics.mean(decode_ms)
     achieved = nbytes["decode"] / (dec_ms / 1e3) / 1e9
-    traffic = recorded_traffic(args.workload)
+    kind = decode_kernel_kind(wl)
+    traffic = recorded_traffic(args.workload, kind)
     ms_per_step = total_ms / K
     line = {
         "metric": METRIC,
@@ -358,7 +369,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "decode_kernel (+ merge_kernel when split)", "mean_launch_us": round(dec_ms * 1e3, 2),
+                     "kernel": ("decode_mma_kernel" if kind == "tensor_core" else "decode_kernel")
+                     + " (+ merge_kernel when split)", "kernel_sources_hash": kernel_hash(kind),
+                     "mean_launch_us": round(dec_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": nbytes["decode"]},
         "clocks": clocks,
     }

@@ -30,17 +30,17 @@ unsigned int* error_word() {
 
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st) {
     const int64_t rows = static_cast<int64_t>(p.S) * p.Hq;
-    const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
+    const dim3 grid(static_cast<unsigned>(rows));
     if (q_dtype == PKV_BF16) {
         if (p.D == 128)
-            merge_kernel<128, BF16><<<grid, 256, 0, st>>>(p);
+            merge_kernel<128, BF16><<<grid, kMergeThreads, 0, st>>>(p);
         else
-            merge_kernel<64, BF16><<<grid, 256, 0, st>>>(p);
+            merge_kernel<64, BF16><<<grid, kMergeThreads, 0, st>>>(p);
     } else {
         if (p.D == 128)
-            merge_kernel<128, F16><<<grid, 256, 0, st>>>(p);
+            merge_kernel<128, F16><<<grid, kMergeThreads, 0, st>>>(p);
         else
-            merge_kernel<64, F16><<<grid, 256, 0, st>>>(p);
+            merge_kernel<64, F16><<<grid, kMergeThreads, 0, st>>>(p);
     }
     return cudaGetLastError();
 }

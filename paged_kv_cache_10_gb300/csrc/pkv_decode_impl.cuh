@@ -349,16 +349,21 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     }
 }
 
-// Log-sum-exp merge of the split-K partials of one (sequence, query head)
-// row per warp: M = max_p m_p, w_p = l_p 2^(m_p - M),
-// out = sum_p w_p o_p / sum_p w_p.  Rows of single-partition sequences were
-// written by the main kernel and are skipped.
+// Log-sum-exp merge of the split-K partials, one CTA of kMergeThreads per
+// (sequence, query head) row: M = max_p m_p, w_p = l_p 2^(m_p - M),
+// out = sum_p w_p o_p / sum_p w_p.  The weights of a chunk of partitions
+// are computed once into shared memory; then thread d walks the chunk with
+// 8 independent loads in flight (each a coalesced row of partial outputs).
+// Rows of single-partition sequences were written by the main kernel and are
+// skipped.
+constexpr int kMergeThreads = 128;
+
 template <int D, typename QT>
-__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
-    constexpr int PER = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-    if (row >= static_cast<int64_t>(p.S) * p.Hq) return;
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+    __shared__ float w_s[kMergeThreads];
+    __shared__ float red[kMergeThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
     const int s = static_cast<int>(row / p.Hq);
     int L = __ldg(p.seq_lens + s);
     const int Lmax = min(p.MB * kBlockSize, p.NP * p.P);
@@ -367,35 +372,52 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
     if (nparts <= 1) return;
     const float* pm = p.part_m + row * p.NP;
     const float* pl = p.part_l + row * p.NP;
+    const float* po = p.part_o + row * p.NP * D;
+
     float M = -INFINITY;
-    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, pm[i]);
+    for (int i = tid; i < nparts; i += kMergeThreads) M = fmaxf(M, pm[i]);
 #pragma unroll
     for (int mask = 16; mask > 0; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mask));
-    float acc[PER];
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float den = 0.f;
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+
+    float acc = 0.f, den = 0.f;
     if (M != -INFINITY) {
-        for (int base = 0; base < nparts; base += 32) {
-            const int i = base + lane;
-            float wmine = 0.f;
-            if (i < nparts) {
-                const float l = pl[i];
-                wmine = l > 0.f ? l * exp2f(pm[i] - M) : 0.f;
+        for (int base = 0; base < nparts; base += kMergeThreads) {
+            const int cnt = min(kMergeThreads, nparts - base);
+            __syncthreads();  // previous chunk's weights fully consumed
+            if (tid < cnt) {
+                const float l = pl[base + tid];
+                w_s[tid] = l > 0.f ? l * exp2f(pm[base + tid] - M) : 0.f;
             }
-            const int cnt = min(32, nparts - base);
-            for (int j = 0; j < cnt; ++j) {
-                const float w = __shfl_sync(kFull, wmine, j);
-                den += w;
-                const float* o = p.part_o + (row * p.NP + base + j) * D;
+            __syncthreads();
+            if (tid < D) {
+                const float* o = po + static_cast<int64_t>(base) * D + tid;
+                int j = 0;
+                for (; j + 8 <= cnt; j += 8) {
+                    float v[8];
 #pragma unroll
-                for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, o[lane + 32 * e], acc[e]);
+                    for (int u = 0; u < 8; ++u) v[u] = o[(j + u) * D];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        acc = fmaf(w_s[j + u], v[u], acc);
+                        den += w_s[j + u];
+                    }
+                }
+                for (; j < cnt; ++j) {
+                    acc = fmaf(w_s[j], o[j * D], acc);
+                    den += w_s[j];
+                }
             }
         }
     }
-    auto* out = reinterpret_cast<typename QT::storage*>(p.out) + row * D;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) out[lane + 32 * e] = from_float<QT>(den > 0.f ? acc[e] / den : 0.f);
+    if (tid < D) {
+        auto* out = reinterpret_cast<typename QT::storage*>(p.out) + row * D;
+        out[tid] = from_float<QT>(den > 0.f ? acc / den : 0.f);
+    }
 }
 
 // ------------------------------------------------------------- launchers

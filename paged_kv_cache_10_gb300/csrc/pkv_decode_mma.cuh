@@ -52,7 +52,9 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
-// D = A . B + D with A rows 8..15 zero (a1 = a3 = 0).
+// D = A . B + D in place, with A rows 8..15 zero (a1 = a3 = 0): rows 8..15
+// of the accumulator start at zero and stay zero, so only d[0], d[1] carry
+// data, but the four registers stay one in-place group (no moves).
 template <bool BF>
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
     if constexpr (BF) {
@@ -68,6 +70,22 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a2, uin
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
             : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
     }
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Splits a 32-bit word of four E4M3 bytes into two f16x2 words (bytes 0,1
+// and bytes 2,3), with the hardware conversion.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
@@ -107,17 +125,28 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Copy stages per warp and resident CTAs per SM: about 190 KB of tiles in
+// flight per SM either way; fp8 tiles are half the size, so twice the warps
+// share the same bytes (its per-block instruction count is higher).
+template <typename KT>
+struct MmaCfg {
+    static constexpr int kStages = KT::bytes == 1 ? 4 : 2;
+    static constexpr int kCtasPerSm = 3;
+};
+
 template <typename KT, int NW, int NST>
 struct MmaSmem {
     static constexpr int kTile = kBlockSize * 128 * KT::bytes;  // 4096 (16-bit) or 2048 (fp8)
     static constexpr int kStage = 2 * kTile;
     static constexpr int kBarOffset = NW * NST * kStage;
     static constexpr int kPhysOffset = kBarOffset + NW * NST * 8;
-    static constexpr int kBytes = kPhysOffset + NW * NST * 4 + 1024;  // + alignment slack
+    // merge weights: [NW][8] per-warp scale factors, [8] 1/denominator, [8] denominator
+    static constexpr int kMergeOffset = kPhysOffset + NW * NST * 4;
+    static constexpr int kBytes = kMergeOffset + (NW * 8 + 16) * 4 + 1024;  // + alignment slack
 };
 
 template <int G, typename KT, typename QT, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv) {
     constexpr int D = 128;
@@ -241,6 +270,28 @@ __global__ void __launch_bounds__(NW * 32)
             unsigned char* kt = wbase + stage * STAGE;
             unsigned char* vt = kt + TILE;
             const uint32_t kts = smem_addr(kt), vts = smem_addr(vt);
+            if (nvalid < kBlockSize) {
+                // zero the value rows past the sequence end (stale pool bytes
+                // must not reach the MMA: 0 * NaN is NaN)
+                constexpr int kChunksPerRow = kFP8 ? 8 : 16;
+                const int nz = (kBlockSize - nvalid) * kChunksPerRow;
+                for (int i = lane; i < nz; i += 32) {
+                    const int row = nvalid + i / kChunksPerRow, c = i % kChunksPerRow;
+                    *reinterpret_cast<uint4*>(vt + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            // fp8: value fragments are loaded up front so their latency hides
+            // behind Q K^T (chunk r0 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9)
+            uint4 va[4];
+            if constexpr (kFP8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = 2 * qd + (i & 1) + 8 * (i >> 1);
+                    va[i] = *reinterpret_cast<const uint4*>(vt + swz128(tok, r0));
+                }
+            }
             // ---- S^T = Q K^T  (n-tile j = tokens 8j .. 8j+7)
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             if constexpr (!kFP8) {
@@ -255,16 +306,23 @@ __global__ void __launch_bounds__(NW * 32)
                     mma16816<kBF>(sa[1], qa[kk][0], qa[kk][1], b2, b3);
                 }
             } else {
+                uint32_t w[2][8];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int tok = 8 * j + r0;
                     const uint4 c0 = *reinterpret_cast<const uint4*>(kt + swz128(tok, 2 * qd));
                     const uint4 c1 = *reinterpret_cast<const uint4*>(kt + swz128(tok, 2 * qd + 1));
-                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    w[j][0] = c0.x; w[j][1] = c0.y; w[j][2] = c0.z; w[j][3] = c0.w;
+                    w[j][4] = c1.x; w[j][5] = c1.y; w[j][6] = c1.z; w[j][7] = c1.w;
+                }
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma16816<false>(sa[j], qa[kk][0], qa[kk][1], e4m3x2_to_f16x2(w[kk]),
-                                        e4m3x2_to_f16x2(w[kk] >> 16));
+                for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        uint32_t blo, bhi;
+                        e4m3x4_to_f16x4(w[j][kk], blo, bhi);
+                        mma16816<false>(sa[j], qa[kk][0], qa[kk][1], blo, bhi);
+                    }
                 }
             }
             // ---- online softmax on row r0 (tokens 2qd, 2qd+1, 8+2qd, 9+2qd)
@@ -275,33 +333,25 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (tk[i] >= nvalid) sv[i] = -INFINITY;
-                // zero the value rows past the sequence end (stale pool bytes
-                // must not reach the MMA: 0 * NaN is NaN)
-                constexpr int kChunksPerRow = kFP8 ? 8 : 16;
-                const int nz = (kBlockSize - nvalid) * kChunksPerRow;
-                for (int i = lane; i < nz; i += 32) {
-                    const int row = nvalid + i / kChunksPerRow, c = i % kChunksPerRow;
-                    *reinterpret_cast<uint4*>(vt + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
             }
             float bm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
             bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
             const float mn = fmaxf(m, bm);
-            const float alpha = exp2f(m - mn);
+            const float alpha = mn == m ? 1.f : ex2(m - mn);
             m = mn;
             float pr[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pr[i] = exp2f(sv[i] - mn);
+            for (int i = 0; i < 4; ++i) pr[i] = ex2(sv[i] - mn);
             lsum = lsum * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
             const uint32_t pa0 = pack2<kBF>(pr[0], pr[1]);
             const uint32_t pa2 = pack2<kBF>(pr[2], pr[3]);
+            if (__any_sync(kFull, alpha != 1.f)) {  // skip when no row's max moved
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                o[j][0] *= alpha;
-                o[j][1] *= alpha;
+                for (int j = 0; j < 16; ++j) {
+                    o[j][0] *= alpha;
+                    o[j][1] *= alpha;
+                }
             }
             // ---- O += P V
             if constexpr (!kFP8) {
@@ -316,22 +366,21 @@ __global__ void __launch_bounds__(NW * 32)
                     mma16816<kBF>(o[2 * i + 1], pa0, pa2, b2, b3);
                 }
             } else {
-                const uint4 ra = *reinterpret_cast<const uint4*>(vt + swz128(2 * qd, r0));
-                const uint4 rb = *reinterpret_cast<const uint4*>(vt + swz128(2 * qd + 1, r0));
-                const uint4 rc = *reinterpret_cast<const uint4*>(vt + swz128(2 * qd + 8, r0));
-                const uint4 rd = *reinterpret_cast<const uint4*>(vt + swz128(2 * qd + 9, r0));
-                const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-                const uint32_t wc[4] = {rc.x, rc.y, rc.z, rc.w}, wd[4] = {rd.x, rd.y, rd.z, rd.w};
+                const uint32_t wa[4] = {va[0].x, va[0].y, va[0].z, va[0].w};
+                const uint32_t wb[4] = {va[1].x, va[1].y, va[1].z, va[1].w};
+                const uint32_t wc[4] = {va[2].x, va[2].y, va[2].z, va[2].w};
+                const uint32_t wd[4] = {va[3].x, va[3].y, va[3].z, va[3].w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
 #pragma unroll
                     for (int i = 0; i < 4; i += 2) {
                         const int j = 4 * w + i;
                         const uint32_t sel = i == 0 ? 0x5140u : 0x7362u;
-                        const uint32_t ab = __byte_perm(wa[w], wb[w], sel);
-                        const uint32_t cd = __byte_perm(wc[w], wd[w], sel);
-                        mma16816<false>(o[j], pa0, pa2, e4m3x2_to_f16x2(ab), e4m3x2_to_f16x2(cd));
-                        mma16816<false>(o[j + 1], pa0, pa2, e4m3x2_to_f16x2(ab >> 16), e4m3x2_to_f16x2(cd >> 16));
+                        uint32_t ab0, ab1, cd0, cd1;
+                        e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), ab0, ab1);
+                        e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), cd0, cd1);
+                        mma16816<false>(o[j], pa0, pa2, ab0, cd0);
+                        mma16816<false>(o[j + 1], pa0, pa2, ab1, cd1);
                     }
                 }
             }
@@ -348,45 +397,65 @@ __global__ void __launch_bounds__(NW * 32)
         }
     }
 
-    // ---- warp state -> shared memory ([G] m, [G] l, [G][D] acc)
+    // ---- warp state -> shared memory: [G] m, [G] l, then the accumulators
+    // in fragment order with a 33-word pitch (value (j, e) of lane l at
+    // 2G + (2j + e) * 33 + l): stores cover 32 consecutive words and the
+    // merge's reads of consecutive head dimensions fall in distinct banks.
     lsum += __shfl_xor_sync(kFull, lsum, 1);
     lsum += __shfl_xor_sync(kFull, lsum, 2);
     float* ws = reinterpret_cast<float*>(wbase);
     __syncwarp();
-    if (r0 < G) {
-        if (qd == 0) {
-            ws[r0] = aborted ? -INFINITY : m;
-            ws[G + r0] = aborted ? 0.f : lsum;
+    if (r0 < G && qd == 0) {
+        ws[r0] = aborted ? -INFINITY : m;
+        ws[G + r0] = aborted ? 0.f : lsum;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) ws[2 * G + (2 * j + e) * 33 + lane] = aborted ? 0.f : o[j][e];
+    __syncthreads();
+
+    // ---- cross-warp log-sum-exp weights, once per (warp, head)
+    float* msc = reinterpret_cast<float*>(smem + SM::kMergeOffset);  // [NW][8]
+    float* minv = msc + NW * 8;                                       // [8]
+    float* mden = minv + 8;                                           // [8]
+    if (threadIdx.x < G) {
+        const int g = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * NST * STAGE)[g]);
+        float den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float* wsw = reinterpret_cast<float*>(smem + w * NST * STAGE);
+            const float sc = (M != -INFINITY && wsw[g] != -INFINITY) ? exp2f(wsw[g] - M) : 0.f;
+            msc[w * 8 + g] = sc;
+            den = fmaf(sc, wsw[G + g], den);
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int d = kFP8 ? 16 * (2 * qd + e) + j : 8 * j + 2 * qd + e;
-                ws[2 * G + r0 * D + d] = aborted ? 0.f : o[j][e];
-            }
+        minv[g] = den > 0.f ? 1.f / den : 0.f;
+        mden[g] = den > 0.f ? den : 0.f;
     }
     __syncthreads();
 
     for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int g = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * NST * STAGE)[g]);
-        float num = 0.f, den = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float* wsw = reinterpret_cast<float*>(smem + w * NST * STAGE);
-                const float mw = wsw[g];
-                if (mw != -INFINITY) {
-                    const float sc = exp2f(mw - M);
-                    den = fmaf(sc, wsw[G + g], den);
-                    num = fmaf(sc, wsw[2 * G + g * D + d], num);
-                }
-            }
+        // inverse of the fragment order: head dimension d of row g
+        int j, e, q4;
+        if constexpr (kFP8) {
+            j = d & 15;
+            e = (d >> 4) & 1;
+            q4 = d >> 5;
+        } else {
+            j = d >> 3;
+            e = d & 1;
+            q4 = (d >> 1) & 3;
         }
-        const float out = den > 0.f ? num / den * p.v_scale : 0.f;
+        const int frag = 2 * G + (2 * j + e) * 33 + g * 4 + q4;
+        float num = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            num = fmaf(msc[w * 8 + g], reinterpret_cast<float*>(smem + w * NST * STAGE)[frag], num);
+        const float out = num * minv[g] * p.v_scale;
         const int64_t row = static_cast<int64_t>(s) * p.Hq + h * G + g;
         if (nparts == 1) {
             reinterpret_cast<typename QT::storage*>(p.out)[row * D + d] = from_float<QT>(out);
@@ -394,25 +463,22 @@ __global__ void __launch_bounds__(NW * 32)
             const int64_t prow = row * p.NP + part;
             p.part_o[prow * D + d] = out;
             if (d == 0) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * NST * STAGE)[g]);
                 p.part_m[prow] = M;
-                p.part_l[prow] = den;
+                p.part_l[prow] = mden[g];
             }
         }
     }
 }
 
 // ------------------------------------------------------------- launchers
-template <typename KT>
-constexpr int mma_stages() {
-    constexpr int st = kStageBudget / (kDecodeWarps * 2 * kBlockSize * 128 * KT::bytes);
-    return st < 2 ? 2 : (st > 8 ? 8 : st);
-}
-
 template <int G, typename KT, typename QT>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t st) {
     constexpr int NW = kDecodeWarps;
-    constexpr int NST = mma_stages<KT>();
+    constexpr int NST = MmaCfg<KT>::kStages;
     constexpr int SMEM = MmaSmem<KT, NW, NST>::kBytes;
     auto kern = decode_mma_kernel<G, KT, QT, NW, NST>;
     static bool configured[kMaxDevices] = {};

@@ -13,9 +13,12 @@
 namespace pkv {
 
 // Upper bound on mbarrier polls before a wait gives up and reports
-// PKV_DEVERR_TIMEOUT (each poll may suspend the warp for a while, so this is
-// seconds of wall time -- far beyond any legitimate copy latency).
-constexpr uint32_t kWaitLimit = 1u << 24;
+// PKV_DEVERR_TIMEOUT.  Each poll suspends the thread until the phase
+// completes or kWaitHintNs elapses, so the bound is at most about
+// kWaitLimit * kWaitHintNs = 1.6 s of wall time -- far beyond any legitimate
+// copy latency -- while a waiting warp issues few instructions.
+constexpr uint32_t kWaitLimit = 1u << 14;
+constexpr uint32_t kWaitHintNs = 100000;
 
 __device__ __forceinline__ void report(unsigned int* err, unsigned int bit) {
     atomicOr(err, bit);
@@ -44,10 +47,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitHintNs)
         : "memory");
     return ok != 0;
 }
