@@ -46,7 +46,13 @@ def _load():
     global _lib
     if _lib is None:
         build()
-        lib = ctypes.CDLL(_LIB)
+        _lib = bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def bind(lib):
+    """Declares the C signatures on a loaded oracle library and returns it."""
+    if True:
         P = ctypes.c_void_p
         i32, i64, f64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
         lib.pkvo_f16_to_double.argtypes = [ctypes.c_uint16]
@@ -71,8 +77,7 @@ def _load():
         lib.pkvo_copy_blocks.restype = i32
         lib.pkvo_num_threads.argtypes = []
         lib.pkvo_num_threads.restype = i32
-        _lib = lib
-    return _lib
+    return lib
 
 
 def _ptr(a: np.ndarray):
