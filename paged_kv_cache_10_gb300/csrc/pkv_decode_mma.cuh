@@ -4,30 +4,30 @@
 // Same computation as decode_kernel ("vLLM：大语言模型推理与服务库" section 4.4:
 // per query head, walk the block table, q . K -> softmax -> weighted V), same
 // grid (partition, kv head, sequence) and per-warp copy pipelines, but the
-// two products of a 16-token block run on the tensor cores:
+// two products of a 16-token block run on the tensor cores with the G query
+// heads of the group on the MMA's N = 8 columns:
 //
-//   S^T [16 x 16] = Q [16 x 128] . K^T [128 x 16]    (rows = query heads,
-//                                                      G of 16 used)
-//   O   [16 x 128] += P [16 x 16] . V [16 x 128]
+//   S   [16 tok x 8 heads]  = K   [16 x 128] . Q^T [128 x 8]   (8 MMAs)
+//   O^T [128 d  x 8 heads] += V^T [128 x 16] . P^T [16 x 8]     (8 MMAs)
 //
-// with mma.m16n8k16 (fp32 accumulate).  The GQA group gives an M = 16 tile
-// (G real rows); the newer 5th-generation MMA needs M >= 64, i.e. >= 8x
-// padding plus a tensor-memory round trip per block for the online
-// softmax, while this path keeps scores, probabilities and the output
-// accumulator in registers: the S^T accumulator fragment of the first
-// product is exactly the A-operand fragment of the second.
+// with mma.m16n8k16 and fp32 accumulation.  For G = 8 every column is used
+// (G = 4 / 2: half / a quarter).  The newer 5th-generation MMA needs M >= 64
+// and would round-trip the scores through tensor memory for the online
+// softmax every block; this path keeps scores, probabilities and output in
+// registers.  P goes from the accumulator layout of S to the B-operand
+// layout of P^T with two 8x8 register transposes (movmatrix).
 //
 // Tiles arrive through 2-D TMA tensor copies with the 128-byte swizzle
 // (16-byte chunk c of smem row r stored at chunk c ^ (r & 7)), so the
-// fragment loads below (ldmatrix for 16-bit pools; 16-byte loads for fp8)
-// are free of shared-memory bank conflicts.
+// fragment loads (ldmatrix for 16-bit pools; 16-byte loads for fp8) are free
+// of shared-memory bank conflicts.
 //
 // fp8 E4M3 pools: the MMA runs in f16.  Key and value bytes are turned into
 // f16 pairs in registers (hardware e4m3x2 -> f16x2 conversion, exact), with
-// the contraction index permuted so that each lane reads whole 16-byte
-// chunks: the k-th MMA column of lane quad member q covers head dimensions
-// 32q + 4k .. 32q + 4k + 3 for keys, and output column n of n-tile j is
-// head dimension 16n + j for values.  q is converted to f16 (exact in the
+// index permutations chosen so each lane reads whole 16-byte chunks: for
+// keys, contraction column k of lane quad member q covers head dimensions
+// 32q + 4k .. 32q + 4k + 3; for values, row g / g + 8 of m-tile i is head
+// dimension 16g + 2i / 16g + 2i + 1.  q is converted to f16 (exact in the
 // normal range).
 #pragma once
 
@@ -52,24 +52,31 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "r"(addr));
 }
 
-// D = A . B + D in place, with A rows 8..15 zero (a1 = a3 = 0): rows 8..15
-// of the accumulator start at zero and stay zero, so only d[0], d[1] carry
-// data, but the four registers stay one in-place group (no moves).
+// D = A . B + D in place, all four A registers given.
 template <bool BF>
-__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816a(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
     if constexpr (BF) {
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
             "{%0,%1,%2,%3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     } else {
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
             "{%0,%1,%2,%3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
     }
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held as one register per lane
+// (lane l holds row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22; -inf -> 0).
@@ -103,11 +110,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-
 template <bool BF>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     if constexpr (BF) {
@@ -130,8 +132,8 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // share the same bytes (its per-block instruction count is higher).
 template <typename KT>
 struct MmaCfg {
-    static constexpr int kStages = KT::bytes == 1 ? 4 : 2;
-    static constexpr int kCtasPerSm = 3;
+    static constexpr int kStages = KT::bytes == 1 ? 3 : 2;
+    static constexpr int kCtasPerSm = KT::bytes == 1 ? 4 : 3;
 };
 
 template <typename KT, int NW, int NST>
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = lane >> 2, qd = lane & 3;
+    const int g8 = lane >> 2, qd = lane & 3;  // fragment row group / quad member
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
 
     int L = __ldg(p.seq_lens + s);
@@ -225,35 +227,37 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
         ++k_issue;
     };
 
-    // ---- A fragments of Q (rows = heads of the group; rows >= G are zero)
-    uint32_t qa[8][2];
+    // ---- B fragments of Q^T (column n = head g8 of the group; heads >= G zero)
+    uint32_t qb[8][2];
     {
-        const int g = r0 < G ? r0 : 0;
+        const int g = g8 < G ? g8 : 0;
         const int64_t row = static_cast<int64_t>(s) * p.Hq + h * G + g;
         const unsigned char* qrow = static_cast<const unsigned char*>(p.q) + row * D * 2;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             if constexpr (!kFP8) {
-                qa[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * qd) * 2);
-                qa[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 8 + 2 * qd) * 2);
+                qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * qd) * 2);
+                qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 8 + 2 * qd) * 2);
             } else {
                 uint32_t w[2];
                 load_words<8>(qrow + (32 * qd + 4 * kk) * 2, w);
                 float f[4];
                 Unpack<QT, 4>::run(w, f);
-                qa[kk][0] = pack2<false>(f[0], f[1]);
-                qa[kk][1] = pack2<false>(f[2], f[3]);
+                qb[kk][0] = pack2<false>(f[0], f[1]);
+                qb[kk][1] = pack2<false>(f[2], f[3]);
             }
-            if (r0 >= G) qa[kk][0] = qa[kk][1] = 0u;
+            if (g8 >= G) qb[kk][0] = qb[kk][1] = 0u;
         }
     }
 
     for (int i = 0; i < NST && k_issue < nb_w; ++i) issue_next();
 
-    float o[16][4];
+    // O^T accumulators: m-tile i, c0/c1 = (row g8, heads 2qd, 2qd+1),
+    // c2/c3 = (row g8 + 8, heads 2qd, 2qd+1).
+    float o[8][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-    float m = -INFINITY, lsum = 0.f;
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // heads 2qd (A), 2qd+1 (B)
 
     bool aborted = false;
     for (int k = 0; k < nb_w; ++k) {
@@ -282,88 +286,93 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                 }
                 __syncwarp();
             }
-            // fp8: value fragments are loaded up front so their latency hides
-            // behind Q K^T (chunk r0 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9)
+            // fp8: value bytes loaded up front (chunk g8 of tokens 2qd, 2qd+1,
+            // 2qd+8, 2qd+9) so their latency hides behind K Q^T
             uint4 va[4];
             if constexpr (kFP8) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tok = 2 * qd + (i & 1) + 8 * (i >> 1);
-                    va[i] = *reinterpret_cast<const uint4*>(vt + swz128(tok, r0));
+                    va[i] = *reinterpret_cast<const uint4*>(vt + swz128(tok, g8));
                 }
             }
-            // ---- S^T = Q K^T  (n-tile j = tokens 8j .. 8j+7)
+            // ---- S = K Q^T, two accumulators (even / odd k-steps) to halve the chain
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if constexpr (!kFP8) {
-                const int mat = lane >> 3, rr = lane & 7;
-                const int tok = rr + 8 * (mat >> 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int chunk = 2 * kk + (mat & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), b0, b1, b2, b3);
-                    mma16816<kBF>(sa[0], qa[kk][0], qa[kk][1], b0, b1);
-                    mma16816<kBF>(sa[1], qa[kk][0], qa[kk][1], b2, b3);
-                }
-            } else {
-                uint32_t w[2][8];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int tok = 8 * j + r0;
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(kt + swz128(tok, 2 * qd));
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(kt + swz128(tok, 2 * qd + 1));
-                    w[j][0] = c0.x; w[j][1] = c0.y; w[j][2] = c0.z; w[j][3] = c0.w;
-                    w[j][4] = c1.x; w[j][5] = c1.y; w[j][6] = c1.z; w[j][7] = c1.w;
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        uint32_t blo, bhi;
-                        e4m3x4_to_f16x4(w[j][kk], blo, bhi);
-                        mma16816<false>(sa[j], qa[kk][0], qa[kk][1], blo, bhi);
-                    }
-                }
-            }
-            // ---- online softmax on row r0 (tokens 2qd, 2qd+1, 8+2qd, 9+2qd)
-            float sv[4] = {sa[0][0] * p.qk_scale, sa[0][1] * p.qk_scale, sa[1][0] * p.qk_scale,
-                           sa[1][1] * p.qk_scale};
-            if (nvalid < kBlockSize) {
-                const int tk[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (tk[i] >= nvalid) sv[i] = -INFINITY;
-            }
-            float bm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
-            bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
-            const float mn = fmaxf(m, bm);
-            const float alpha = mn == m ? 1.f : ex2(m - mn);
-            m = mn;
-            float pr[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pr[i] = ex2(sv[i] - mn);
-            lsum = lsum * alpha + (pr[0] + pr[1]) + (pr[2] + pr[3]);
-            const uint32_t pa0 = pack2<kBF>(pr[0], pr[1]);
-            const uint32_t pa2 = pack2<kBF>(pr[2], pr[3]);
-            if (__any_sync(kFull, alpha != 1.f)) {  // skip when no row's max moved
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    o[j][0] *= alpha;
-                    o[j][1] *= alpha;
-                }
-            }
-            // ---- O += P V
             if constexpr (!kFP8) {
                 const int mat = lane >> 3, rr = lane & 7;
                 const int tok = rr + 8 * (mat & 1);
 #pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int chunk = 2 * kk + (mat >> 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
+                    mma16816a<kBF>(sa[kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+                }
+            } else {
+                uint32_t w0[8], w1[8];
+                {
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(kt + swz128(g8, 2 * qd));
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(kt + swz128(g8, 2 * qd + 1));
+                    const uint4 c2 = *reinterpret_cast<const uint4*>(kt + swz128(g8 + 8, 2 * qd));
+                    const uint4 c3 = *reinterpret_cast<const uint4*>(kt + swz128(g8 + 8, 2 * qd + 1));
+                    w0[0] = c0.x; w0[1] = c0.y; w0[2] = c0.z; w0[3] = c0.w;
+                    w0[4] = c1.x; w0[5] = c1.y; w0[6] = c1.z; w0[7] = c1.w;
+                    w1[0] = c2.x; w1[1] = c2.y; w1[2] = c2.z; w1[3] = c2.w;
+                    w1[4] = c3.x; w1[5] = c3.y; w1[6] = c3.z; w1[7] = c3.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint32_t a01, a45, a23, a67;
+                    e4m3x4_to_f16x4(w0[kk], a01, a45);
+                    e4m3x4_to_f16x4(w1[kk], a23, a67);
+                    mma16816a<false>(sa[kk & 1], a01, a23, a45, a67, qb[kk][0], qb[kk][1]);
+                }
+            }
+            // ---- online softmax: s0 (tok g8, head A), s1 (tok g8, head B),
+            //      s2 (tok g8+8, head A), s3 (tok g8+8, head B)
+            float sv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sv[c] = (sa[0][c] + sa[1][c]) * p.qk_scale;
+            if (nvalid < kBlockSize) {
+                if (g8 >= nvalid) sv[0] = sv[1] = -INFINITY;
+                if (g8 + 8 >= nvalid) sv[2] = sv[3] = -INFINITY;
+            }
+            float bA = fmaxf(sv[0], sv[2]), bB = fmaxf(sv[1], sv[3]);
+#pragma unroll
+            for (int mask = 4; mask < 32; mask <<= 1) {
+                bA = fmaxf(bA, __shfl_xor_sync(kFull, bA, mask));
+                bB = fmaxf(bB, __shfl_xor_sync(kFull, bB, mask));
+            }
+            const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
+            const float alA = nA == mA ? 1.f : ex2(mA - nA);
+            const float alB = nB == mB ? 1.f : ex2(mB - nB);
+            mA = nA;
+            mB = nB;
+            const float p0 = ex2(sv[0] - nA), p1 = ex2(sv[1] - nB), p2 = ex2(sv[2] - nA), p3 = ex2(sv[3] - nB);
+            lA = lA * alA + (p0 + p2);
+            lB = lB * alB + (p1 + p3);
+            if (__any_sync(kFull, alA != 1.f || alB != 1.f)) {  // skip when no head's max moved
+#pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int chunk = 2 * i + (mat >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), b0, b1, b2, b3);
-                    mma16816<kBF>(o[2 * i], pa0, pa2, b0, b1);
-                    mma16816<kBF>(o[2 * i + 1], pa0, pa2, b2, b3);
+                    o[i][0] *= alA;
+                    o[i][1] *= alB;
+                    o[i][2] *= alA;
+                    o[i][3] *= alB;
+                }
+            }
+            // P^T fragments: transpose the (token, head) 8x8 tiles of P
+            const uint32_t pb0 = movmatrix_t(pack2<kBF>(p0, p1));  // tokens 0..7
+            const uint32_t pb1 = movmatrix_t(pack2<kBF>(p2, p3));  // tokens 8..15
+            // ---- O^T += V^T P^T
+            if constexpr (!kFP8) {
+                const int mat = lane >> 3, rr = lane & 7;
+                const int tok = rr + 8 * (mat >> 1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int chunk = 2 * i + (mat & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(vts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
+                    mma16816a<kBF>(o[i], a0, a1, a2, a3, pb0, pb1);
                 }
             } else {
                 const uint32_t wa[4] = {va[0].x, va[0].y, va[0].z, va[0].w};
@@ -371,17 +380,13 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                 const uint32_t wc[4] = {va[2].x, va[2].y, va[2].z, va[2].w};
                 const uint32_t wd[4] = {va[3].x, va[3].y, va[3].z, va[3].w};
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                    for (int i = 0; i < 4; i += 2) {
-                        const int j = 4 * w + i;
-                        const uint32_t sel = i == 0 ? 0x5140u : 0x7362u;
-                        uint32_t ab0, ab1, cd0, cd1;
-                        e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), ab0, ab1);
-                        e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), cd0, cd1);
-                        mma16816<false>(o[j], pa0, pa2, ab0, cd0);
-                        mma16816<false>(o[j + 1], pa0, pa2, ab1, cd1);
-                    }
+                for (int i = 0; i < 8; ++i) {
+                    const int w = i >> 1;
+                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2i, 2i+1 of the chunk
+                    uint32_t a01, a23, a45, a67;
+                    e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), a01, a23);
+                    e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), a45, a67);
+                    mma16816a<false>(o[i], a01, a23, a45, a67, pb0, pb1);
                 }
             }
         }
@@ -397,22 +402,26 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
         }
     }
 
-    // ---- warp state -> shared memory: [G] m, [G] l, then the accumulators
-    // in fragment order with a 33-word pitch (value (j, e) of lane l at
-    // 2G + (2j + e) * 33 + l): stores cover 32 consecutive words and the
-    // merge's reads of consecutive head dimensions fall in distinct banks.
-    lsum += __shfl_xor_sync(kFull, lsum, 1);
-    lsum += __shfl_xor_sync(kFull, lsum, 2);
+    // ---- warp state -> shared memory: [8] m, [8] l, then the accumulators in
+    // fragment order with a 33-word pitch (value c of m-tile i of lane l at
+    // 16 + (4i + c) * 33 + l).
+#pragma unroll
+    for (int mask = 4; mask < 32; mask <<= 1) {
+        lA += __shfl_xor_sync(kFull, lA, mask);
+        lB += __shfl_xor_sync(kFull, lB, mask);
+    }
     float* ws = reinterpret_cast<float*>(wbase);
     __syncwarp();
-    if (r0 < G && qd == 0) {
-        ws[r0] = aborted ? -INFINITY : m;
-        ws[G + r0] = aborted ? 0.f : lsum;
+    if (g8 == 0) {
+        ws[2 * qd] = aborted ? -INFINITY : mA;
+        ws[2 * qd + 1] = aborted ? -INFINITY : mB;
+        ws[8 + 2 * qd] = aborted ? 0.f : lA;
+        ws[8 + 2 * qd + 1] = aborted ? 0.f : lB;
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) ws[2 * G + (2 * j + e) * 33 + lane] = aborted ? 0.f : o[j][e];
+        for (int c = 0; c < 4; ++c) ws[16 + (4 * i + c) * 33 + lane] = aborted ? 0.f : o[i][c];
     __syncthreads();
 
     // ---- cross-warp log-sum-exp weights, once per (warp, head)
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
             const float* wsw = reinterpret_cast<float*>(smem + w * NST * STAGE);
             const float sc = (M != -INFINITY && wsw[g] != -INFINITY) ? exp2f(wsw[g] - M) : 0.f;
             msc[w * 8 + g] = sc;
-            den = fmaf(sc, wsw[G + g], den);
+            den = fmaf(sc, wsw[8 + g], den);
         }
         minv[g] = den > 0.f ? 1.f / den : 0.f;
         mden[g] = den > 0.f ? den : 0.f;
@@ -439,18 +448,19 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
 
     for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int g = idx / D, d = idx % D;
-        // inverse of the fragment order: head dimension d of row g
-        int j, e, q4;
+        // inverse of the fragment layout: head g, head dimension d
+        int i, upper, gl;
         if constexpr (kFP8) {
-            j = d & 15;
-            e = (d >> 4) & 1;
-            q4 = d >> 5;
+            gl = d >> 4;
+            i = (d & 15) >> 1;
+            upper = d & 1;
         } else {
-            j = d >> 3;
-            e = d & 1;
-            q4 = (d >> 1) & 3;
+            i = d >> 4;
+            upper = (d >> 3) & 1;
+            gl = d & 7;
         }
-        const int frag = 2 * G + (2 * j + e) * 33 + g * 4 + q4;
+        const int c = 2 * upper + (g & 1);
+        const int frag = 16 + (4 * i + c) * 33 + 4 * gl + (g >> 1);
         float num = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w)
