@@ -352,17 +352,23 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
 // Log-sum-exp merge of the split-K partials, one CTA of kMergeThreads per
 // (sequence, query head) row: M = max_p m_p, w_p = l_p 2^(m_p - M),
 // out = sum_p w_p o_p / sum_p w_p.  The weights of a chunk of partitions
-// are computed once into shared memory; then thread d walks the chunk with
-// 8 independent loads in flight (each a coalesced row of partial outputs).
-// Rows of single-partition sequences were written by the main kernel and are
-// skipped.
-constexpr int kMergeThreads = 128;
+// are computed once into shared memory; the kMergeThreads / D thread groups
+// then each walk every (kMergeThreads / D)-th partition of the chunk for
+// their head dimension d with 16 independent loads in flight (each load a
+// coalesced row of partial outputs), and the groups' sums are added in
+// shared memory.  Rows of single-partition sequences were written by the
+// main kernel and are skipped.
+constexpr int kMergeThreads = 256;
 
 template <int D, typename QT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+    constexpr int NG = kMergeThreads / D;  // thread groups sharing one head dimension
     __shared__ float w_s[kMergeThreads];
     __shared__ float red[kMergeThreads / 32];
+    __shared__ float part_acc[kMergeThreads];
+    __shared__ float part_den[kMergeThreads];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = tid % D, grp = tid / D;
     const int64_t row = blockIdx.x;
     const int s = static_cast<int>(row / p.Hq);
     int L = __ldg(p.seq_lens + s);
@@ -394,29 +400,37 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
                 w_s[tid] = l > 0.f ? l * exp2f(pm[base + tid] - M) : 0.f;
             }
             __syncthreads();
-            if (tid < D) {
-                const float* o = po + static_cast<int64_t>(base) * D + tid;
-                int j = 0;
-                for (; j + 8 <= cnt; j += 8) {
-                    float v[8];
+            const float* o = po + static_cast<int64_t>(base) * D + d;
+            int j = grp;
+            for (; j + 15 * NG < cnt; j += 16 * NG) {
+                float v[16];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) v[u] = o[(j + u) * D];
+                for (int u = 0; u < 16; ++u) v[u] = o[(j + u * NG) * D];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        acc = fmaf(w_s[j + u], v[u], acc);
-                        den += w_s[j + u];
-                    }
+                for (int u = 0; u < 16; ++u) {
+                    acc = fmaf(w_s[j + u * NG], v[u], acc);
+                    den += w_s[j + u * NG];
                 }
-                for (; j < cnt; ++j) {
-                    acc = fmaf(w_s[j], o[j * D], acc);
-                    den += w_s[j];
-                }
+            }
+            for (; j < cnt; j += NG) {
+                acc = fmaf(w_s[j], o[j * D], acc);
+                den += w_s[j];
             }
         }
     }
-    if (tid < D) {
+    // combine the groups' partial sums for each head dimension
+    part_acc[tid] = acc;
+    part_den[tid] = den;
+    __syncthreads();
+    if (grp == 0) {
+        float a = acc, dn = den;
+#pragma unroll
+        for (int q = 1; q < NG; ++q) {
+            a += part_acc[q * D + d];
+            dn += part_den[q * D + d];
+        }
         auto* out = reinterpret_cast<typename QT::storage*>(p.out) + row * D;
-        out[tid] = from_float<QT>(den > 0.f ? acc / den : 0.f);
+        out[d] = from_float<QT>(dn > 0.f ? a / dn : 0.f);
     }
 }
 
