@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include "pkv_decode_impl.cuh"
+#include "pkv_merge.cuh"
 
 namespace pkv {
 
@@ -31,16 +32,23 @@ unsigned int* error_word() {
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st) {
     const int64_t rows = static_cast<int64_t>(p.S) * p.Hq;
     const dim3 grid(static_cast<unsigned>(rows));
+    const bool narrow = p.NP <= kMergeNarrowMaxParts;
     if (q_dtype == PKV_BF16) {
-        if (p.D == 128)
-            merge_kernel<128, BF16><<<grid, kMergeThreads, 0, st>>>(p);
-        else
-            merge_kernel<64, BF16><<<grid, kMergeThreads, 0, st>>>(p);
+        if (p.D == 128) {
+            if (narrow) merge_kernel<128, BF16, 128><<<grid, 128, 0, st>>>(p);
+            else merge_kernel<128, BF16, 256><<<grid, 256, 0, st>>>(p);
+        } else {
+            if (narrow) merge_kernel<64, BF16, 128><<<grid, 128, 0, st>>>(p);
+            else merge_kernel<64, BF16, 256><<<grid, 256, 0, st>>>(p);
+        }
     } else {
-        if (p.D == 128)
-            merge_kernel<128, F16><<<grid, kMergeThreads, 0, st>>>(p);
-        else
-            merge_kernel<64, F16><<<grid, kMergeThreads, 0, st>>>(p);
+        if (p.D == 128) {
+            if (narrow) merge_kernel<128, F16, 128><<<grid, 128, 0, st>>>(p);
+            else merge_kernel<128, F16, 256><<<grid, 256, 0, st>>>(p);
+        } else {
+            if (narrow) merge_kernel<64, F16, 128><<<grid, 128, 0, st>>>(p);
+            else merge_kernel<64, F16, 256><<<grid, 256, 0, st>>>(p);
+        }
     }
     return cudaGetLastError();
 }

@@ -1,0 +1,103 @@
+// pkv_merge.cuh -- log-sum-exp merge of split-K decode partials.
+//
+// The pages give only the partition axis of the decode grid (openEuler essay
+// on vLLM, "PagedAttention：把操作系统的分页搬上 GPU": grid (num_heads,
+// num_seqs, max_num_partitions)); the reduce is the standard log-sum-exp
+// identity over the partitions' (max, sum, normalised output).
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+constexpr unsigned kMergeFull = 0xffffffffu;
+
+// Log-sum-exp merge of the split-K partials, one CTA of kMergeThreads per
+// (sequence, query head) row: M = max_p m_p, w_p = l_p 2^(m_p - M),
+// out = sum_p w_p o_p / sum_p w_p.  The weights of a chunk of partitions
+// are computed once into shared memory; the kMergeThreads / D thread groups
+// then each walk every (kMergeThreads / D)-th partition of the chunk for
+// their head dimension d with 16 independent loads in flight (each load a
+// coalesced row of partial outputs), and the groups' sums are added in
+// shared memory.  Rows of single-partition sequences were written by the
+// main kernel and are skipped.
+template <int D, typename QT, int kMergeThreads>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+    constexpr int NG = kMergeThreads / D;  // thread groups sharing one head dimension
+    __shared__ float w_s[kMergeThreads];
+    __shared__ float red[kMergeThreads / 32];
+    __shared__ float part_acc[kMergeThreads];
+    __shared__ float part_den[kMergeThreads];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = tid % D, grp = tid / D;
+    const int64_t row = blockIdx.x;
+    const int s = static_cast<int>(row / p.Hq);
+    int L = __ldg(p.seq_lens + s);
+    const int Lmax = min(p.MB * kBlockSize, p.NP * p.P);
+    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
+    const int nparts = L > 0 ? (L + p.P - 1) / p.P : 1;
+    if (nparts <= 1) return;
+    const float* pm = p.part_m + row * p.NP;
+    const float* pl = p.part_l + row * p.NP;
+    const float* po = p.part_o + row * p.NP * D;
+
+    float M = -INFINITY;
+    for (int i = tid; i < nparts; i += kMergeThreads) M = fmaxf(M, pm[i]);
+#pragma unroll
+    for (int mask = 16; mask > 0; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kMergeFull, M, mask));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
+
+    float acc = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+        for (int base = 0; base < nparts; base += kMergeThreads) {
+            const int cnt = min(kMergeThreads, nparts - base);
+            __syncthreads();  // previous chunk's weights fully consumed
+            if (tid < cnt) {
+                const float l = pl[base + tid];
+                w_s[tid] = l > 0.f ? l * exp2f(pm[base + tid] - M) : 0.f;
+            }
+            __syncthreads();
+            const float* o = po + static_cast<int64_t>(base) * D + d;
+            int j = grp;
+            for (; j + 15 * NG < cnt; j += 16 * NG) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = o[(j + u * NG) * D];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    acc = fmaf(w_s[j + u * NG], v[u], acc);
+                    den += w_s[j + u * NG];
+                }
+            }
+            for (; j < cnt; j += NG) {
+                acc = fmaf(w_s[j], o[j * D], acc);
+                den += w_s[j];
+            }
+        }
+    }
+    // combine the groups' partial sums for each head dimension
+    part_acc[tid] = acc;
+    part_den[tid] = den;
+    __syncthreads();
+    if (grp == 0) {
+        float a = acc, dn = den;
+#pragma unroll
+        for (int q = 1; q < NG; ++q) {
+            a += part_acc[q * D + d];
+            dn += part_den[q * D + d];
+        }
+        auto* out = reinterpret_cast<typename QT::storage*>(p.out) + row * D;
+        out[d] = from_float<QT>(dn > 0.f ? a / dn : 0.f);
+    }
+}
+
+// Threads per merge CTA: rows with few partitions are latency-bound on the
+// CTA's own steps, so they get a narrow CTA; many partitions get two groups
+// per head dimension to double the loads in flight.
+constexpr int kMergeNarrowMaxParts = 16;
+
+}  // namespace pkv
