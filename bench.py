@@ -47,6 +47,8 @@ _CSRC = "paged_kv_cache_10_gb300/csrc/"
 KERNEL_SOURCES = {
     "cuda_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh"],
     "tensor_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh"],
+    "cascade": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh",
+                _CSRC + "pkv_cascade.cu"],
 }
 
 
@@ -233,7 +235,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl = workloads.NAMED[args.workload]()
-    step = DecodeStep(wl, device=dev, partition_tokens=args.partition)
+    step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=args.cascade)
     nbytes = step_bytes(step)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -334,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     dec_ms = statistics.mean(decode_ms)
     achieved = nbytes["decode"] / (dec_ms / 1e3) / 1e9
-    kind = decode_kernel_kind(wl)
+    kind = decode_kernel_kind(wl) if not args.cascade else "cascade"
     traffic = recorded_traffic(args.workload, kind)
     ms_per_step = total_ms / K
     line = {
@@ -359,6 +361,8 @@ def run_ours(args, rank, world, local_rank):
             "block_size": wl.b, "kv_dtype": wl.kv_dtype, "num_blocks": wl.NB, "max_seq_len": step.max_seq_len,
             "mean_seq_len": float(step.seq_lens.mean()), "partition_tokens": step.effective_partition(),
             "cow_pairs": int(len(step.pairs)), "appended_tokens": int((step.slots >= 0).sum()),
+            "decode": ("cascade: %d groups, prefix up to %d blocks" % (step.groups.num_groups, step.groups.max_blocks)
+                       if step.cascade else "plain"),
             "bytes_per_step": nbytes, "l2": ("flushed between steps (2x L2 write)" if flush else
                                              f"inputs larger than L2 ({working_set / 2**20:.0f} MiB vs "
                                              f"{l2 / 2**20:.0f} MiB), no flush"),
@@ -369,8 +373,10 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": ("decode_mma_kernel" if kind == "tensor_core" else "decode_kernel")
-                     + " (+ merge_kernel when split)", "kernel_sources_hash": kernel_hash(kind),
+                     "kernel": {"tensor_core": "decode_mma_kernel (+ merge_kernel when split)",
+                                "cuda_core": "decode_kernel (+ merge_kernel when split)",
+                                "cascade": "cascade_prefix_kernel + decode kernel + merge_kernel"}[kind],
+                     "kernel_sources_hash": kernel_hash(kind),
                      "mean_launch_us": round(dec_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": nbytes["decode"]},
         "clocks": clocks,
@@ -436,6 +442,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--partition", type=int, default=None, help="tokens per split-K partition (0 = auto)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="timed steps only (no e2e loop, clock-window extension or CPU baseline): for ncu runs")

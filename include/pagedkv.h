@@ -212,6 +212,50 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
                                               int32_t partition_tokens, void* stream);
 
 /*
+ * Shared-prefix ("cascade") decode attention: the same function as
+ * pkv_paged_attention_decode, computed so that blocks shared by a group of
+ * sequences are read once per group rather than once per sequence.  Shared
+ * blocks arise from fork, prefix sharing and parallel sampling ([P4]
+ * "Prefix Caching 与 Copy-on-Write"; [P1] "束搜索与并行采样的三大调度原语").
+ * Each member's attention is split into the group's shared leading blocks
+ * (all member query heads attend to them together, on the tensor cores) and
+ * the member's own remaining tokens; the two are combined exactly by the
+ * log-sum-exp merge.
+ *
+ * Arguments as for pkv_paged_attention_decode, plus the groups (device
+ * int32 arrays, as produced by pkv_alloc_prefix_groups):
+ *   seq_group[num_seqs]: group of each batch row, or -1;
+ *   group_blocks[num_groups]: leading blocks shared by every member -- the
+ *     first group_blocks[g] entries of every member's block table must be
+ *     identical and each of those blocks full (16 valid tokens);
+ *   group_offsets[num_groups + 1], group_members[]: CSR list of the batch
+ *     rows of each group;
+ *   max_group_members, max_group_blocks: host bounds of the two (size the
+ *     launch).
+ * workspace must hold pkv_decode_cascade_workspace_bytes(...) bytes.
+ * Implemented for f16 / bf16 pools (q of the same type), head_size 128,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; fp8 pools return
+ * PKV_ERR_UNSUPPORTED.  A member index or block count out of range sets
+ * PKV_DEVERR_SEQ_LEN and the offending rows are skipped.
+ */
+pkv_status pkv_paged_attention_decode_cascade(const void* q, int32_t q_dtype, int32_t num_seqs,
+                                              int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                              const pkv_cache_desc* desc, const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                              int32_t max_seq_len, const int32_t* seq_group,
+                                              const int32_t* group_blocks, const int32_t* group_offsets,
+                                              const int32_t* group_members, int32_t num_groups,
+                                              int32_t max_group_members, int32_t max_group_blocks, float scale,
+                                              void* out, void* workspace, size_t workspace_bytes,
+                                              int32_t partition_tokens, void* stream);
+
+/* Workspace bytes of pkv_paged_attention_decode_cascade (0 on invalid sizes;
+ * partition_tokens = 0 sizes for the automatic choice's largest case). */
+size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
+                                          int32_t max_seq_len, int32_t partition_tokens,
+                                          int32_t max_group_blocks);
+
+/*
  * Partition size the automatic choice (partition_tokens = 0) would use for
  * these sizes on the current device, or a negative pkv_status on error.
  */
@@ -310,6 +354,19 @@ pkv_status pkv_alloc_seq_len(const pkv_alloc* a, int64_t seq_id, int64_t* n);
 int32_t pkv_alloc_refcount(const pkv_alloc* a, int32_t block);
 int32_t pkv_alloc_num_free(const pkv_alloc* a);
 int32_t pkv_alloc_num_seqs(const pkv_alloc* a);
+/* Groups of batch rows that share leading blocks, for cascade decode.  Rows
+ * (seq_ids[i] >= 0) with at least min_blocks full blocks are bucketed by their
+ * first block id; a bucket of two or more rows becomes a group whose shared
+ * prefix is the longest run of identical leading block ids, counting only
+ * blocks full in every member, if that run is >= min_blocks.  Outputs:
+ * seq_group[n] (-1 when ungrouped), group_blocks[*num_groups],
+ * group_offsets[*num_groups + 1], group_members (batch rows; capacity n),
+ * the largest group and the largest prefix.  Capacities of group_blocks and
+ * group_offsets: n and n + 1. */
+pkv_status pkv_alloc_prefix_groups(const pkv_alloc* a, const int64_t* seq_ids, int32_t n, int32_t min_blocks,
+                                   int32_t* seq_group, int32_t* group_blocks, int32_t* group_offsets,
+                                   int32_t* group_members, int32_t* num_groups, int32_t* max_members,
+                                   int32_t* max_blocks);
 /* Fault injection for tests: the k-th block allocation from now (k >= 1)
  * fails as if the pool were empty; k <= 0 disables. */
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k);

@@ -16,6 +16,7 @@
 // Every public call is all-or-nothing: failures leave the state unchanged
 // (OOM returns a status instead of throwing).
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -312,6 +313,62 @@ int32_t pkv_alloc_num_free(const pkv_alloc* a) {
 
 int32_t pkv_alloc_num_seqs(const pkv_alloc* a) {
     return a ? static_cast<int32_t>(a->seqs.size()) : -1;
+}
+
+pkv_status pkv_alloc_prefix_groups(const pkv_alloc* a, const int64_t* seq_ids, int32_t n, int32_t min_blocks,
+                                   int32_t* seq_group, int32_t* group_blocks, int32_t* group_offsets,
+                                   int32_t* group_members, int32_t* num_groups, int32_t* max_members,
+                                   int32_t* max_blocks) {
+    if (!a || n < 0 || min_blocks < 1 || !num_groups || !max_members || !max_blocks) return PKV_ERR_INVALID;
+    if (n > 0 && (!seq_ids || !seq_group || !group_blocks || !group_offsets || !group_members)) return PKV_ERR_INVALID;
+    std::vector<const Seq*> seqs(n, nullptr);
+    for (int32_t i = 0; i < n; ++i) {
+        if (seq_ids[i] < 0) continue;
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+        seqs[i] = &it->second;
+    }
+    // Bucket rows by their first block, in order of first appearance.
+    std::vector<int32_t> order;
+    std::unordered_map<int32_t, std::vector<int32_t>> buckets;
+    for (int32_t i = 0; i < n; ++i) {
+        seq_group[i] = -1;
+        if (!seqs[i] || seqs[i]->len / a->block_size < min_blocks) continue;
+        const int32_t first = seqs[i]->blocks[0];
+        auto& b = buckets[first];
+        if (b.empty()) order.push_back(first);
+        b.push_back(i);
+    }
+    int32_t ng = 0, nm = 0, mm = 0, mb = 0;
+    group_offsets[0] = 0;
+    for (int32_t key : order) {
+        const std::vector<int32_t>& rows = buckets[key];
+        if (rows.size() < 2) continue;
+        // longest common run of identical leading block ids, full blocks only
+        int64_t lcp = seqs[rows[0]]->len / a->block_size;
+        for (int32_t r : rows) lcp = std::min<int64_t>(lcp, seqs[r]->len / a->block_size);
+        for (size_t k = 1; k < rows.size(); ++k) {
+            const std::vector<int32_t>& x = seqs[rows[0]]->blocks;
+            const std::vector<int32_t>& y = seqs[rows[k]]->blocks;
+            int64_t j = 0;
+            while (j < lcp && x[j] == y[j]) ++j;
+            lcp = j;
+        }
+        if (lcp < min_blocks) continue;
+        group_blocks[ng] = static_cast<int32_t>(lcp);
+        for (int32_t r : rows) {
+            seq_group[r] = ng;
+            group_members[nm++] = r;
+        }
+        group_offsets[ng + 1] = nm;
+        mm = std::max<int32_t>(mm, static_cast<int32_t>(rows.size()));
+        mb = std::max<int32_t>(mb, static_cast<int32_t>(lcp));
+        ++ng;
+    }
+    *num_groups = ng;
+    *max_members = mm;
+    *max_blocks = mb;
+    return PKV_OK;
 }
 
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k) {

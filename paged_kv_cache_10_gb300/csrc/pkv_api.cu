@@ -66,8 +66,8 @@ int num_sms() {
 }
 
 namespace {
-
 std::atomic<int> g_decode_path{0};  // 0 auto, 1 CUDA cores, 2 tensor cores
+}  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -99,12 +99,11 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t
     return r == CUDA_SUCCESS;
 }
 
-// Smallest partition the automatic choice uses (sizes the P = 0 workspace).
-constexpr int kAutoMinPartition = 256;
-
+namespace {
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
 
 // Tokens per split-K partition when the caller passes 0.  Enough CTAs for a
 // few waves of resident CTAs keep the SMs evenly loaded when sequence
@@ -126,15 +125,28 @@ int auto_partition(int S, int Hkv, int max_seq_len) {
     return static_cast<int>(P);
 }
 
-size_t workspace_bytes(int64_t S, int64_t Hq, int64_t D, int64_t max_seq_len, int64_t P) {
-    const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
-    if (NP <= 1) return 0;
+size_t partials_bytes(int64_t S, int64_t Hq, int64_t D, int64_t NP) {
     // m, l and o rows, each region 256-byte aligned
     const int64_t rows = S * Hq * NP;
     const int64_t ml = ceil_div(rows * 4, 256) * 256;
     return static_cast<size_t>(2 * ml + rows * D * 4);
 }
 
+void partials_layout(DecodeParams& p, void* workspace) {
+    const int64_t rows = static_cast<int64_t>(p.S) * p.Hq * p.NP;
+    const int64_t ml = ceil_div(rows * 4, 256) * 256;
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    p.part_m = reinterpret_cast<float*>(w);
+    p.part_l = reinterpret_cast<float*>(w + ml);
+    p.part_o = reinterpret_cast<float*>(w + 2 * ml);
+}
+
+namespace {
+size_t workspace_bytes(int64_t S, int64_t Hq, int64_t D, int64_t max_seq_len, int64_t P) {
+    const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
+    if (NP <= 1) return 0;
+    return partials_bytes(S, Hq, D, NP);
+}
 }  // namespace
 }  // namespace pkv
 
@@ -223,14 +235,7 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
     p.qk_scale = scale * log2e * (d->kv_dtype == PKV_FP8_E4M3 ? d->k_scale : 1.f);
     p.v_scale = d->kv_dtype == PKV_FP8_E4M3 ? d->v_scale : 1.f;
     p.err = err;
-    if (need > 0) {
-        const int64_t rows = static_cast<int64_t>(num_seqs) * num_q_heads * NP;
-        const int64_t ml = ceil_div(rows * 4, 256) * 256;
-        unsigned char* w = static_cast<unsigned char*>(workspace);
-        p.part_m = reinterpret_cast<float*>(w);
-        p.part_l = reinterpret_cast<float*>(w + ml);
-        p.part_o = reinterpret_cast<float*>(w + 2 * ml);
-    }
+    if (need > 0) partials_layout(p, workspace);
 
     // Tensor-core kernel for grouped-query heads at head_size 128; CUDA
     // cores otherwise (one query row per KV head is not a dense tile).

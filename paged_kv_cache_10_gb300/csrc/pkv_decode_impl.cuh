@@ -96,15 +96,24 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     const int hf = lane >> 4, li = lane & 15;
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
 
+    // Sequence length, clamped to the block table's reach and to the
+    // partitions this launch covers; the sequence's own range starts after
+    // its shared prefix (cascade decode) or at 0.
     int L = __ldg(p.seq_lens + s);
-    const int Lmax = min(p.MB * kBlockSize, p.NP * p.P);  // the table's and the launch's reach
-    if (L < 0 || L > Lmax) {
-        if (threadIdx.x == 0 && part == 0 && h == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-        L = L < 0 ? 0 : Lmax;
+    const int Lcap = p.MB * kBlockSize;
+    bool bad = L < 0 || L > Lcap;
+    L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
+    const int start = own_start(p.seq_group, p.group_blocks, s, L, &bad);
+    int Lown = L - start;
+    if (Lown > (p.NP - p.part_base) * p.P) {
+        bad = true;
+        Lown = (p.NP - p.part_base) * p.P;
+        L = start + Lown;
     }
-    const int nparts = L > 0 ? (L + p.P - 1) / p.P : 1;
+    if (bad && threadIdx.x == 0 && part == 0 && h == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+    const int nparts = Lown > 0 ? (Lown + p.P - 1) / p.P : (p.cascade ? 0 : 1);
     if (part >= nparts) return;
-    const int t0 = part * p.P;
+    const int t0 = start + part * p.P;
     const int t1 = min(L, t0 + p.P);
     const int j0 = t0 / kBlockSize;
     const int nblk = (t1 + kBlockSize - 1) / kBlockSize - j0;
@@ -336,10 +345,10 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
         }
         const float o = den > 0.f ? num / den * p.v_scale : 0.f;
         const int64_t row = static_cast<int64_t>(s) * p.Hq + h * G + g;
-        if (nparts == 1) {
+        if (nparts == 1 && !p.cascade) {
             reinterpret_cast<typename QT::storage*>(p.out)[row * D + d] = from_float<QT>(o);
         } else {
-            const int64_t prow = row * p.NP + part;
+            const int64_t prow = row * p.NP + p.part_base + part;
             p.part_o[prow * D + d] = o;
             if (d == 0) {
                 p.part_m[prow] = M;
@@ -376,7 +385,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(p.NP, p.Hkv, p.S);
+    dim3 grid(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
     kern<<<grid, NW * 32, SMEM, st>>>(p);
     return cudaGetLastError();
 }

@@ -14,6 +14,8 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;
 constexpr int kMaxDevices = 64;
+// Smallest partition the automatic choice uses (sizes the P = 0 workspace).
+constexpr int kAutoMinPartition = 256;
 
 // Arguments of one decode launch, already validated on the host.
 struct DecodeParams {
@@ -32,7 +34,32 @@ struct DecodeParams {
     float qk_scale;   // scale * log2(e) * k_scale
     float v_scale;    // 1 for f16/bf16 pools
     unsigned int* err;
+    // Shared-prefix (cascade) decode: a sequence in group g >= 0 starts its
+    // own attention at token group_blocks[g] * 16 (the prefix is attended by
+    // the prefix kernel); partials of this launch go to partition index
+    // part_base + p, and with cascade != 0 the output is never written
+    // directly (the merge always runs).  All null / 0 for plain decode.
+    const int32_t* seq_group = nullptr;
+    const int32_t* group_blocks = nullptr;
+    int32_t part_base = 0;
+    int32_t cascade = 0;
 };
+
+// First token of a sequence's own (non-shared) attention range, clamped
+// into [0, L] on whole blocks; out-of-range group data reports
+// PKV_DEVERR_SEQ_LEN through the caller.
+__host__ __device__ inline int own_start(const int32_t* seq_group, const int32_t* group_blocks, int s, int L,
+                                         bool* bad) {
+    if (!seq_group) return 0;
+    const int g = seq_group[s];
+    if (g < 0) return 0;
+    int start = group_blocks[g] * kBlockSize;
+    if (start < 0 || start > L) {
+        *bad = true;
+        start = start < 0 ? 0 : (L / kBlockSize) * kBlockSize;
+    }
+    return start;
+}
 
 // Device address of the error word on the current device (cached).
 unsigned int* error_word();
@@ -58,6 +85,13 @@ cudaError_t launch_decode_mma_fp8_f16q(const DecodeParams& p, int G, const CUten
 
 // Log-sum-exp merge of split-K partials into out (q dtype).
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);
+
+// Host helpers shared by the entry points (pkv_api.cu).
+int auto_partition(int S, int Hkv, int max_seq_len);
+bool encode_pool_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t rows, int D);
+// Partials of S*Hq rows x NP partitions: m, l (256-byte aligned regions), o.
+size_t partials_bytes(int64_t S, int64_t Hq, int64_t D, int64_t NP);
+void partials_layout(DecodeParams& p, void* workspace);  // sets part_m/l/o from S, Hq, NP
 
 int num_sms();
 

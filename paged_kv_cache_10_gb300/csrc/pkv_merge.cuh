@@ -32,17 +32,29 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     const int d = tid % D, grp = tid / D;
     const int64_t row = blockIdx.x;
     const int s = static_cast<int>(row / p.Hq);
+    // same clamping as the main kernels
     int L = __ldg(p.seq_lens + s);
-    const int Lmax = min(p.MB * kBlockSize, p.NP * p.P);
-    L = L < 0 ? 0 : (L > Lmax ? Lmax : L);
-    const int nparts = L > 0 ? (L + p.P - 1) / p.P : 1;
-    if (nparts <= 1) return;
-    const float* pm = p.part_m + row * p.NP;
-    const float* pl = p.part_l + row * p.NP;
-    const float* po = p.part_o + row * p.NP * D;
+    const int Lcap = p.MB * kBlockSize;
+    L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
+    bool bad = false;
+    const int start = own_start(p.seq_group, p.group_blocks, s, L, &bad);
+    const int Lown = min(L - start, (p.NP - p.part_base) * p.P);
+    const int nown = Lown > 0 ? (Lown + p.P - 1) / p.P : 0;
+    int first, nparts;  // partitions [first, first + nparts) of this row
+    if (!p.cascade) {
+        first = 0;
+        nparts = nown > 0 ? nown : 1;
+        if (nparts <= 1) return;  // written by the main kernel
+    } else {
+        first = start > 0 ? 0 : p.part_base;  // prefix partials only for group members
+        nparts = p.part_base + nown - first;
+    }
+    const float* pm = p.part_m + row * p.NP + first;
+    const float* pl = p.part_l + row * p.NP + first;
+    const float* po = p.part_o + (row * p.NP + first) * D;
 
     float M = -INFINITY;
-    for (int i = tid; i < nparts; i += kMergeThreads) M = fmaxf(M, pm[i]);
+    for (int i = tid; i < nparts; i += kMergeThreads) M = fmaxf(M, pl[i] > 0.f ? pm[i] : -INFINITY);
 #pragma unroll
     for (int mask = 16; mask > 0; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kMergeFull, M, mask));
     if (lane == 0) red[warp] = M;
@@ -52,7 +64,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     for (int w = 1; w < kMergeThreads / 32; ++w) M = fmaxf(M, red[w]);
 
     float acc = 0.f, den = 0.f;
-    if (M != -INFINITY) {
+    if (M != -INFINITY && nparts > 0) {
         for (int base = 0; base < nparts; base += kMergeThreads) {
             const int cnt = min(kMergeThreads, nparts - base);
             __syncthreads();  // previous chunk's weights fully consumed
@@ -69,13 +81,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
                 for (int u = 0; u < 16; ++u) v[u] = o[(j + u * NG) * D];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    acc = fmaf(w_s[j + u * NG], v[u], acc);
-                    den += w_s[j + u * NG];
+                    const float w = w_s[j + u * NG];
+                    acc = w > 0.f ? fmaf(w, v[u], acc) : acc;  // empty partials carry no data
+                    den += w;
                 }
             }
             for (; j < cnt; j += NG) {
-                acc = fmaf(w_s[j], o[j * D], acc);
-                den += w_s[j];
+                const float w = w_s[j];
+                acc = w > 0.f ? fmaf(w, o[j * D], acc) : acc;
+                den += w;
             }
         }
     }

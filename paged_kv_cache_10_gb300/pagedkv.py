@@ -31,7 +31,8 @@ EXPORTED = [
     "pkv_alloc_seq_new", "pkv_alloc_fork", "pkv_alloc_append_slot", "pkv_alloc_seq_extend",
     "pkv_alloc_free", "pkv_alloc_append_batch", "pkv_alloc_export", "pkv_alloc_block_table",
     "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
-    "pkv_alloc_fail_after",
+    "pkv_alloc_fail_after", "pkv_paged_attention_decode_cascade", "pkv_decode_cascade_workspace_bytes",
+    "pkv_alloc_prefix_groups",
 ]
 
 
@@ -108,6 +109,10 @@ def lib():
         "pkv_alloc_num_free": (i32, [P]),
         "pkv_alloc_num_seqs": (i32, [P]),
         "pkv_alloc_fail_after": (None, [P, i64]),
+        "pkv_paged_attention_decode_cascade": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, P, P, P, P, i32, i32,
+                                                     i32, ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
+        "pkv_decode_cascade_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32, i32]),
+        "pkv_alloc_prefix_groups": (i32, [P, P, i32, i32, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -258,6 +263,46 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, desc: CacheDesc, block_t
     _check(st, "paged_attention_decode_noalloc")
 
 
+def decode_cascade_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: int, max_seq_len: int,
+                                   partition_tokens: int, max_group_blocks: int) -> int:
+    return int(lib().pkv_decode_cascade_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len,
+                                                        partition_tokens, max_group_blocks))
+
+
+@dataclass
+class PrefixGroups:
+    """Output of Allocator.prefix_groups (host numpy arrays)."""
+    seq_group: np.ndarray      # int32 [n]
+    group_blocks: np.ndarray   # int32 [num_groups]
+    group_offsets: np.ndarray  # int32 [num_groups + 1]
+    group_members: np.ndarray  # int32 [members]
+    max_members: int
+    max_blocks: int
+
+    @property
+    def num_groups(self) -> int:
+        return int(self.group_blocks.shape[0])
+
+
+def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_tables, seq_lens, max_seq_len: int,
+                                   scale: float, out, seq_group, group_blocks, group_offsets, group_members,
+                                   max_group_members: int, max_group_blocks: int, workspace,
+                                   partition_tokens: int = 0, q_dtype: str | None = None, stream=None) -> None:
+    """Shared-prefix decode; the group arrays are int32 device tensors."""
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    ng = int(group_blocks.shape[0])
+    ptr = lambda t, n: _dev_ptr(t, n) if t.numel() > 0 else None
+    st = lib().pkv_paged_attention_decode_cascade(
+        _dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq, _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        ctypes.byref(desc.c()), _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]),
+        _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), _dev_ptr(seq_group, "seq_group"),
+        ptr(group_blocks, "group_blocks"), ptr(group_offsets, "group_offsets"), ptr(group_members, "group_members"),
+        ng, int(max_group_members), int(max_group_blocks), float(scale), _dev_ptr(out, "out"),
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(), int(partition_tokens),
+        _stream(stream))
+    _check(st, "paged_attention_decode_cascade")
+
+
 def get_device_error(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pkv_get_device_error(ctypes.byref(flags), _stream(stream)), "get_device_error")
@@ -354,6 +399,21 @@ class Allocator:
 
     def num_seqs(self) -> int:
         return int(lib().pkv_alloc_num_seqs(self._h))
+
+    def prefix_groups(self, seq_ids, min_blocks: int = 16) -> PrefixGroups:
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        sg = np.empty(max(n, 1), np.int32)
+        gb = np.empty(max(n, 1), np.int32)
+        go = np.empty(n + 1, np.int32)
+        gm = np.empty(max(n, 1), np.int32)
+        ng, mm, mb = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pkv_alloc_prefix_groups(self._h, _np_ptr(ids), n, int(min_blocks), _np_ptr(sg), _np_ptr(gb),
+                                             _np_ptr(go), _np_ptr(gm), ctypes.byref(ng), ctypes.byref(mm),
+                                             ctypes.byref(mb)), "alloc_prefix_groups")
+        k = ng.value
+        return PrefixGroups(sg[:n].copy(), gb[:k].copy(), go[:k + 1].copy(), gm[:go[k] if k else 0].copy(),
+                            mm.value, mb.value)
 
     def fail_after(self, k: int) -> None:
         lib().pkv_alloc_fail_after(self._h, int(k))

@@ -29,7 +29,8 @@ def _to_dev(a: np.ndarray, device) -> torch.Tensor:
 class DecodeStep:
     """Device state and launch sequence of one workload's decode step."""
 
-    def __init__(self, wl, device="cuda", partition_tokens=None, alloc: pk.Allocator | None = None):
+    def __init__(self, wl, device="cuda", partition_tokens=None, alloc: pk.Allocator | None = None,
+                 cascade: bool = False, cascade_min_blocks: int = 16):
         self.wl = wl
         self.device = torch.device(device)
         self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.kv_dtype,
@@ -57,7 +58,20 @@ class DecodeStep:
         self.d_tables = torch.from_numpy(self.tables).to(dev)
         self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
         self.out = torch.empty((wl.S, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
-        ws = pk.decode_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens)
+        self.cascade = cascade
+        if cascade:
+            # groups of rows sharing leading blocks (host), decoded with one
+            # pass over each shared prefix
+            self.groups = self.alloc.prefix_groups(rows, cascade_min_blocks)
+            g = self.groups
+            self.d_seq_group = torch.from_numpy(g.seq_group).to(dev)
+            self.d_group_blocks = torch.from_numpy(g.group_blocks).to(dev)
+            self.d_group_offsets = torch.from_numpy(g.group_offsets).to(dev)
+            self.d_group_members = torch.from_numpy(g.group_members).to(dev)
+            ws = pk.decode_cascade_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens,
+                                                   g.max_blocks)
+        else:
+            ws = pk.decode_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
         self.launches = 0
 
@@ -71,6 +85,9 @@ class DecodeStep:
         n = 2  # append + decode
         if len(self.pairs):
             n += 1
+        if self.cascade:
+            n += 1 + (1 if self.groups.num_groups else 0)  # merge, prefix
+            return n
         P = self.effective_partition()
         if self.max_seq_len > P:
             n += 1  # merge
@@ -87,6 +104,15 @@ class DecodeStep:
                            in_dtype=self.wl.in_dtype, stream=stream)
 
     def decode(self, stream=None, q=None, tables=None, lens=None, out=None):
+        if self.cascade:
+            g = self.groups
+            pk.paged_attention_decode_cascade(
+                self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
+                self.d_tables if tables is None else tables, self.d_lens if lens is None else lens,
+                self.max_seq_len, self.wl.scale, self.out if out is None else out, self.d_seq_group,
+                self.d_group_blocks, self.d_group_offsets, self.d_group_members, g.max_members, g.max_blocks,
+                self.workspace, partition_tokens=self.partition_tokens, q_dtype=self.wl.q_dtype, stream=stream)
+            return
         pk.paged_attention_decode(self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
                                   self.d_tables if tables is None else tables,
                                   self.d_lens if lens is None else lens, self.max_seq_len, self.wl.scale,

@@ -242,6 +242,38 @@ def custom(name, seed, lens, Hq, Hkv, D, kv_dtype="bf16", q_dtype=None, NB=None,
                  partition_tokens=partition_tokens)
 
 
+def fork_groups(name, seed, groups, singles, Hq, Hkv, D=128, kv_dtype="bf16", partition_tokens=0) -> Workload:
+    """Fork trees: for each (prefix_tokens, members) in ``groups`` a template
+    sequence of prefix_tokens (a multiple of 16) is forked into ``members``
+    sequences, each extended by its own U[0, 300] tokens; ``singles``
+    independent sequences of U[1, 600] tokens join the batch.  Every sequence
+    appends one token in the step."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(7)[6]))
+    setup, lens, s = [], [], 0
+    need = 0
+    for gi, (prefix, members) in enumerate(groups):
+        assert prefix % BLOCK_SIZE == 0
+        T = (1 << 30) + gi
+        setup.append(("new", T, prefix))
+        need += _blocks(prefix)
+        for _ in range(members):
+            suf = int(rng.integers(0, 300, endpoint=True))
+            setup += [("fork", T, s), ("extend", s, suf)]
+            lens.append(prefix + suf + 1)
+            need += _blocks(prefix + suf + 1) - _blocks(prefix) + 1
+            s += 1
+        setup.append(("free", T))
+    for _ in range(singles):
+        L = int(rng.integers(1, 600, endpoint=True))
+        setup.append(("new", s, L - 1))
+        lens.append(L)
+        need += _blocks(L) + 1
+        s += 1
+    NB = need + math.ceil(0.25 * need)
+    return build(name, seed, s, Hq, Hkv, D, NB, kv_dtype, kv_dtype, setup, list(range(s)), lens,
+                 partition_tokens=partition_tokens)
+
+
 NAMED = {
     "tiny_fp16": tiny_fp16,
     "llama7b_mha": llama7b_mha,

@@ -257,3 +257,49 @@ def test_prefix_share_workload_script_produces_copy_on_write(pk):
     assert 50 <= len(pairs) <= 64
     tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
     assert lens.tolist() == wl.seq_lens
+
+
+def _groups_model(tables, lens, min_blocks, b=16):
+    """Independent restatement of the grouping rule for cascade decode."""
+    order, buckets = [], {}
+    for i, (t, L) in enumerate(zip(tables, lens)):
+        if t is None or L // b < min_blocks:
+            continue
+        if t[0] not in buckets:
+            buckets[t[0]] = []
+            order.append(t[0])
+        buckets[t[0]].append(i)
+    out = []
+    for key in order:
+        rows = buckets[key]
+        if len(rows) < 2:
+            continue
+        full = min(lens[r] // b for r in rows)
+        lcp = 0
+        while lcp < full and len({tables[r][lcp] for r in rows}) == 1:
+            lcp += 1
+        if lcp >= min_blocks:
+            out.append((lcp, rows))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefix_groups_match_model(pk, seed):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.fork_groups("g", 50 + seed, [(64, 3), (160, 5), (32, 1)], 4, 8, 2, 128)
+    a = pk.Allocator(wl.NB, 16, wl.free_order)
+    pk.apply_setup(a, wl.setup)
+    a.append_batch(wl.step_seqs)
+    rows = list(range(wl.S)) + [-1]
+    for min_blocks in (1, 2, 4, 10):
+        g = a.prefix_groups(rows, min_blocks)
+        tables = [a.block_table(r) for r in range(wl.S)] + [None]
+        lens = [a.seq_len(r) for r in range(wl.S)] + [0]
+        want = _groups_model(tables, lens, min_blocks)
+        got = [(int(g.group_blocks[k]), g.group_members[g.group_offsets[k]:g.group_offsets[k + 1]].tolist())
+               for k in range(g.num_groups)]
+        assert got == want
+        for k, (lcp, members) in enumerate(got):
+            assert all(g.seq_group[r] == k for r in members)
+        grouped = {r for _, ms in got for r in ms}
+        assert all(g.seq_group[r] == -1 for r in range(len(rows)) if r not in grouped)
