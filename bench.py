@@ -251,6 +251,10 @@ def run_ours(args, rank, world, local_rank):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    graph = step.capture() if args.graph else None
+    if graph is not None:
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
     barrier()
     torch.cuda.synchronize()
     t_load0 = time.monotonic()
@@ -259,10 +263,13 @@ def run_ours(args, rank, world, local_rank):
             flush_buf.zero_()
         a, b, c = ev[i]
         a.record(stream)
-        step.copy()
-        step.append()
-        b.record(stream)
-        step.decode()
+        if graph is not None:
+            graph.replay()  # the whole step, one launch
+        else:
+            step.copy()
+            step.append()
+            b.record(stream)
+            step.decode()
         c.record(stream)
     torch.cuda.synchronize()
     t_load1 = time.monotonic()
@@ -272,7 +279,19 @@ def run_ours(args, rank, world, local_rank):
         total_ms = sum(step_ms)
     else:
         total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    decode_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if graph is None:
+        decode_ms = [b.elapsed_time(c) for _, b, c in ev]
+    else:
+        # kernel roofline from eager decode launches of the same workload
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            if flush:
+                flush_buf.zero_()
+            dev_ev[i][0].record(stream)
+            step.decode()
+            dev_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        decode_ms = [x.elapsed_time(y) for x, y in dev_ev]
     # extend the load window (same steps, untimed) if it was too short for clock samples
     if sampler and not args.profile and t_load1 - t_load0 < 1.0:
         t_ext = time.monotonic()
@@ -367,6 +386,7 @@ def run_ours(args, rank, world, local_rank):
                                              f"inputs larger than L2 ({working_set / 2**20:.0f} MiB vs "
                                              f"{l2 / 2**20:.0f} MiB), no flush"),
             "parallelism": f"replicas x{world}",
+            "launch": "CUDA graph replay per step" if args.graph else "eager launches",
         },
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
@@ -442,6 +462,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--partition", type=int, default=None, help="tokens per split-K partition (0 = auto)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--graph", action="store_true",
+                    help="time steps as CUDA-graph replays (one launch per step)")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
     ap.add_argument("--no-cpu-baseline", action="store_true")

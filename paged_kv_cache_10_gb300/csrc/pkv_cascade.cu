@@ -26,7 +26,7 @@ namespace pkv {
 
 constexpr int kPrefixPartitionBlocks = 16;  // 256 tokens per prefix partition
 constexpr int kCascadeWarps = 4;            // 4 x 16 rows per CTA
-constexpr int kCascadeStages = 4;
+constexpr int kCascadeStages = 8;
 
 struct CascadeParams {
     DecodeParams base;
@@ -177,8 +177,10 @@ __global__ void __launch_bounds__(NW * 32)
         if (phys >= 0 && phys < p.NB) {
             const uint32_t kts = smem_addr(smem + stage * STAGE), vts = kts + TILE;
             // ---- S = Q K^T for 16 rows x 16 tokens (n-tile j = tokens 8j..8j+7)
+            // four independent accumulator chains (2 n-tiles x even/odd k-steps)
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             {
+                float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 const int mat = lane >> 3, rr = lane & 7;
                 const int tok = rr + 8 * (mat >> 1);
 #pragma unroll
@@ -186,9 +188,14 @@ __global__ void __launch_bounds__(NW * 32)
                     const int ch = 2 * kk + (mat & 1);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(kts + (ch >> 3) * 2048 + swz128(tok, ch & 7), b0, b1, b2, b3);
-                    mma16816a<kBF>(sa[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-                    mma16816a<kBF>(sa[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+                    float(*acc)[4] = (kk & 1) ? sb : sa;
+                    mma16816a<kBF>(acc[0], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                    mma16816a<kBF>(acc[1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
                 }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) sa[j][c] += sb[j][c];
             }
             // ---- online softmax for rows ra (c0, c1) and rb (c2, c3); prefix blocks are full
             float pr[2][4];

@@ -123,3 +123,16 @@ class DecodeStep:
         self.copy(stream)
         self.append(stream)
         self.decode(stream)
+
+    def capture(self):
+        """Records one step (copy, append, decode and its merge) into a CUDA
+        graph and returns it; ``graph.replay()`` re-issues the same kernels
+        with one launch.  Run the step eagerly once first, so every
+        one-time set-up (kernel attributes, device addresses) is done."""
+        self.run()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run()
+        torch.cuda.synchronize()
+        return graph

@@ -208,3 +208,21 @@ def test_library_is_loaded_from_the_tree(lib):
     import os
     maps = open("/proc/self/maps").read()
     assert os.path.realpath(lib.LIB_PATH) in maps
+
+
+def test_graph_replay_matches_eager(lib):
+    """A captured step replays the same kernels: outputs and pools identical."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.custom("graph", 81, [1, 33, 700, 2100], 32, 8, 128, kv_dtype="bf16")
+    st = DecodeStep(wl, device="cuda")
+    g = st.capture()
+    st.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    err, _ = check_step(st)
+    assert err <= TOL["bf16"]
+    first = host_bits(st.out).copy()
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(st.out), first)
