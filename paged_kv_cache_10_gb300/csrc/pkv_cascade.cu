@@ -26,7 +26,7 @@ namespace pkv {
 
 constexpr int kPrefixPartitionBlocks = 16;  // 256 tokens per prefix partition
 constexpr int kCascadeWarps = 4;            // 4 x 16 rows per CTA
-constexpr int kCascadeStages = 8;
+constexpr int kCascadeStages = 6;
 
 struct CascadeParams {
     DecodeParams base;
@@ -41,8 +41,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// 4 CTAs per SM (<= 128 registers): a group's (prefix partition, KV head,
+// row chunk) tasks then fit one wave on the 152 SMs for typical groups
+// instead of spilling a small second wave.
 template <typename KT, typename QT, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, 4)
     cascade_prefix_kernel(const CascadeParams cp, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
     constexpr int D = 128;
