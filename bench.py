@@ -406,6 +406,43 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------ swap timing
+def run_swap(args, local_rank):
+    """Times pkv_swap_blocks on the workload's pool: all blocks of the first
+    half of the batch out to a pinned host pool and back (CUDA events)."""
+    from paged_kv_cache_10_gb300 import pagedkv as pk
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = workloads.NAMED[args.workload]()
+    st = DecodeStep(wl, device=dev)
+    rows = list(range(max(1, wl.S // 2)))
+    blocks = sorted({b for r in rows for b in st.alloc.block_table(r)})
+    n = len(blocks)
+    pairs = torch.tensor([[b, i] for i, b in enumerate(blocks)], dtype=torch.int32, device=dev)
+    shape = (n,) + tuple(st.k_cache.shape[1:])
+    k_host = torch.empty(shape, dtype=st.k_cache.dtype).pin_memory()
+    v_host = torch.empty(shape, dtype=st.v_cache.dtype).pin_memory()
+    nbytes = 2 * n * st.k_cache[0].numel() * st.k_cache.element_size()
+    res = {}
+    for name, direction in (("device_to_host", pk.SWAP_OUT), ("host_to_device", pk.SWAP_IN)):
+        for _ in range(max(args.warmup, 3)):
+            pk.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, v_host, pairs, direction)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            pk.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, v_host, pairs, direction)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        res[name] = {"us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    assert pk.get_device_error() == 0
+    return {"metric": "KV block swap bandwidth (pkv_swap_blocks, pinned mapped host pool)", "unit": "GB/s",
+            "workload": wl.name, "blocks": n, "bytes_per_swap": nbytes, "steps": args.steps, **res}
+
+
 # ----------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     if rank != 0:
@@ -462,6 +499,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--partition", type=int, default=None, help="tokens per split-K partition (0 = auto)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--swap", action="store_true",
+                    help="time block swap to / from a pinned host pool instead of the decode step")
     ap.add_argument("--graph", action="store_true",
                     help="time steps as CUDA-graph replays (one launch per step)")
     ap.add_argument("--cascade", action="store_true",
@@ -474,7 +513,9 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.swap:
+        line = run_swap(args, local_rank) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         if world > 1:

@@ -133,6 +133,27 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* d
                            const int32_t* pairs, int32_t num_pairs, void* stream);
 
 /*
+ * Block swap between the device pool and a host pool, for preemption by
+ * swapping ([P1] scheduling section: under memory pressure a sequence's KV
+ * blocks are moved to CPU memory and brought back later instead of being
+ * recomputed).
+ *
+ * k_host, v_host: host pools in the pool layout ([num_host_blocks][Hkv][16]
+ *   [D] each), pinned and mapped into the device address space (e.g.
+ *   cudaHostAlloc with cudaHostAllocMapped, or registered with
+ *   cudaHostRegisterMapped); otherwise PKV_ERR_INVALID.  The copy runs as
+ *   one kernel that reads or writes host memory directly.
+ * pairs: device int32 [num_pairs][2] = (device block, host block).
+ * direction 0 copies device -> host (swap out), 1 host -> device (swap in).
+ *   Every byte of both pools' blocks is copied.  Destination blocks must be
+ *   distinct.  An id out of range sets PKV_DEVERR_COPY_PAIR and skips the
+ *   pair.  The host data is complete once the stream reaches this point.
+ */
+pkv_status pkv_swap_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* desc, void* k_host, void* v_host,
+                           int32_t num_host_blocks, const int32_t* pairs, int32_t num_pairs, int32_t direction,
+                           void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_attention_decode needs for these sizes
  * (split-K partials: per (seq, query head, partition) a running max, a sum
  * and a normalised head_size-vector, all fp32).  partition_tokens = 0 asks
@@ -367,6 +388,18 @@ pkv_status pkv_alloc_prefix_groups(const pkv_alloc* a, const int64_t* seq_ids, i
                                    int32_t* seq_group, int32_t* group_blocks, int32_t* group_offsets,
                                    int32_t* group_members, int32_t* num_groups, int32_t* max_members,
                                    int32_t* max_blocks);
+/* Swap a sequence between a device allocator and a host-block allocator
+ * (a second pkv_alloc over the host pool's block ids, same block size).
+ * swap_out moves seq_id from `dev` to `host`; swap_in moves it back.  One new
+ * block is taken per block of the sequence, the old ones are released, and
+ * pairs ([*n][2], capacity cap) receive (device block, host block) for
+ * pkv_swap_blocks in either direction.  Every block of the sequence must
+ * be held by it alone (refcount 1), else PKV_ERR_INVALID; PKV_ERR_OOM if
+ * the target has too few free blocks.  All or nothing. */
+pkv_status pkv_alloc_swap_out(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, int32_t* pairs, int32_t cap,
+                              int32_t* n);
+pkv_status pkv_alloc_swap_in(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, int32_t* pairs, int32_t cap,
+                             int32_t* n);
 /* Fault injection for tests: the k-th block allocation from now (k >= 1)
  * fails as if the pool were empty; k <= 0 disables. */
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k);

@@ -95,6 +95,20 @@ class AllocatorModel:
         for blk in reversed(table):
             self._release(blk)
 
+    def move_to(self, other: "AllocatorModel", seq: int):
+        """Moves seq into another pool (swap out / in): one new block per
+        block, all held by this sequence alone; returns (old, new) pairs."""
+        table = self.tables[seq]
+        assert all(self.ref[b] == 1 for b in table)
+        if len(table) > len(other.free):
+            raise OutOfBlocks()
+        new = [other._take() for _ in table]
+        other.tables[seq] = new
+        other.lens[seq] = self.lens[seq]
+        pairs = list(zip(table, new))
+        self.free_seq(seq)
+        return pairs
+
     # -- views
     def block_table(self, seq: int) -> list[int]:
         return list(self.tables[seq])

@@ -371,6 +371,55 @@ pkv_status pkv_alloc_prefix_groups(const pkv_alloc* a, const int64_t* seq_ids, i
     return PKV_OK;
 }
 
+namespace {
+// Moves seq_id from allocator `from` to allocator `to`: takes one block of
+// `to` per block of the sequence, records (from_block, to_block) pairs,
+// releases the `from` blocks.  Every block must be held by this sequence
+// alone.  All or nothing.
+pkv_status move_seq(pkv_alloc* from, pkv_alloc* to, int64_t seq_id, int32_t* pairs, int32_t cap, int32_t* n,
+                    bool pairs_from_first) {
+    if (!from || !to || !n || cap < 0 || from == to) return PKV_ERR_INVALID;
+    if (from->block_size != to->block_size) return PKV_ERR_INVALID;
+    auto it = from->seqs.find(seq_id);
+    if (it == from->seqs.end()) return PKV_ERR_NOT_FOUND;
+    if (to->seqs.count(seq_id)) return PKV_ERR_INVALID;
+    const Seq& s = it->second;
+    const int32_t nb = static_cast<int32_t>(s.blocks.size());
+    if (nb > cap || (nb > 0 && !pairs)) return PKV_ERR_INVALID;
+    for (int32_t b : s.blocks)
+        if (from->ref[b] != 1) return PKV_ERR_INVALID;  // shared blocks cannot move
+    if (nb > static_cast<int32_t>(to->free_stack.size())) return PKV_ERR_OOM;
+    Seq moved;
+    moved.len = s.len;
+    for (int32_t i = 0; i < nb; ++i) {
+        if (!to->can_take()) {
+            for (auto r = moved.blocks.rbegin(); r != moved.blocks.rend(); ++r) to->untake(*r);
+            return PKV_ERR_OOM;
+        }
+        moved.blocks.push_back(to->take());
+    }
+    for (int32_t i = 0; i < nb; ++i) {
+        pairs[2 * i] = pairs_from_first ? s.blocks[i] : moved.blocks[i];
+        pairs[2 * i + 1] = pairs_from_first ? moved.blocks[i] : s.blocks[i];
+    }
+    for (auto r = s.blocks.rbegin(); r != s.blocks.rend(); ++r) from->release(*r);
+    from->seqs.erase(it);
+    to->seqs.emplace(seq_id, std::move(moved));
+    *n = nb;
+    return PKV_OK;
+}
+}  // namespace
+
+pkv_status pkv_alloc_swap_out(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, int32_t* pairs, int32_t cap,
+                              int32_t* n) {
+    return move_seq(dev, host, seq_id, pairs, cap, n, true);
+}
+
+pkv_status pkv_alloc_swap_in(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, int32_t* pairs, int32_t cap,
+                             int32_t* n) {
+    return move_seq(host, dev, seq_id, pairs, cap, n, false);
+}
+
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k) {
     if (a) a->fail_countdown = k > 0 ? k : 0;
 }

@@ -118,6 +118,30 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(unsigned char* kc, uns
     for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) d4[i] = s4[i];
 }
 
+// Swap: grid (num_pairs, kCopySplit, 2 pools); moves 1/kCopySplit of one
+// block of one pool between the device pool and the host pool (pinned,
+// device-mapped memory, same [blocks][Hkv][16][D] layout) with 16-byte
+// vectors.  direction 0: device -> host, 1: host -> device.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(unsigned char* kc, unsigned char* vc, unsigned char* kh,
+                                                          unsigned char* vh, const int32_t* __restrict__ pairs,
+                                                          int NB, int NH, int64_t block_bytes, int direction,
+                                                          unsigned int* err) {
+    const int pr = blockIdx.x;
+    const int32_t dblk = __ldg(pairs + 2 * pr), hblk = __ldg(pairs + 2 * pr + 1);
+    if (dblk < 0 || dblk >= NB || hblk < 0 || hblk >= NH) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) report(err, PKV_DEVERR_COPY_PAIR);
+        return;
+    }
+    unsigned char* dev = (blockIdx.z == 0 ? kc : vc) + dblk * block_bytes;
+    unsigned char* host = (blockIdx.z == 0 ? kh : vh) + hblk * block_bytes;
+    const uint4* src = reinterpret_cast<const uint4*>(direction == 0 ? dev : host);
+    uint4* dst = reinterpret_cast<uint4*>(direction == 0 ? host : dev);
+    const int64_t vecs = block_bytes / 16;
+    const int64_t per = (vecs + kCopySplit - 1) / kCopySplit;
+    const int64_t lo = blockIdx.y * per, hi = min(vecs, lo + per);
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) dst[i] = src[i];
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool desc_ok(const pkv_cache_desc* d) {
@@ -202,5 +226,37 @@ extern "C" pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const pkv_ca
     copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache), pairs, desc->num_blocks,
         block_bytes, err);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" pkv_status pkv_swap_blocks(void* k_cache, void* v_cache, const pkv_cache_desc* desc, void* k_host,
+                                      void* v_host, int32_t num_host_blocks, const int32_t* pairs,
+                                      int32_t num_pairs, int32_t direction, void* stream) {
+    if (!desc_ok(desc) || num_pairs < 0 || num_host_blocks < 0 || (direction != 0 && direction != 1))
+        return PKV_ERR_INVALID;
+    if (!desc_supported(desc)) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k_host || !v_host || !pairs || num_host_blocks == 0) return PKV_ERR_INVALID;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_host) || !aligned16(v_host) ||
+        (reinterpret_cast<uintptr_t>(pairs) & 3u))
+        return PKV_ERR_INVALID;
+    // The host pools must be pinned and mapped into the device address space.
+    void* kd = nullptr;
+    void* vd = nullptr;
+    if (cudaHostGetDevicePointer(&kd, k_host, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&vd, v_host, 0) != cudaSuccess || !kd || !vd) {
+        cudaGetLastError();  // clear the sticky-free error of the failed query
+        return PKV_ERR_INVALID;
+    }
+    if (!aligned16(kd) || !aligned16(vd)) return PKV_ERR_INVALID;
+    unsigned int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    const int64_t block_bytes = static_cast<int64_t>(desc->num_kv_heads) * kBlockSize * desc->head_size *
+                                (desc->kv_dtype == PKV_FP8_E4M3 ? 1 : 2);
+    dim3 grid(num_pairs, kCopySplit, 2);
+    swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<unsigned char*>(k_cache), static_cast<unsigned char*>(v_cache),
+        static_cast<unsigned char*>(kd), static_cast<unsigned char*>(vd), pairs, desc->num_blocks, num_host_blocks,
+        block_bytes, direction, err);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

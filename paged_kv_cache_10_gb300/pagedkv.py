@@ -32,7 +32,7 @@ EXPORTED = [
     "pkv_alloc_free", "pkv_alloc_append_batch", "pkv_alloc_export", "pkv_alloc_block_table",
     "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
     "pkv_alloc_fail_after", "pkv_paged_attention_decode_cascade", "pkv_decode_cascade_workspace_bytes",
-    "pkv_alloc_prefix_groups",
+    "pkv_alloc_prefix_groups", "pkv_swap_blocks", "pkv_alloc_swap_out", "pkv_alloc_swap_in",
 ]
 
 
@@ -113,6 +113,9 @@ def lib():
                                                      i32, ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
         "pkv_decode_cascade_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32, i32]),
         "pkv_alloc_prefix_groups": (i32, [P, P, i32, i32, P, P, P, P, P, P, P]),
+        "pkv_swap_blocks": (i32, [P, P, D, P, P, i32, P, i32, i32, P]),
+        "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
+        "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -303,6 +306,22 @@ def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_t
     _check(st, "paged_attention_decode_cascade")
 
 
+SWAP_OUT, SWAP_IN = 0, 1
+
+
+def swap_blocks(k_cache, v_cache, desc: CacheDesc, k_host, v_host, pairs, direction: int, stream=None) -> None:
+    """k_host, v_host: pinned CPU tensors [NH, Hkv, 16, D] (torch pin_memory
+    memory is mapped); pairs: int32 device [n, 2] of (device block, host block)."""
+    for t, n in ((k_host, "k_host"), (v_host, "v_host")):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous pinned CPU tensor")
+    n = int(pairs.shape[0])
+    st = lib().pkv_swap_blocks(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
+                               k_host.data_ptr(), v_host.data_ptr(), int(k_host.shape[0]),
+                               _dev_ptr(pairs, "pairs") if n else None, n, int(direction), _stream(stream))
+    _check(st, "swap_blocks")
+
+
 def get_device_error(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pkv_get_device_error(ctypes.byref(flags), _stream(stream)), "get_device_error")
@@ -414,6 +433,22 @@ class Allocator:
         k = ng.value
         return PrefixGroups(sg[:n].copy(), gb[:k].copy(), go[:k + 1].copy(), gm[:go[k] if k else 0].copy(),
                             mm.value, mb.value)
+
+    def swap_out(self, host: "Allocator", seq: int) -> np.ndarray:
+        """Moves seq to the host allocator; returns (device, host) block pairs."""
+        pairs = np.empty((max(self.num_blocks, 1), 2), np.int32)
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_swap_out(self._h, host._h, seq, _np_ptr(pairs), pairs.shape[0], ctypes.byref(n)),
+               "alloc_swap_out")
+        return pairs[: n.value].copy()
+
+    def swap_in(self, host: "Allocator", seq: int) -> np.ndarray:
+        """Moves seq back from the host allocator; returns (device, host) pairs."""
+        pairs = np.empty((max(host.num_blocks, 1), 2), np.int32)
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_swap_in(self._h, host._h, seq, _np_ptr(pairs), pairs.shape[0], ctypes.byref(n)),
+               "alloc_swap_in")
+        return pairs[: n.value].copy()
 
     def fail_after(self, k: int) -> None:
         lib().pkv_alloc_fail_after(self._h, int(k))

@@ -303,3 +303,40 @@ def test_prefix_groups_match_model(pk, seed):
             assert all(g.seq_group[r] == k for r in members)
         grouped = {r for _, ms in got for r in ms}
         assert all(g.seq_group[r] == -1 for r in range(len(rows)) if r not in grouped)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_swap_out_and_in_match_model(pk, seed):
+    rng = np.random.default_rng(100 + seed)
+    dev, host = pk.Allocator(40, 16, rng.permutation(40)), pk.Allocator(24, 16, rng.permutation(24))
+    mdev, mhost = AllocatorModel(40, 16, dev._order), AllocatorModel(24, 16, host._order)
+    for s in range(6):
+        n = int(rng.integers(1, 90))
+        dev.seq_new(s, n)
+        mdev.seq_new(s, n)
+    dev.fork(0, 9)
+    mdev.fork(0, 9)
+    with pytest.raises(pk.PagedKVError):
+        dev.swap_out(host, 0)  # shared blocks cannot move
+    for s in (1, 3, 4):
+        got = dev.swap_out(host, s)
+        assert [tuple(x) for x in got.tolist()] == mdev.move_to(mhost, s)
+    assert dev.num_free() == mdev.num_free() and host.num_free() == mhost.num_free()
+    slot, _ = dev.append_slot(2)  # the device pool keeps working meanwhile
+    assert slot == mdev.append_slot(2)[0]
+    for s in (3, 1):
+        got = dev.swap_in(host, s)  # pairs are (device block, host block)
+        want = [(new, old) for old, new in mhost.move_to(mdev, s)]
+        assert [tuple(x) for x in got.tolist()] == want
+        assert dev.block_table(s) == mdev.block_table(s) and dev.seq_len(s) == mdev.lens[s]
+    assert [dev.refcount(b) for b in range(40)] == mdev.ref
+    assert [host.refcount(b) for b in range(24)] == mhost.ref
+
+
+def test_swap_out_is_all_or_nothing(pk):
+    dev, host = pk.Allocator(20, 16), pk.Allocator(2, 16)
+    dev.seq_new(1, 70)  # 5 blocks, host has 2
+    before = (dev.block_table(1), dev.num_free(), host.num_free())
+    with pytest.raises(pk.OutOfBlocks):
+        dev.swap_out(host, 1)
+    assert (dev.block_table(1), dev.num_free(), host.num_free()) == before

@@ -226,3 +226,79 @@ def test_graph_replay_matches_eager(lib):
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(host_bits(st.out), first)
+
+
+def test_swap_round_trip_preserves_sequences(lib):
+    """Swap two sequences out to a pinned host pool, let other data overwrite
+    their old device blocks, swap them back into new blocks: the host copy is
+    bit-exact and decode of the swapped-in sequences matches the oracle on the
+    original data."""
+    import oracle
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.custom("swap", 91, [40, 300, 17, 700], 16, 2, 128, kv_dtype="bf16")
+    st = DecodeStep(wl, device="cuda")
+    st.run()
+    torch.cuda.synchronize()
+    NH = 64
+    k_host = torch.zeros((NH, wl.Hkv, 16, wl.D), dtype=torch.uint16).pin_memory()
+    v_host = torch.zeros_like(k_host).pin_memory()
+    host = lib.Allocator(NH, 16)
+    orig_k, orig_v = host_bits(st.k_cache).copy(), host_bits(st.v_cache).copy()
+    moved = {}
+    for s in (1, 3):
+        old_table = st.alloc.block_table(s)
+        pairs = st.alloc.swap_out(host, s)
+        assert [p[0] for p in pairs.tolist()] == old_table
+        lib.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, v_host,
+                        torch.from_numpy(pairs).cuda(), lib.SWAP_OUT)
+        moved[s] = pairs
+    torch.cuda.synchronize()
+    kh = k_host.view(torch.int16).numpy().view(np.uint16)
+    vh = v_host.view(torch.int16).numpy().view(np.uint16)
+    for s, pairs in moved.items():
+        for d, h in pairs.tolist():
+            assert np.array_equal(kh[h], orig_k[d]) and np.array_equal(vh[h], orig_v[d])
+    # freed device blocks get overwritten by other work
+    st.k_cache.view(torch.int16).random_(0, 30000)
+    st.v_cache.view(torch.int16).random_(0, 30000)
+    keep_k, keep_v = host_bits(st.k_cache).copy(), host_bits(st.v_cache).copy()
+    for s in (3, 1):
+        pairs = st.alloc.swap_in(host, s)
+        lib.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, v_host,
+                        torch.from_numpy(pairs).cuda(), lib.SWAP_IN)
+        for d, h in pairs.tolist():
+            keep_k[d], keep_v[d] = kh[h], vh[h]
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    assert np.array_equal(host_bits(st.k_cache), keep_k) and np.array_equal(host_bits(st.v_cache), keep_v)
+    # decode the swapped-in sequences from their new blocks
+    rows = np.array([1, 3])
+    tables, lens = st.alloc.export(rows, st.max_blocks)
+    q = st.q.view(torch.int16)[torch.from_numpy(rows).cuda()].contiguous().view(torch.uint16)
+    out = torch.empty_like(q)
+    ws = torch.empty(max(lib.decode_workspace_bytes(2, wl.Hq, wl.D, int(lens.max()), 0), 16), dtype=torch.uint8,
+                     device="cuda")
+    lib.paged_attention_decode(q, st.k_cache, st.v_cache, st.desc, torch.from_numpy(tables).cuda(),
+                               torch.from_numpy(lens).cuda(), int(lens.max()), wl.scale, out, workspace=ws,
+                               q_dtype="bf16")
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), "bf16", keep_k, keep_v, "bf16", tables, lens,
+                              wl.scale)
+    got = oracle.dequantize(host_bits(out), "bf16")
+    assert np.max(np.abs(got - ref)) <= TOL["bf16"]
+    # and it is the attention of the original data (old tables, original pools)
+    ref0 = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), "bf16", orig_k, orig_v, "bf16",
+                               st.tables[rows], st.seq_lens[rows], wl.scale)
+    assert np.max(np.abs(got - ref0)) <= TOL["bf16"]
+
+
+def test_swap_rejects_unpinned_host_memory(lib):
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.custom("swap2", 92, [40], 4, 2, 128, kv_dtype="bf16")
+    st = DecodeStep(wl, device="cuda")
+    k_host = torch.zeros((4, 2, 16, 128), dtype=torch.uint16)
+    with pytest.raises(ValueError):
+        lib.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, k_host,
+                        torch.zeros((1, 2), dtype=torch.int32, device="cuda"), lib.SWAP_OUT)
