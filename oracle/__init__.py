@@ -69,6 +69,9 @@ def bind(lib):
         lib.pkvo_paged_decode_partials.argtypes = [P, i32, i32, i32, P, P, i32, i32, i32, i32, i32,
                                                    f64, f64, P, i32, P, f64, i32, i32, P, P, P]
         lib.pkvo_paged_decode_partials.restype = i32
+        lib.pkvo_paged_prefill.argtypes = [P, i32, i32, i32, i32, P, P, P, i32, i32, i32, i32, i32, f64, f64,
+                                           P, i32, P, f64, P]
+        lib.pkvo_paged_prefill.restype = i32
         lib.pkvo_lse_merge.argtypes = [i64, i32, i32, P, P, P, P]
         lib.pkvo_lse_merge.restype = None
         lib.pkvo_append.argtypes = [P, P, i32, i32, P, P, P, i32, i32, i32, i32, i32, f32, f32]
@@ -136,6 +139,31 @@ def paged_decode(q, q_dtype, k_pool, v_pool, kv_dtype, block_tables, seq_lens, s
     rc = _load().pkvo_paged_decode(_ptr(q), DTYPE_CODE[q_dtype], S, Hq, _ptr(k_pool), _ptr(v_pool),
                                    DTYPE_CODE[kv_dtype], NB, b, Hkv, D, float(k_scale), float(v_scale),
                                    _ptr(bt), bt.shape[1], _ptr(sl), float(scale), _ptr(out))
+    if rc:
+        raise ValueError("oracle: invalid argument or block id")
+    return out
+
+
+def paged_prefill(q, q_dtype, query_start, k_pool, v_pool, kv_dtype, block_tables, seq_lens, scale,
+                  k_scale=1.0, v_scale=1.0) -> np.ndarray:
+    """float64 out[T, Hq, D] of causal paged prefill (see pkv_oracle.c).
+
+    q: raw bits [T, Hq, D]; query_start: int32 [S + 1] (rows of each sequence's
+    new tokens); seq_lens: int32 [S], each counting the new tokens.
+    """
+    T, Hq, D = q.shape
+    NB, Hkv, b, D2 = k_pool.shape
+    assert D == D2 and v_pool.shape == k_pool.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    S = sl.shape[0]
+    assert qs.shape == (S + 1,)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = _load().pkvo_paged_prefill(_ptr(np.ascontiguousarray(q)), DTYPE_CODE[q_dtype], T, Hq, S, _ptr(qs),
+                                    _ptr(k_pool), _ptr(v_pool), DTYPE_CODE[kv_dtype], NB, b, Hkv, D,
+                                    float(k_scale), float(v_scale), _ptr(bt), bt.shape[1] if bt.ndim == 2 else 0,
+                                    _ptr(sl), float(scale), _ptr(out))
     if rc:
         raise ValueError("oracle: invalid argument or block id")
     return out

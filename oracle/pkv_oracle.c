@@ -1,6 +1,7 @@
 /*
  * pkv_oracle.c -- plain float64 CPU oracle for paged decode attention,
- * the slot-mapped KV append and the copy-on-write block copy.
+ * paged (chunked) prefill attention, the slot-mapped KV append and the
+ * copy-on-write block copy.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only tests/, __graft_entry__.smoke() and the cpu_baseline
@@ -222,6 +223,85 @@ int pkvo_paged_decode(const void* q, int q_dtype, int S, int Hq,
         weighted_v(&a, s, i, 0, L, sc, o);
         for (int d = 0; d < D; ++d) o[d] /= sum;
         free(sc);
+    }
+    return status;
+}
+
+/* Paged prefill attention (causal, multi-query).  Prefill processes a
+ * prompt's tokens and writes their KV into the blocks; chunked prefill splits
+ * a long prompt into chunks of at most a token budget that run in successive
+ * iterations ([P1] "PagedAttention 内存管理与核心数据结构": prefill then decode;
+ * [P1] scheduling section on chunked prefill).  Each query token therefore
+ * attends to every earlier token of its sequence -- the context already in
+ * the pool from earlier chunks -- and to the tokens of its own chunk up to
+ * and including itself.
+ *
+ * Sequence s owns the query rows [query_start[s], query_start[s+1]) of q
+ * ([T][Hq][D]); n_s = query_start[s+1] - query_start[s] new tokens whose KV
+ * is already in the pool, at the last n_s of its seq_lens[s] positions.  Row
+ * j is at position p = seq_lens[s] - n_s + j and
+ *     out[query_start[s] + j][i] = sum_{t <= p} softmax_t(scale * q.k_t) * v_t
+ * with keys and values gathered through block_tables[s] as in decode.  Rows
+ * outside every sequence's range are left at zero.  Returns 1 on an invalid
+ * argument (n_s > seq_lens[s], a decreasing or out-of-range query_start, a
+ * block id outside the pool). */
+int pkvo_paged_prefill(const void* q, int q_dtype, int T, int Hq, int S, const int32_t* query_start,
+                       const void* k_pool, const void* v_pool, int kv_dtype,
+                       int NB, int b, int Hkv, int D, double k_scale, double v_scale,
+                       const int32_t* block_tables, int MB, const int32_t* seq_lens,
+                       double scale, double* out) {
+    pkvo_args a = {q, q_dtype, S, Hq, k_pool, v_pool, kv_dtype, NB, b, Hkv, D,
+                   k_scale, v_scale, block_tables, MB, seq_lens, scale};
+    if (check_args(&a) || T < 0) return PKVO_EINVAL;
+    if (S > 0 && query_start[0] < 0) return PKVO_EINVAL;
+    for (int s = 0; s < S; ++s) {
+        int n = query_start[s + 1] - query_start[s];
+        if (n < 0 || query_start[s + 1] > T || n > seq_lens[s]) return PKVO_EINVAL;
+    }
+    memset(out, 0, sizeof(double) * (size_t)T * Hq * D);
+    int G = Hq / Hkv;
+    int status = PKVO_OK;
+    int64_t rows = (int64_t)T * Hq;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < rows; ++r) {
+        int tok = (int)(r / Hq), i = (int)(r % Hq), h = i / G;
+        int s = -1;
+        for (int c = 0; c < S; ++c)
+            if (tok >= query_start[c] && tok < query_start[c + 1]) { s = c; break; }
+        if (s < 0) continue;
+        int n = query_start[s + 1] - query_start[s];
+        int p = seq_lens[s] - n + (tok - query_start[s]);   /* this token's position */
+        int nk = p + 1;                                      /* keys 0..p */
+        double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)nk);
+        for (int d = 0; d < D; ++d) qrow[d] = elem_to_double(q, q_dtype, r * D + d);
+        int bad = 0;
+        for (int t = 0; t < nk && !bad; ++t) {
+            int32_t blk = block_tables[(int64_t)s * MB + t / b];
+            if (blk < 0 || blk >= NB) { bad = 1; break; }
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += qrow[d] * elem_to_double(k_pool, kv_dtype, pool_index(blk, h, t % b, d, Hkv, b, D)) * k_scale;
+            sc[t] = scale * dot;
+        }
+        if (bad) {
+#pragma omp atomic write
+            status = PKVO_EINVAL;
+            free(qrow); free(sc);
+            continue;
+        }
+        double m = -INFINITY;
+        for (int t = 0; t < nk; ++t) m = sc[t] > m ? sc[t] : m;
+        double sum = 0.0;
+        for (int t = 0; t < nk; ++t) { sc[t] = exp(sc[t] - m); sum += sc[t]; }
+        double* o = out + r * D;
+        for (int t = 0; t < nk; ++t) {
+            int32_t blk = block_tables[(int64_t)s * MB + t / b];
+            for (int d = 0; d < D; ++d)
+                o[d] += sc[t] * elem_to_double(v_pool, kv_dtype, pool_index(blk, h, t % b, d, Hkv, b, D)) * v_scale;
+        }
+        for (int d = 0; d < D; ++d) o[d] /= sum;
+        free(qrow); free(sc);
     }
     return status;
 }

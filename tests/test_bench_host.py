@@ -58,6 +58,8 @@ def test_step_bytes_counts_the_gathered_kv():
         seq_lens = np.array([17, 40], np.int32)
         slots = np.array([5, -1], np.int64)
         pairs = np.zeros((1, 2), np.int32)
+        # row 1 shares its first block (full in both) with row 0
+        tables = np.array([[7, 3, -1], [7, 9, 4]], np.int32)
 
     nb = bench.step_bytes(Step())
     assert nb["kv"] == (17 + 40) * 2 * 2 * 128 * 2
@@ -65,3 +67,6 @@ def test_step_bytes_counts_the_gathered_kv():
     assert nb["append"] == 1 * 2 * 2 * 128 * (2 + 2) + 2 * 8
     assert nb["copy"] == 1 * (2 * 2 * (2 * 16 * 128 * 2) + 8)
     assert nb["total"] == nb["decode"] + nb["append"] + nb["copy"]
+    # distinct tokens: block 7 (16), block 3 (1), block 9 (16), block 4 (8)
+    assert nb["unique_kv"] == (16 + 1 + 16 + 8) * 2 * 2 * 128 * 2
+    assert nb["decode_unique"] == nb["decode"] - nb["kv"] + nb["unique_kv"]

@@ -22,8 +22,8 @@ MUTANTS = [
     ("GQA heads interleaved instead of grouped", "    int G = a->Hq / a->Hkv;\n    int h = i / G;\n    double* qrow",
      "    int G = a->Hq / a->Hkv;\n    int h = i % a->Hkv; (void)G;\n    double* qrow"),
     ("score scale dropped", "sc[t - t0] = a->scale * dot;", "sc[t - t0] = dot;"),
-    ("normalised by length, not by the sum", "for (int d = 0; d < D; ++d) o[d] /= sum;\n        free(sc);\n    }\n    return status;\n}\n\n/* Split-K",
-     "for (int d = 0; d < D; ++d) o[d] /= L;\n        free(sc);\n    }\n    return status;\n}\n\n/* Split-K"),
+    ("normalised by length, not by the sum", "for (int d = 0; d < D; ++d) o[d] /= sum;\n        free(sc);\n    }\n    return status;\n}\n\n/* Paged prefill",
+     "for (int d = 0; d < D; ++d) o[d] /= L;\n        free(sc);\n    }\n    return status;\n}\n\n/* Paged prefill"),
     ("pool rows and columns transposed", "return ((blk * Hkv + h) * (int64_t)b + off) * D + d;",
      "return ((blk * Hkv + h) * (int64_t)D + d) * b + off;"),
     ("value gathered from the key pool", "acc[d] += w[t - t0] * elem_to_double(a->v_pool,", "acc[d] += w[t - t0] * elem_to_double(a->k_pool,"),
@@ -38,6 +38,14 @@ MUTANTS = [
     ("partition max not rebased", "m_out[r] = m;\n        l_out[r] = sum;", "m_out[r] = 0.0;\n        l_out[r] = sum;"),
     ("append slot offset off by one", "int off = (int)(slot % b);", "int off = (int)((slot + 1) % b);"),
     ("append encodes with multiply-by-scale", "float kq = kx / k_scale;", "float kq = kx * k_scale;"),
+    ("prefill mask drops the diagonal", "int nk = p + 1;                                      /* keys 0..p */",
+     "int nk = p;"),
+    ("prefill positions ignore the earlier context", "int p = seq_lens[s] - n + (tok - query_start[s]);",
+     "int p = tok - query_start[s];"),
+    ("prefill query row taken per sequence", "for (int d = 0; d < D; ++d) qrow[d] = elem_to_double(q, q_dtype, r * D + d);",
+     "for (int d = 0; d < D; ++d) qrow[d] = elem_to_double(q, q_dtype, ((int64_t)s * Hq + i) * D + d);"),
+    ("prefill GQA heads interleaved", "int tok = (int)(r / Hq), i = (int)(r % Hq), h = i / G;",
+     "int tok = (int)(r / Hq), i = (int)(r % Hq), h = i % Hkv; (void)G;"),
     ("copy skips the value pool", "memmove((char*)v_pool + dst * block_bytes, (char*)v_pool + src * block_bytes, (size_t)block_bytes);",
      "(void)0;"),
 ]
@@ -60,11 +68,17 @@ def _pin_calls():
         (pins.test_gqa_equal_queries_give_equal_rows_and_zero_length_gives_zeros, {}),
         (pins.test_oracle_rejects_out_of_pool_block_ids, {}),
         (pins.test_copy_blocks_copies_pairs_and_nothing_else, {}),
+        (pins.test_prefill_of_single_tokens_equals_decode, {}),
+        (pins.test_prefill_first_prompt_token_returns_its_value, {}),
+        (pins.test_prefill_in_two_chunks_equals_one_pass, {}),
+        (pins.test_prefill_matches_50_digit_brute_force, {}),
+        (pins.test_prefill_invariant_under_block_relabelling, {}),
     ]
     for dt in ("f16", "bf16", "e4m3"):
         for G in (1, 4):
             calls.append((pins.test_decode_matches_contiguous_library_attention, {"dtype": dt, "G": G}))
         calls.append((pins.test_append_lands_at_the_mapped_slot_only, {"dtype": dt}))
+        calls.append((pins.test_prefill_matches_contiguous_causal_library_attention, {"dtype": dt, "G": 4}))
     for P in (16, 32, 48, 512):
         calls.append((pins.test_partitioned_merge_equals_unsplit, {"P": P}))
     return calls

@@ -15,6 +15,10 @@ fails at least one of them:
     mean of V; a dominant key returns its value; equal queries in a GQA group
     give equal rows; length 0 gives zeros);
   * split-K partials + log-sum-exp merge equal the unsplit result;
+  * causal paged prefill against torch softmax(Q K^T * scale + causal mask) V
+    on the gathered keys, 50-digit brute force, decode for one-token chunks,
+    one pass against two chunks, block relabelling, and the first prompt
+    token returning its own value;
   * append / copy_blocks checked by reading back through the block table.
 """
 import decimal
@@ -249,6 +253,133 @@ def test_oracle_rejects_out_of_pool_block_ids():
     case["block_tables"][0, 1] = 4
     with pytest.raises(ValueError):
         oracle.paged_decode(**case)
+
+
+# ------------------------------------------------------------------ prefill
+def make_prefill_case(Hq, Hkv, D, lens, qlens, dtype="bf16", seed=0, NB=None):
+    """A decode-style case plus packed query rows: sequence s owns the last
+    qlens[s] of its lens[s] positions, rows query_start[s]..query_start[s+1]."""
+    case = make_case(len(lens), Hq, Hkv, D, lens, dtype=dtype, seed=seed, NB=NB)
+    rng = np.random.default_rng(seed + 100)
+    T = int(sum(qlens))
+    qd = case["q_dtype"]
+    case["q"] = bits16(rng.standard_normal((T, Hq, D)).astype(np.float32), qd)
+    case["query_start"] = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    return case
+
+
+def causal_reference(case, G, ks=1.0, vs=1.0):
+    """torch float64 softmax(Q K^T * scale + causal mask) V per sequence, on the
+    gathered contiguous keys and values."""
+    qf = oracle.dequantize(case["q"], case["q_dtype"])
+    T, Hq, D = qf.shape
+    out = np.zeros((T, Hq, D))
+    qs = case["query_start"]
+    for s in range(len(case["seq_lens"])):
+        L = int(case["seq_lens"][s])
+        n = int(qs[s + 1] - qs[s])
+        if n == 0:
+            continue
+        ctx = L - n
+        pos = torch.arange(ctx, L, dtype=torch.int64)[:, None]
+        key = torch.arange(L, dtype=torch.int64)[None, :]
+        mask = key > pos
+        for h in range(Hq // G):
+            K, V = gathered(case, s, h)
+            Kf = torch.from_numpy(oracle.dequantize(K, case["kv_dtype"]) * ks)
+            Vf = torch.from_numpy(oracle.dequantize(V, case["kv_dtype"]) * vs)
+            for g in range(G):
+                i = h * G + g
+                Q = torch.from_numpy(qf[qs[s]:qs[s + 1], i])
+                sc = (Q @ Kf.T) * case["scale"]
+                sc = sc.masked_fill(mask, float("-inf"))
+                out[qs[s]:qs[s + 1], i] = (torch.softmax(sc, dim=1) @ Vf).numpy()
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("G", [1, 4])
+def test_prefill_matches_contiguous_causal_library_attention(dtype, G):
+    Hkv = 2
+    case = make_prefill_case(Hkv * G, Hkv, 32, [5, 40, 33, 70], [5, 17, 1, 33], dtype=dtype, seed=11)
+    ks, vs = (0.05, 0.07) if dtype == "e4m3" else (1.0, 1.0)
+    out = oracle.paged_prefill(**case, k_scale=ks, v_scale=vs)
+    ref = causal_reference(case, G, ks, vs)
+    assert np.max(np.abs(out - ref)) <= 1e-12
+
+
+def test_prefill_of_single_tokens_equals_decode():
+    case = make_prefill_case(8, 2, 32, [1, 17, 50, 64], [1, 1, 1, 1], dtype="bf16", seed=12)
+    pre = oracle.paged_prefill(**case)
+    dec_case = {k: v for k, v in case.items() if k != "query_start"}
+    dec = oracle.paged_decode(**dec_case)
+    assert np.max(np.abs(pre - dec)) <= 1e-14
+
+
+def test_prefill_first_prompt_token_returns_its_value():
+    case = make_prefill_case(4, 2, 16, [9, 30], [9, 30], dtype="bf16", seed=13)
+    out = oracle.paged_prefill(**case)
+    for s in range(2):
+        row = case["query_start"][s]
+        for i in range(4):
+            _, V = gathered(case, s, i // 2)
+            assert np.array_equal(out[row, i], oracle.dequantize(V[0], "bf16"))
+
+
+def test_prefill_in_two_chunks_equals_one_pass():
+    whole = make_prefill_case(4, 1, 16, [50], [50], dtype="bf16", seed=14)
+    out = oracle.paged_prefill(**whole)
+    first = dict(whole, q=whole["q"][:20], query_start=np.array([0, 20], np.int32),
+                 seq_lens=np.array([20], np.int32))
+    second = dict(whole, q=whole["q"][20:], query_start=np.array([0, 30], np.int32))
+    a = oracle.paged_prefill(**first)
+    b = oracle.paged_prefill(**second)
+    assert np.max(np.abs(np.concatenate([a, b]) - out)) <= 1e-15
+
+
+def test_prefill_matches_50_digit_brute_force():
+    case = make_prefill_case(2, 1, 8, [13, 20], [4, 6], dtype="bf16", seed=15)
+    out = oracle.paged_prefill(**case)
+    decimal.getcontext().prec = 50
+    D = decimal.Decimal
+    qf = oracle.dequantize(case["q"], "bf16")
+    qs = case["query_start"]
+    for s in range(2):
+        K, V = gathered(case, s, 0)
+        Kf, Vf = oracle.dequantize(K, "bf16"), oracle.dequantize(V, "bf16")
+        L = len(Kf)
+        n = qs[s + 1] - qs[s]
+        for j in range(n):
+            p = L - n + j
+            for i in range(2):
+                row = qf[qs[s] + j, i]
+                sc = [sum(D(float(row[d])) * D(float(Kf[t, d])) for d in range(8)) * D(case["scale"])
+                      for t in range(p + 1)]
+                m = max(sc)
+                w = [(x - m).exp() for x in sc]
+                tot = sum(w)
+                for d in range(8):
+                    ref = sum(w[t] * D(float(Vf[t, d])) for t in range(len(w))) / tot
+                    assert abs(out[qs[s] + j, i, d] - float(ref)) <= 1e-13
+
+
+def test_prefill_invariant_under_block_relabelling():
+    case = make_prefill_case(8, 2, 64, [1, 17, 50, 64], [1, 10, 50, 3], NB=40, dtype="f16", seed=16)
+    out = oracle.paged_prefill(**case)
+    perm = np.random.default_rng(19).permutation(40)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(40)
+    bt = case["block_tables"]
+    case2 = dict(case, k_pool=case["k_pool"][inv], v_pool=case["v_pool"][inv],
+                 block_tables=np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32))
+    assert np.array_equal(out, oracle.paged_prefill(**case2))
+
+
+def test_prefill_rejects_more_new_tokens_than_the_sequence_holds():
+    case = make_prefill_case(2, 1, 16, [10], [10], dtype="bf16", seed=17)
+    case["seq_lens"] = np.array([9], np.int32)
+    with pytest.raises(ValueError):
+        oracle.paged_prefill(**case)
 
 
 # ------------------------------------------------------------ append / copy
