@@ -277,6 +277,39 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                           int32_t max_group_blocks);
 
 /*
+ * Paged (chunked) prefill attention, causal, on the tensor cores.  Prefill
+ * processes a prompt's tokens together; chunked prefill cuts a long prompt
+ * into chunks that run in successive iterations, each attending to the KV
+ * of the earlier chunks already in the pool ([P1] "PagedAttention 内存管理与
+ * 核心数据结构" and the scheduling section on chunked prefill).
+ *
+ * q, out: [num_tokens][num_q_heads][head_size] (q_dtype); the new tokens of
+ *   all sequences packed back to back.
+ * query_start: device int32 [num_seqs + 1]: sequence s owns rows
+ *   [query_start[s], query_start[s+1]) of q and out, n_s rows in all.
+ * seq_lens: device int32 [num_seqs]: tokens of sequence s in the pool,
+ *   counting its n_s new ones, whose K/V must already be appended (the last
+ *   n_s positions).  Row j of sequence s sits at position seq_lens[s] - n_s + j
+ *   and attends to positions 0..that position:
+ *     out[query_start[s] + j][i] = sum_{t <= pos} softmax_t(scale * q.k_t) v_t
+ *   with query head i reading KV head i / (num_q_heads / num_kv_heads).
+ * max_query_len: host bound on every n_s (sizes the grid); a larger n_s sets
+ *   PKV_DEVERR_SEQ_LEN and its rows past the bound may be left unwritten.
+ * Rows of out outside every sequence's range are not written.
+ * Implemented for f16 / bf16 pools with q of the same type, head_size 128,
+ * num_q_heads / num_kv_heads in {1, 2, 4, 8}; others return
+ * PKV_ERR_UNSUPPORTED.  Inconsistent query_start / seq_lens (n_s < 0,
+ * n_s > seq_lens[s], past num_tokens or the block table) set
+ * PKV_DEVERR_SEQ_LEN and the sequence is skipped; a block id outside the pool
+ * sets PKV_DEVERR_BLOCK_ID.  Needs no workspace.
+ */
+pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype, int32_t num_tokens, int32_t num_q_heads,
+                                       int32_t num_seqs, const int32_t* query_start, int32_t max_query_len,
+                                       const void* k_cache, const void* v_cache, const pkv_cache_desc* desc,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, float scale, void* out, void* stream);
+
+/*
  * Partition size the automatic choice (partition_tokens = 0) would use for
  * these sizes on the current device, or a negative pkv_status on error.
  */
@@ -362,6 +395,16 @@ pkv_status pkv_alloc_free(pkv_alloc* a, int64_t seq_id);
  * to its state before the call. */
 pkv_status pkv_alloc_append_batch(pkv_alloc* a, const int64_t* seq_ids, int32_t n, int64_t* slots,
                                   int32_t* pairs, int32_t pairs_cap, int32_t* num_pairs);
+/* Chunked prefill: reserve counts[i] new token slots for sequence seq_ids[i]
+ * (each sequence at most once; counts[i] >= 0), in order, as append_slot
+ * would one token at a time.  slots (capacity slots_cap >= sum counts)
+ * receives the slots sequence after sequence; pairs receives the
+ * copy-on-write pairs ([*num_pairs][2], capacity pairs_cap >= n: only a
+ * sequence's first new token can land in a shared partial block).  All or
+ * nothing, like append_batch. */
+pkv_status pkv_alloc_append_tokens(pkv_alloc* a, const int64_t* seq_ids, const int32_t* counts, int32_t n,
+                                   int64_t* slots, int64_t slots_cap, int32_t* pairs, int32_t pairs_cap,
+                                   int32_t* num_pairs);
 /* Export padded block tables and lengths for a batch: tables is
  * [n][max_blocks] (unused entries -1), seq_lens [n]; a row whose seq_id is
  * negative gets length 0.  PKV_ERR_INVALID if a table does not fit. */

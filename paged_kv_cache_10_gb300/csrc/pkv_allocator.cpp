@@ -259,6 +259,45 @@ pkv_status pkv_alloc_append_batch(pkv_alloc* a, const int64_t* seq_ids, int32_t 
     return PKV_OK;
 }
 
+pkv_status pkv_alloc_append_tokens(pkv_alloc* a, const int64_t* seq_ids, const int32_t* counts, int32_t n,
+                                   int64_t* slots, int64_t slots_cap, int32_t* pairs, int32_t pairs_cap,
+                                   int32_t* num_pairs) {
+    if (!a || n < 0 || (n > 0 && (!seq_ids || !counts)) || !num_pairs) return PKV_ERR_INVALID;
+    if (pairs_cap < n || (n > 0 && !pairs)) return PKV_ERR_INVALID;
+    int64_t total = 0;
+    {
+        std::unordered_map<int64_t, int> seen;
+        for (int32_t i = 0; i < n; ++i) {
+            if (counts[i] < 0 || seq_ids[i] < 0 || seen[seq_ids[i]]++) return PKV_ERR_INVALID;
+            total += counts[i];
+        }
+    }
+    if (total > slots_cap || (total > 0 && !slots)) return PKV_ERR_INVALID;
+    std::vector<AppendUndo> undo;
+    undo.reserve(static_cast<size_t>(total));
+    int32_t np = 0;
+    int64_t k = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        for (int32_t t = 0; t < counts[i]; ++t, ++k) {
+            int32_t cs = -1, cd = -1;
+            AppendUndo u{};
+            pkv_status st = append_one(a, seq_ids[i], &slots[k], &cs, &cd, &u);
+            if (st != PKV_OK) {
+                for (auto r = undo.rbegin(); r != undo.rend(); ++r) undo_append(a, *r);
+                return st;
+            }
+            undo.push_back(u);
+            if (cs >= 0) {  // only a sequence's first new token can meet a shared partial block
+                pairs[2 * np] = cs;
+                pairs[2 * np + 1] = cd;
+                ++np;
+            }
+        }
+    }
+    *num_pairs = np;
+    return PKV_OK;
+}
+
 pkv_status pkv_alloc_export(const pkv_alloc* a, const int64_t* seq_ids, int32_t n, int32_t* tables,
                             int32_t max_blocks, int32_t* seq_lens) {
     if (!a || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !tables || !seq_lens)))

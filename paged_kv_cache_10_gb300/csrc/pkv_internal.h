@@ -89,6 +89,10 @@ cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);
 // Host helpers shared by the entry points (pkv_api.cu).
 int auto_partition(int S, int Hkv, int max_seq_len);
 bool encode_pool_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t rows, int D);
+// 3-D view of a 16-bit [T][H][D] tensor with a box of 64 elements x box_h x
+// box_t and the 128-byte swizzle (a box lands as box_t * box_h rows of 128
+// bytes, token-major).
+bool encode_token_head_map(CUtensorMap* map, const void* base, int D, int H, int64_t T, int box_h, int box_t);
 // Partials of S*Hq rows x NP partitions: m, l (256-byte aligned regions), o.
 size_t partials_bytes(int64_t S, int64_t Hq, int64_t D, int64_t NP);
 void partials_layout(DecodeParams& p, void* workspace);  // sets part_m/l/o from S, Hq, NP

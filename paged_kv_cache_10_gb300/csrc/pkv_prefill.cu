@@ -1,0 +1,475 @@
+// pkv_prefill.cu -- paged (chunked) prefill attention on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Prefill processes a prompt's tokens at once; chunked prefill cuts a long
+// prompt into chunks of at most a token budget that run in successive
+// iterations ("vLLM 高性能大语言模型推理引擎深度技术评估与分布式架构展望",
+// "PagedAttention 内存管理与核心数据结构" and its scheduling section on chunked
+// prefill).  A chunk's query tokens attend causally to the sequence's whole
+// history in the paged pool -- earlier chunks and their own chunk up to
+// themselves -- gathered through the block table like decode.
+//
+// One CTA takes 128 query rows of one (sequence, KV head): 128 / G tokens x
+// the G query heads of the group, so every key / value tile feeds all heads
+// that read it.  Per 128-key tile (8 pool blocks):
+//   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, fp32 in tensor memory
+//   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
+//   O += P V     tcgen05.mma with P from shared memory, O in tensor memory
+// Warp roles: warp 0 loads (TMA: Q once by a 3-D map, K and V per block by
+// the pool's 2-D map), warp 1 issues the MMAs and owns the tensor memory,
+// warps 2-5 run the online softmax, the O corrections and the epilogue.
+// S is double-buffered in tensor memory, so Q K^T of the next tile and P V
+// of the previous one run while the softmax works.  The running max is
+// rebased only when it grows by more than 2^8, which keeps every
+// probability <= 256 and skips most O corrections; the final O / l is the
+// same softmax.
+#include <cstdint>
+#include <mutex>
+#include <type_traits>
+
+#include "pkv_decode_mma.cuh"  // ex2, pack2, swz128, fence_proxy_async_smem
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kPD = 128;        // head_size
+constexpr int kTileM = 128;     // query rows per CTA
+constexpr int kTileN = 128;     // keys per tile
+constexpr int kStages = 2;      // K / V ring depth
+constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
+constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
+constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr float kRebase = 8.0f;  // log2 units
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kOpBytes;
+constexpr int kOffV = kOffK + kStages * kOpBytes;
+constexpr int kOffP = kOffV + kStages * kOpBytes;
+constexpr int kOffBar = kOffP + kOpBytes;
+// q_full, k_full[S], v_full[S], kv_empty[S], v_zero, s_full[2], s_free[2], p_full, o_done, drain
+constexpr int kNumBars = 1 + 3 * kStages + 1 + 2 + 2 + 3;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+struct PrefillParams {
+    const int32_t* query_start;  // [S + 1]
+    const int32_t* block_tables; // [S][MB]
+    const int32_t* seq_lens;     // [S], counting the new tokens
+    void* out;                   // [T][Hq][D]
+    int32_t S, T, Hq, Hkv, MB, NB;
+    int32_t G, TT;               // heads per KV head, tokens per CTA (128 / G)
+    int32_t num_qtiles;          // CTAs per (sequence, KV head) along the queries
+    int32_t max_query_len;       // the caller's bound on every chunk
+    float qk_scale;              // scale * log2(e)
+    unsigned int* err;
+};
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
+                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    constexpr bool kBF = std::is_same<T, BF16>::value;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+    uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    uint64_t* k_full = q_full + 1;
+    uint64_t* v_full = k_full + kStages;
+    uint64_t* kv_empty = v_full + kStages;
+    uint64_t* v_zero = kv_empty + kStages;
+    uint64_t* s_full = v_zero + 1;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* o_done = p_full + 1;
+    uint64_t* drain = o_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int s = blockIdx.z, h = blockIdx.y;
+    const int qt = p.num_qtiles - 1 - static_cast<int>(blockIdx.x);  // longest key ranges first
+
+    // ---- this CTA's rows and keys (uniform across the CTA)
+    const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
+    const int n = q1 - q0;
+    const int L = __ldg(p.seq_lens + s);
+    if (q0 < 0 || n < 0 || q1 > p.T || L < n || L > p.MB * kBlockSize) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+        return;
+    }
+    if (n > p.max_query_len && threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+    const int t0 = qt * p.TT;
+    if (t0 >= n) return;
+    const int ctx = L - n;                                // tokens before this chunk
+    const int kv_end = ctx + t0 + min(p.TT, n - t0);      // keys [0, kv_end)
+    const int nkt = (kv_end + kTileN - 1) / kTileN;
+    const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(k_full + i, 1);
+            mbar_init(v_full + i, 1);
+            mbar_init(kv_empty + i, 1);
+        }
+        mbar_init(v_zero, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(s_free + i, kSoftmaxThreads);
+        }
+        mbar_init(p_full, kSoftmaxThreads);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tO = tmem + 256;  // columns [0, 256): S double buffer
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        const uint64_t pol_q = policy_evict_first();
+        const uint64_t pol_kv = policy_evict_last();  // re-read by the sequence's other query tiles
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, kOpBytes);
+            for (int dh = 0; dh < 2; ++dh)
+                tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * p.G, q0 + t0, q_full, pol_q);
+        }
+        int issued = 0;
+        for (int j = 0; j < nkt; ++j) {
+            const int st = j % kStages;
+            const int nb_tile = min(8, nblk - j * 8);
+            int phys = 0;
+            if (lane < nb_tile) {
+                phys = __ldg(p.block_tables + static_cast<int64_t>(s) * p.MB + j * 8 + lane);
+                if (phys < 0 || phys >= p.NB) {
+                    report(p.err, PKV_DEVERR_BLOCK_ID);
+                    phys = 0;
+                }
+            }
+            const bool waited = j < kStages || mbar_wait(kv_empty + st, ((j / kStages) + 1) & 1);
+            if (!warp_all(waited)) {
+                if (lane == 0) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            if (!warp_all(*abort_flag == 0)) break;  // uniform across the warp
+            const int row = (phys * p.Hkv + h) * kBlockSize;
+            if (lane == 0) mbar_arrive_expect_tx(k_full + st, nb_tile * 2 * kBlockTileBytes);
+            __syncwarp();
+            if (lane < nb_tile) {
+                unsigned char* d = sm + kOffK + st * kOpBytes + lane * kBlockTileBytes;
+                tc::tma_load_2d(d, &tmk, 0, row, k_full + st, pol_kv);
+                tc::tma_load_2d(d + kHalfBytes, &tmk, 64, row, k_full + st, pol_kv);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(v_full + st, nb_tile * 2 * kBlockTileBytes);
+            __syncwarp();
+            if (lane < nb_tile) {
+                unsigned char* d = sm + kOffV + st * kOpBytes + lane * kBlockTileBytes;
+                tc::tma_load_2d(d, &tmv, 0, row, v_full + st, pol_kv);
+                tc::tma_load_2d(d + kHalfBytes, &tmv, 64, row, v_full + st, pol_kv);
+            }
+            issued = j + 1;
+            if (j == nkt - 1) {
+                // Value rows at or past kv_end get probability 0, but the
+                // pool slots past a sequence's end (and never-loaded rows)
+                // may hold any bits, NaN included, and 0 * NaN = NaN in the
+                // MMA: clear them once the tile has landed.
+                const int r0 = kv_end - j * kTileN;
+                bool okv = true;
+                if (r0 < kTileN) {
+                    okv = warp_all(mbar_wait(v_full + st, (j / kStages) & 1));
+                    if (okv) {
+                        unsigned char* vb = sm + kOffV + st * kOpBytes;
+                        for (int idx = lane; idx < (kTileN - r0) * 16; idx += 32) {
+                            const int r = r0 + (idx >> 4), c = idx & 15;
+                            *reinterpret_cast<uint4*>(vb + (c >> 3) * kHalfBytes + swz128(r, c & 7)) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (!okv) {
+                        report(p.err, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    tc::arrive(v_zero);
+                }
+            }
+        }
+        // every copy this warp started has landed before the CTA can exit
+        for (int j = max(0, issued - kStages); j < issued; ++j) {
+            const int st = j % kStages;
+            const bool ok = mbar_wait(k_full + st, (j / kStages) & 1) && mbar_wait(v_full + st, (j / kStages) & 1);
+            if (!ok && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        if (lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
+            const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
+            const uint32_t aQ = smem_addr(sm + kOffQ), aP = smem_addr(sm + kOffP);
+            bool ok = mbar_wait(q_full, 0);
+            for (int j = 0; ok && j <= nkt; ++j) {
+                if (*abort_flag) break;
+                if (j < nkt) {
+                    const int st = j % kStages, sb = j & 1;
+                    ok = mbar_wait(k_full + st, (j / kStages) & 1);
+                    if (ok && j >= 2) ok = mbar_wait(s_free + sb, ((j >> 1) + 1) & 1);
+                    if (!ok) break;
+                    tc::fence_after();
+                    const uint32_t aK = smem_addr(sm + kOffK + st * kOpBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kPD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        tc::mma_f16(tmem + sb * kTileN, tc::sdesc_sw128(aQ + off, 16, 1024),
+                                    tc::sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
+                    }
+                    tc::commit(s_full + sb);
+                }
+                if (j >= 1) {
+                    const int i = j - 1, st = i % kStages;
+                    ok = mbar_wait(v_full + st, (i / kStages) & 1);
+                    if (ok && i == nkt - 1) ok = mbar_wait(v_zero, 0);
+                    if (ok) ok = mbar_wait(p_full, i & 1);
+                    if (!ok) break;
+                    tc::fence_after();
+                    const uint32_t aV = smem_addr(sm + kOffV + st * kOpBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTileN / 16; ++kk) {
+                        tc::mma_f16(tO, tc::sdesc_sw128(aP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
+                                    tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024), idO,
+                                    i > 0 || kk > 0);
+                    }
+                    tc::commit(o_done);
+                    tc::commit(kv_empty + st);
+                }
+            }
+            if (!ok) {
+                report(p.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // the tensor core is idle before the memory it uses is released
+            tc::commit(drain);
+            if (!mbar_wait(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- softmax, O, epilogue
+        const int wq = warp & 3;  // tensor-memory lane quarter of this warp
+        const int row = wq * 32 + lane;
+        const int tt = row / p.G, g = row - tt * p.G;
+        const bool row_valid = t0 + tt < n;
+        const int pos = ctx + t0 + min(tt, n - 1 - t0);  // padding rows reuse the last position
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        unsigned char* Ps = sm + kOffP;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkt; ++j) {
+            const int sb = j & 1;
+            ok = warp_all(mbar_wait(s_full + sb, (j >> 1) & 1));
+            if (!ok || !warp_all(*abort_flag == 0)) break;
+            tc::fence_after();
+            uint32_t x[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::ld32(tmem + lane_base + sb * kTileN + c * 32, x[c]);
+            tc::wait_ld();
+            tc::fence_before();
+            tc::arrive(s_free + sb);
+
+            const int key0 = j * kTileN;
+            const bool masked = key0 + kTileN - 1 > ctx + t0;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float v = __uint_as_float(x[c][i]) * p.qk_scale;
+                    if (masked && key0 + c * 32 + i > pos) v = -INFINITY;
+                    x[c][i] = __float_as_uint(v);
+                    mt = fmaxf(mt, v);
+                }
+            const float m_new = fmaxf(m_ref, mt);
+            const bool rebase = m_new > m_ref + kRebase;
+            float alpha = 1.f;
+            if (rebase) {
+                alpha = ex2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
+                m_ref = m_new;
+            }
+            float lsum = 0.f;
+            uint32_t pk[4][16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = ex2(__uint_as_float(x[c][2 * i]) - m_ref);
+                    const float b = ex2(__uint_as_float(x[c][2 * i + 1]) - m_ref);
+                    lsum += a + b;
+                    pk[c][i] = pack2<kBF>(a, b);
+                }
+            l = l * alpha + lsum;
+
+            if (j > 0) {
+                // P V of the previous tile has finished: P may be rewritten
+                // and O rescaled
+                ok = warp_all(mbar_wait(o_done, (j - 1) & 1));
+                if (!ok) break;
+                tc::fence_after();
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk = c * 4 + q4;  // 8 probabilities
+                    *reinterpret_cast<uint4*>(Ps + (chunk >> 3) * kHalfBytes + swz128(row, chunk & 7)) =
+                        make_uint4(pk[c][4 * q4], pk[c][4 * q4 + 1], pk[c][4 * q4 + 2], pk[c][4 * q4 + 3]);
+                }
+            if (j > 0 && __any_sync(0xffffffffu, rebase)) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tc::ld32(tO + lane_base + c * 32, o);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tc::st32(tO + lane_base + c * 32, o);
+                }
+                tc::wait_st();
+            }
+            fence_proxy_async_smem();
+            tc::fence_before();
+            tc::arrive(p_full);
+        }
+        const bool live = ok && warp_all(*abort_flag == 0);
+        if (live) ok = warp_all(mbar_wait(o_done, (nkt - 1) & 1));
+        if (live && ok) {
+            tc::fence_after();
+            const float inv = 1.f / l;
+            typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
+                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[32];
+                tc::ld32(tO + lane_base + c * 32, o);
+                tc::wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack2<kBF>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                        w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                        w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                        w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + v4 * 8) = w;
+                    }
+                }
+            }
+        } else if (!ok) {
+            if (lane == 0) {
+                report(p.err, PKV_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename T>
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           cudaStream_t st) {
+    static std::once_flag once[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaError_t attr = cudaSuccess;
+    std::call_once(once[dev], [&] {
+        attr = cudaFuncSetAttribute(prefill_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr != cudaSuccess) return attr;
+    const dim3 grid(p.num_qtiles, p.Hkv, p.S);
+    prefill_tc_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype, int32_t num_tokens,
+                                                  int32_t num_q_heads, int32_t num_seqs, const int32_t* query_start,
+                                                  int32_t max_query_len, const void* k_cache, const void* v_cache,
+                                                  const pkv_cache_desc* desc, const int32_t* block_tables,
+                                                  int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale,
+                                                  void* out, void* stream) {
+    if (!desc || num_tokens < 0 || num_seqs < 0 || max_query_len < 0 || num_q_heads <= 0) return PKV_ERR_INVALID;
+    if (desc->block_size != kBlockSize || desc->num_kv_heads <= 0 || desc->num_blocks <= 0) return PKV_ERR_INVALID;
+    if (num_q_heads % desc->num_kv_heads) return PKV_ERR_INVALID;
+    const int G = num_q_heads / desc->num_kv_heads;
+    if (desc->head_size != kPD || (G != 1 && G != 2 && G != 4 && G != 8)) return PKV_ERR_UNSUPPORTED;
+    if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
+    if (!(scale == scale)) return PKV_ERR_INVALID;
+    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+    if (!q || !out || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start) return PKV_ERR_INVALID;
+    if (max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_INVALID;
+    if (num_seqs > 65535 || desc->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    unsigned int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+
+    PrefillParams p{};
+    p.query_start = query_start;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.S = num_seqs;
+    p.T = num_tokens;
+    p.Hq = num_q_heads;
+    p.Hkv = desc->num_kv_heads;
+    p.MB = max_blocks_per_seq;
+    p.NB = desc->num_blocks;
+    p.G = G;
+    p.TT = kTileM / G;
+    p.num_qtiles = (max_query_len + p.TT - 1) / p.TT;
+    p.max_query_len = max_query_len;
+    p.qk_scale = scale * 1.4426950408889634f;
+    p.err = err;
+
+    CUtensorMap tq, tk, tv;
+    const int64_t pool_rows = static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize;
+    if (!encode_token_head_map(&tq, q, kPD, num_q_heads, num_tokens, G, kTileM / G) || !encode_pool_map(&tk, k_cache, 2, pool_rows, kPD) ||
+        !encode_pool_map(&tv, v_cache, 2, pool_rows, kPD))
+        return PKV_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = desc->kv_dtype == PKV_BF16 ? launch_prefill<BF16>(p, tq, tk, tv, st)
+                                                      : launch_prefill<F16>(p, tq, tk, tv, st);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -33,6 +33,7 @@ EXPORTED = [
     "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
     "pkv_alloc_fail_after", "pkv_paged_attention_decode_cascade", "pkv_decode_cascade_workspace_bytes",
     "pkv_alloc_prefix_groups", "pkv_swap_blocks", "pkv_alloc_swap_out", "pkv_alloc_swap_in",
+    "pkv_paged_attention_prefill", "pkv_alloc_append_tokens",
 ]
 
 
@@ -116,6 +117,9 @@ def lib():
         "pkv_swap_blocks": (i32, [P, P, D, P, P, i32, P, i32, i32, P]),
         "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
+        "pkv_alloc_append_tokens": (i32, [P, P, P, i32, P, i64, P, i32, P]),
+        "pkv_paged_attention_prefill": (i32, [P, i32, i32, i32, i32, P, i32, P, P, D, P, i32, P, ctypes.c_float,
+                                              P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -306,6 +310,22 @@ def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_t
     _check(st, "paged_attention_decode_cascade")
 
 
+def paged_attention_prefill(q, k_cache, v_cache, desc: CacheDesc, query_start, max_query_len: int, block_tables,
+                            seq_lens, scale: float, out, q_dtype: str | None = None, stream=None) -> None:
+    """Causal paged prefill: q, out [T, Hq, D]; query_start int32 [S + 1],
+    block_tables int32 [S, MB], seq_lens int32 [S] (device tensors)."""
+    T, Hq = int(q.shape[0]), int(q.shape[1])
+    S = int(seq_lens.shape[0])
+    if int(query_start.shape[0]) != S + 1:
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    st = lib().pkv_paged_attention_prefill(
+        _dev_ptr(q, "q"), _dtype_code(q, q_dtype), T, Hq, S, _dev_ptr(query_start, "query_start"), int(max_query_len),
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
+        _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
+        float(scale), _dev_ptr(out, "out"), _stream(stream))
+    _check(st, "paged_attention_prefill")
+
+
 SWAP_OUT, SWAP_IN = 0, 1
 
 
@@ -388,6 +408,22 @@ class Allocator:
         _check(lib().pkv_alloc_append_batch(self._h, _np_ptr(ids), n, _np_ptr(slots), _np_ptr(pairs), max(n, 1),
                                             ctypes.byref(npairs)), "alloc_append_batch")
         return slots, pairs[: npairs.value].copy()
+
+    def append_tokens(self, seq_ids, counts):
+        """Reserves counts[i] new token slots for seq_ids[i] (chunked
+        prefill); returns (slots [sum counts], copy-on-write pairs [n, 2])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        n = ids.shape[0]
+        if cnt.shape != (n,):
+            raise ValueError("seq_ids and counts differ in length")
+        total = int(cnt.sum()) if n else 0
+        slots = np.empty(max(total, 1), np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int32)
+        npairs = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_append_tokens(self._h, _np_ptr(ids), _np_ptr(cnt), n, _np_ptr(slots), total,
+                                             _np_ptr(pairs), max(n, 1), ctypes.byref(npairs)), "alloc_append_tokens")
+        return slots[:total].copy(), pairs[: npairs.value].copy()
 
     def export(self, seq_ids, max_blocks: int):
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)

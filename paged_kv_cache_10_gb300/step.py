@@ -136,3 +136,53 @@ class DecodeStep:
             self.run()
         torch.cuda.synchronize()
         return graph
+
+
+class PrefillStep:
+    """Device state and launch sequence of one paged (chunked) prefill step.
+
+    Host: the allocator holds every sequence's earlier context, then reserves
+    one slot per new token (``append_tokens``).  Device, in stream order: ``paged_kv_append`` of the new
+    tokens' K/V -> ``paged_attention_prefill`` for their query rows."""
+
+    def __init__(self, wl, device="cuda", alloc: pk.Allocator | None = None):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.dtype,
+                                 block_size=wl.b)
+        self.alloc = alloc or pk.Allocator(wl.NB, wl.b, wl.free_order)
+        for s, c in enumerate(wl.ctx):
+            self.alloc.seq_new(s, int(c))
+        self.slots, self.pairs = self.alloc.append_tokens(np.arange(wl.S), wl.qlens)
+        assert len(self.pairs) == 0  # no block is shared
+        self.tables, self.seq_lens = self.alloc.export(np.arange(wl.S, dtype=np.int64), wl.max_blocks)
+        self.query_start = np.zeros(wl.S + 1, np.int32)
+        self.query_start[1:] = np.cumsum(np.asarray(wl.qlens, dtype=np.int64))
+        dev = self.device
+        self.k_cache = _to_dev(wl.k_pool, dev)
+        self.v_cache = _to_dev(wl.v_pool, dev)
+        self.q = _to_dev(wl.q, dev)
+        self.k_new = _to_dev(wl.k_new, dev)
+        self.v_new = _to_dev(wl.v_new, dev)
+        self.d_slots = torch.from_numpy(self.slots).to(dev)
+        self.d_tables = torch.from_numpy(self.tables).to(dev)
+        self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
+        self.d_query_start = torch.from_numpy(self.query_start).to(dev)
+        self.out = torch.empty((wl.T, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
+
+    def kernel_launches(self) -> int:
+        return 2  # append + prefill attention
+
+    def append(self, stream=None):
+        pk.paged_kv_append(self.k_new, self.v_new, self.d_slots, self.k_cache, self.v_cache, self.desc,
+                           in_dtype=self.wl.dtype, stream=stream)
+
+    def attend(self, stream=None, q=None, out=None):
+        pk.paged_attention_prefill(self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
+                                   self.d_query_start, self.wl.max_query_len, self.d_tables, self.d_lens,
+                                   self.wl.scale, self.out if out is None else out, q_dtype=self.wl.dtype,
+                                   stream=stream)
+
+    def run(self, stream=None):
+        self.append(stream)
+        self.attend(stream)

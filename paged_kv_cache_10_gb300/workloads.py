@@ -28,8 +28,16 @@ prefix sharing with reference counts) on Llama-shaped heads:
                   sequence appends one token (copy-on-write where the pair's
                   last block is partial); 32/8 heads, D 128, bf16
 
-In every workload each sequence appends exactly one new token in the step and
-``seq_len`` counts it.
+In every decode workload each sequence appends exactly one new token in the
+step and ``seq_len`` counts it.
+
+Prefill workloads (``PREFILL``) append a chunk of new tokens per sequence and
+run causal attention for them:
+
+  prefill_chunked_gqa  8 chunks of 512 tokens after U[0,3584] tokens of
+                       context each (a 4096-token batch), 32/8 heads, bf16
+  prefill_prompt_gqa   4 whole prompts of 4096 tokens, 32/8 heads, bf16
+  prefill_prompt_mha   4 whole prompts of 2048 tokens, 32/32 heads, bf16
 """
 from __future__ import annotations
 
@@ -272,6 +280,93 @@ def fork_groups(name, seed, groups, singles, Hq, Hkv, D=128, kv_dtype="bf16", pa
     NB = need + math.ceil(0.25 * need)
     return build(name, seed, s, Hq, Hkv, D, NB, kv_dtype, kv_dtype, setup, list(range(s)), lens,
                  partition_tokens=partition_tokens)
+
+
+@dataclass
+class PrefillWorkload:
+    """Inputs of one paged (chunked) prefill step: sequence s already holds
+    ctx[s] tokens in the pool (allocator script "new"), then appends qlens[s]
+    new tokens (k_new / v_new rows, packed sequence after sequence) and runs
+    causal attention for those rows (q rows, packed the same way)."""
+    name: str
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    NB: int
+    dtype: str            # "f16" | "bf16" (q, pool, appended k/v, output)
+    scale: float
+    ctx: list
+    qlens: list
+    q: np.ndarray          # raw bits [T, Hq, D]
+    k_pool: np.ndarray     # raw bits [NB, Hkv, b, D]
+    v_pool: np.ndarray
+    k_new: np.ndarray      # raw bits [T, Hkv, D]
+    v_new: np.ndarray
+    free_order: np.ndarray
+    b: int = BLOCK_SIZE
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.qlens))
+
+    @property
+    def seq_lens(self) -> list:
+        return [int(c) + int(n) for c, n in zip(self.ctx, self.qlens)]
+
+    @property
+    def max_blocks(self) -> int:
+        return max(1, max(_blocks(L) for L in self.seq_lens))
+
+    @property
+    def max_query_len(self) -> int:
+        return max(self.qlens) if self.qlens else 0
+
+
+def prefill(name, seed, ctx, qlens, Hq, Hkv, D=128, dtype="bf16", NB=None) -> PrefillWorkload:
+    ss = np.random.SeedSequence(seed)
+    s_q, s_k, s_v, s_kn, s_vn, s_free = ss.spawn(6)
+    ctx = [int(c) for c in ctx]
+    qlens = [int(n) for n in qlens]
+    T = sum(qlens)
+    need = sum(_blocks(c + n) for c, n in zip(ctx, qlens))
+    NB = NB or max(4, need + math.ceil(0.10 * need))
+    k_pool, _ = _values(s_k, (NB, Hkv, BLOCK_SIZE, D), dtype)
+    v_pool, _ = _values(s_v, (NB, Hkv, BLOCK_SIZE, D), dtype)
+    q, _ = _values(s_q, (T, Hq, D), dtype)
+    k_new, _ = _values(s_kn, (T, Hkv, D), dtype)
+    v_new, _ = _values(s_vn, (T, Hkv, D), dtype)
+    free_order = np.random.Generator(np.random.PCG64(s_free)).permutation(NB).astype(np.int32)
+    return PrefillWorkload(name=name, S=len(ctx), Hq=Hq, Hkv=Hkv, D=D, NB=NB, dtype=dtype, scale=1.0 / math.sqrt(D),
+                           ctx=ctx, qlens=qlens, q=q, k_pool=k_pool, v_pool=v_pool, k_new=k_new, v_new=v_new,
+                           free_order=free_order)
+
+
+def prefill_chunked_gqa(seed=1010) -> PrefillWorkload:
+    """Chunked prefill, Llama-3-8B-shaped heads (32 / 8, D 128, bf16): a
+    4096-token batch of 8 chunks of 512 tokens, each continuing a prompt with
+    U[0, 3584] tokens already in the pool."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(7)[6]))
+    ctx = rng.integers(0, 3584, size=8, endpoint=True)
+    return prefill("prefill_chunked_gqa", seed, ctx, [512] * 8, 32, 8)
+
+
+def prefill_prompt_gqa(seed=1011) -> PrefillWorkload:
+    """Whole-prompt prefill, Llama-3-8B-shaped heads: 4 prompts of 4096 tokens."""
+    return prefill("prefill_prompt_gqa", seed, [0] * 4, [4096] * 4, 32, 8)
+
+
+def prefill_prompt_mha(seed=1012) -> PrefillWorkload:
+    """Whole-prompt prefill, Llama-7B-shaped heads (32 / 32, D 128, bf16): 4
+    prompts of 2048 tokens."""
+    return prefill("prefill_prompt_mha", seed, [0] * 4, [2048] * 4, 32, 32)
+
+
+PREFILL = {
+    "prefill_chunked_gqa": prefill_chunked_gqa,
+    "prefill_prompt_gqa": prefill_prompt_gqa,
+    "prefill_prompt_mha": prefill_prompt_mha,
+}
 
 
 NAMED = {

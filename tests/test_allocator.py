@@ -340,3 +340,49 @@ def test_swap_out_is_all_or_nothing(pk):
     with pytest.raises(pk.OutOfBlocks):
         dev.swap_out(host, 1)
     assert (dev.block_table(1), dev.num_free(), host.num_free()) == before
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_append_tokens_matches_model(pk, seed):
+    """Chunked-prefill slot reservation equals the model's append_slot one
+    token at a time, including copy-on-write of a shared partial block by a
+    sequence's first new token."""
+    rng = np.random.default_rng(300 + seed)
+    NB = 200
+    free = rng.permutation(NB).astype(np.int32)
+    a, m = pk.Allocator(NB, 16, free), AllocatorModel(NB, 16, free)
+    for s in range(6):
+        L = int(rng.integers(0, 90))
+        a.seq_new(s, L)
+        m.seq_new(s, L)
+    a.fork(2, 10)
+    m.fork(2, 10)
+    seqs = [10, 0, 3, 2, 5]
+    counts = [int(rng.integers(0, 60)) for _ in seqs]
+    slots, pairs = a.append_tokens(seqs, counts)
+    want_slots, want_pairs = [], []
+    for s, c in zip(seqs, counts):
+        for _ in range(c):
+            slot, cow = m.append_slot(s)
+            want_slots.append(slot)
+            if cow:
+                want_pairs.append(cow)
+    assert slots.tolist() == want_slots
+    assert [tuple(p) for p in pairs.tolist()] == want_pairs
+    for s in list(range(6)) + [10]:
+        assert a.block_table(s) == m.block_table(s)
+    assert a.num_free() == m.num_free()
+
+
+def test_append_tokens_is_all_or_nothing(pk):
+    a = pk.Allocator(6, 16)
+    a.seq_new(0, 20)
+    a.seq_new(1, 5)
+    before = (a.block_table(0), a.block_table(1), a.num_free())
+    with pytest.raises(pk.OutOfBlocks):
+        a.append_tokens([0, 1], [30, 60])  # needs 2 + 4 blocks, 3 free
+    assert (a.block_table(0), a.block_table(1), a.num_free()) == before
+    with pytest.raises(pk.PagedKVError):
+        a.append_tokens([0, 0], [1, 1])  # a sequence twice
+    with pytest.raises(pk.PagedKVError):
+        a.append_tokens([0], [-1])

@@ -1,0 +1,183 @@
+"""Paged (chunked) prefill attention on the GPU against the float64 oracle:
+every output element on small mixed batches (several query and key tiles,
+ragged tails, empty chunks, all group sizes, both 16-bit types), sampled rows
+of the full-size workloads (each sampled token is one decode row of the
+oracle at its own position), the appended pool bytes, and the error paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.allocator_model import AllocatorModel
+from parity_util import TOL, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_10_gb300 import build, pagedkv
+    build.build()
+    pagedkv.lib()
+    return pagedkv
+
+
+def run(wl):
+    from paged_kv_cache_10_gb300.step import PrefillStep
+    st = PrefillStep(wl, device="cuda")
+    st.run()
+    torch.cuda.synchronize()
+    return st
+
+
+def model(wl):
+    """Slots, block tables and lengths from the independent allocator model."""
+    m = AllocatorModel(wl.NB, wl.b, wl.free_order)
+    for s, c in enumerate(wl.ctx):
+        m.seq_new(s, c)
+    slots = []
+    for s, n in enumerate(wl.qlens):
+        for _ in range(n):
+            slot, cow = m.append_slot(s)
+            assert cow is None
+            slots.append(slot)
+    tables = np.full((wl.S, wl.max_blocks), -1, np.int32)
+    lens = np.zeros(wl.S, np.int32)
+    for s in range(wl.S):
+        t = m.block_table(s)
+        tables[s, :len(t)] = t
+        lens[s] = m.lens[s]
+    return np.array(slots, np.int64), tables, lens
+
+
+def oracle_pools(wl, slots):
+    kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    return kp, vp
+
+
+def check_full(st):
+    wl = st.wl
+    slots, tables, lens = model(wl)
+    assert np.array_equal(st.slots, slots)
+    assert np.array_equal(st.tables, tables)
+    assert np.array_equal(st.seq_lens, lens)
+    kp, vp = oracle_pools(wl, slots)
+    assert np.array_equal(host_bits(st.k_cache), kp)
+    assert np.array_equal(host_bits(st.v_cache), vp)
+    ref = oracle.paged_prefill(wl.q, wl.dtype, st.query_start, kp, vp, wl.dtype, tables, lens, wl.scale)
+    got = oracle.dequantize(host_bits(st.out), wl.dtype)
+    assert np.all(np.isfinite(got))
+    return float(np.max(np.abs(got - ref))), float(np.max(np.abs(ref)))
+
+
+CASES = [
+    # ctx, qlens: ragged query tiles, key tiles, empty chunks, single tokens
+    ([0, 37, 5, 300, 0, 129], [20, 45, 1, 130, 0, 128]),
+    ([700, 0, 16, 255], [1, 300, 17, 257]),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("case", [0, 1])
+def test_prefill_matches_oracle_every_element(lib, dtype, G, case):
+    from paged_kv_cache_10_gb300 import workloads
+    ctx, qlens = CASES[case]
+    Hkv = 2
+    wl = workloads.prefill("prefill_small", 2000 + 10 * G + case, ctx, qlens, Hkv * G, Hkv, dtype=dtype)
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL[dtype], (err, mx)
+
+
+@pytest.mark.parametrize("name", ["prefill_chunked_gqa", "prefill_prompt_gqa", "prefill_prompt_mha"])
+def test_prefill_full_size_sampled_rows(lib, name):
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.PREFILL[name]()
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    slots, tables, lens = model(wl)
+    assert np.array_equal(st.slots, slots) and np.array_equal(st.tables, tables)
+    kp, vp = oracle_pools(wl, slots)
+    # sampled tokens: first and last of every chunk plus a stride through it
+    rows, seqs, pos = [], [], []
+    qs = st.query_start
+    for s in range(wl.S):
+        n = wl.qlens[s]
+        for j in sorted({0, n - 1, *range(0, n, 97)}):
+            rows.append(qs[s] + j)
+            seqs.append(s)
+            pos.append(int(lens[s]) - n + j)
+    rows = np.array(rows)
+    # one decode row of the oracle per sampled token: its own position is the
+    # last key it may see
+    ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.dtype, kp, vp, wl.dtype,
+                              np.ascontiguousarray(tables[seqs]), np.array(pos, np.int32) + 1, wl.scale)
+    got = oracle.dequantize(host_bits(st.out)[rows], wl.dtype)
+    assert np.all(np.isfinite(got))
+    err = float(np.max(np.abs(got - ref)))
+    assert err <= TOL[wl.dtype], err
+    # every row was written (finite) and the appended pool bytes match
+    assert np.all(np.isfinite(oracle.dequantize(host_bits(st.out), wl.dtype)))
+    assert np.array_equal(host_bits(st.k_cache), kp)
+    assert np.array_equal(host_bits(st.v_cache), vp)
+
+
+def test_prefill_ignores_nan_bytes_past_the_sequence_end(lib):
+    """Pool slots past a sequence's last token (never written) may hold NaN
+    bit patterns; they get probability 0 and must not reach the output."""
+    from paged_kv_cache_10_gb300 import workloads
+    # no earlier context: every key is appended in the step, so every other
+    # pool byte (the rest of each last block, unused blocks) may be NaN
+    wl = workloads.prefill("prefill_nan", 2101, [0, 0, 0], [10, 7, 150], 8, 2, dtype="bf16")
+    wl.k_pool[:] = 0x7fc1
+    wl.v_pool[:] = 0x7fc1
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["bf16"], (err, mx)
+
+
+def test_prefill_rejects_bad_arguments(lib):
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import PrefillStep
+    wl = workloads.prefill("prefill_err", 2102, [5, 0], [9, 30], 8, 2, dtype="bf16")
+    st = PrefillStep(wl, device="cuda")
+    st.run()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    # more new tokens than the sequence holds: flagged, sequence skipped
+    bad_lens = st.d_lens.clone()
+    bad_lens[1] = 10
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                st.d_tables, bad_lens, wl.scale, st.out, q_dtype="bf16")
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_SEQ_LEN
+    # a grid bound below the longest chunk: flagged
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, 8,
+                                st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_SEQ_LEN
+    # block id outside the pool: flagged
+    bad_tables = st.d_tables.clone()
+    bad_tables[0, 0] = wl.NB + 5
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                bad_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_BLOCK_ID
+    # unsupported: q type differing from the pool, head_size 64
+    with pytest.raises(lib.PagedKVError):
+        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                    st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="f16")
+    d64 = lib.CacheDesc(num_blocks=wl.NB, num_kv_heads=2, head_size=64, kv_dtype="bf16")
+    with pytest.raises(lib.PagedKVError):
+        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, d64, st.d_query_start, wl.max_query_len,
+                                    st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
+    # the context is still usable and the correct call still matches
+    st.attend()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["bf16"], (err, mx)
