@@ -432,6 +432,184 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------------ prefill step
+PREFILL_METRIC = "paged prefill attention TFLOP/s (causal, % of GB300 dense bf16 peak) and us/step, 1 GPU"
+
+
+def prefill_flops(wl) -> float:
+    """Algorithmic flops of causal attention for the step's new tokens: each
+    row at position p does q.k and p.v over p + 1 keys, 4 * D flops per key
+    and query head."""
+    tot = 0
+    for c, n in zip(wl.ctx, wl.qlens):
+        tot += n * c + n * (n + 1) // 2  # sum over the chunk of (position + 1)
+    return 4.0 * wl.D * wl.Hq * tot
+
+
+def prefill_bytes(wl) -> int:
+    """Least bytes the step must move: q and out, every key / value of each
+    sequence once per KV head, the appended k / v (read and written)."""
+    kv = sum(wl.seq_lens) * 2 * wl.Hkv * wl.D * 2
+    return 2 * wl.T * wl.Hq * wl.D * 2 + kv + wl.T * 2 * wl.Hkv * wl.D * 2 * 2
+
+
+def measured_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    return 1900.0, "fallback"
+
+
+def prefill_cpu_baseline(wl, budget_s=10.0):
+    """The float64 oracle on the first tokens of each chunk in turn (all
+    heads, each with every key it sees), about budget_s of CPU time."""
+    import oracle
+    from paged_kv_cache_10_gb300.pagedkv import Allocator
+    a = Allocator(wl.NB, wl.b, wl.free_order)
+    for s, c in enumerate(wl.ctx):
+        a.seq_new(s, int(c))
+    slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
+    tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
+    kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
+    m, flops, dt, reps = 8, 0.0, 0.0, 0
+    while dt < budget_s and reps < 10000:
+        s = reps % wl.S
+        n = min(m, wl.qlens[s])
+        if n == 0:
+            reps += 1
+            continue
+        ctx = int(lens[s]) - wl.qlens[s]
+        q = np.ascontiguousarray(wl.q[qs[s]:qs[s] + n])
+        t = time.perf_counter()
+        oracle.paged_prefill(q, wl.dtype, np.array([0, n], np.int32), kp, vp, wl.dtype, tables[s:s + 1],
+                             np.array([ctx + n], np.int32), wl.scale)
+        dt += time.perf_counter() - t
+        flops += 4.0 * wl.D * wl.Hq * (n * ctx + n * (n + 1) // 2)
+        if reps == 0 and dt < budget_s / 50:
+            m = min(4096, m * 4)
+        reps += 1
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} chunk heads of {wl.name} (first <= {m} tokens of a chunk, all heads, every key "
+                      f"they see): float64 causal attention, {dt:.1f} s"}
+
+
+def run_prefill(args, rank, world, local_rank):
+    from paged_kv_cache_10_gb300 import pagedkv as pk
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import PrefillStep
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = workloads.PREFILL[args.workload]()
+    step = PrefillStep(wl, device=dev)
+    flops = prefill_flops(wl)
+    nbytes = prefill_bytes(wl)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = nbytes < 4 * l2
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if flush else None
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    t_load0 = time.monotonic()
+    for i in range(K):
+        if flush:
+            flush_buf.zero_()
+        ev[i][0].record(stream)
+        step.append()
+        ev[i][1].record(stream)
+        step.attend()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_load1 = time.monotonic()
+    barrier()
+    total_ms = sum(a.elapsed_time(c) for a, _, c in ev)
+    attn_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if sampler and not args.profile and t_load1 - t_load0 < 1.0:
+        t_ext = time.monotonic()
+        while time.monotonic() - t_ext < 1.5:
+            for _ in range(20):
+                step.run()
+            torch.cuda.synchronize()
+        t_load1 = time.monotonic()
+    tot_flops, tot_s = aggregate(flops * K, total_ms / 1e3)
+    value = tot_flops / tot_s / 1e12
+
+    # end to end through the public API: inputs from pinned host memory, output back
+    h = {"q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(), "v": step.v_new.cpu().pin_memory(),
+         "slots": step.d_slots.cpu().pin_memory(), "tables": step.d_tables.cpu().pin_memory(),
+         "lens": step.d_lens.cpu().pin_memory(), "qs": step.d_query_start.cpu().pin_memory()}
+    d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
+    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_h.numel() * out_h.element_size()
+    Ke = 0 if args.profile else max(1, min(K, 100))
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        if flush:
+            flush_buf.zero_()
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        pk.paged_kv_append(d["k"], d["v"], d["slots"], step.k_cache, step.v_cache, step.desc, in_dtype=wl.dtype)
+        pk.paged_attention_prefill(d["q"], step.k_cache, step.v_cache, step.desc, d["qs"], wl.max_query_len,
+                                   d["tables"], d["lens"], wl.scale, step.out, q_dtype=wl.dtype)
+        out_h.copy_(step.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if flush and Ke:
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(Ke):
+            flush_buf.zero_()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms -= f0.elapsed_time(f1)
+    e2e_flops, e2e_s = aggregate(flops * Ke, max(e2e_ms, 1e-6) / 1e3)
+    assert pk.get_device_error() == 0, "device error word set during the benchmark"
+    if rank != 0:
+        return None
+    clocks = sampler.summary(t_load0, t_load1) if sampler else None
+    if sampler:
+        sampler.stop()
+    peak, peak_kind = measured_tensor_peak()
+    a_ms = statistics.mean(attn_ms)
+    achieved = flops / (a_ms / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "us_per_step": round(1e3 * total_ms / K, 2),
+        "tokens_per_s": round(world * wl.T / (tot_s / K), 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype + ", fp32 accumulate", "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D,
+                   "new_tokens": wl.T, "chunk_tokens": wl.qlens, "context_tokens": wl.ctx, "num_blocks": wl.NB,
+                   "flops_per_step": flops, "min_bytes_per_step": nbytes,
+                   "l2": ("flushed between steps (2x L2 write)" if flush else "inputs larger than L2, no flush"),
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": K * step.kernel_launches(),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "prefill_tc_kernel", "mean_launch_us": round(a_ms * 1e3, 2),
+                     "algorithmic_flops_per_launch": flops,
+                     "hbm_gbs_at_min_bytes": round(nbytes / (a_ms / 1e3) / 1e9, 1)},
+        "clocks": clocks,
+    }
+    if world == 1 and not (args.no_cpu_baseline or args.profile):
+        line["cpu_baseline"] = prefill_cpu_baseline(wl)
+    return line
+
+
 # ------------------------------------------------------------ swap timing
 def run_swap(args, local_rank):
     """Times pkv_swap_blocks on the workload's pool: all blocks of the first
@@ -548,7 +726,11 @@ def main(argv=None):
             import torch.distributed as dist
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-        line = run_ours(args, rank, world, local_rank)
+        from paged_kv_cache_10_gb300 import workloads
+        if args.workload in workloads.PREFILL:
+            line = run_prefill(args, rank, world, local_rank)
+        else:
+            line = run_ours(args, rank, world, local_rank)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
