@@ -14,12 +14,14 @@
 // that read it.  Per 128-key tile (8 pool blocks):
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, fp32 in tensor memory
 //   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
-//   O += P V     tcgen05.mma with P from shared memory, O in tensor memory
+//   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory
 // Warp roles: warp 0 loads (TMA: Q once by a 3-D map, K and V per block by
 // the pool's 2-D map), warp 1 issues the MMAs and owns the tensor memory,
-// warps 2-5 run the online softmax, the O corrections and the epilogue.
-// S is double-buffered in tensor memory, so Q K^T of the next tile and P V
-// of the previous one run while the softmax works.  The running max is
+// warps 2-9 run the online softmax, the O corrections and the epilogue, two
+// threads per query row (64 keys / O columns each).
+// S is double-buffered in tensor memory and P_j is written back over S_j,
+// where the P V MMA reads it as its A operand; Q K^T of the next tile and
+// P V of the previous one run while the softmax works.  The running max is
 // rebased only when it grows by more than 2^8, which keeps every
 // probability <= 256 and skips most O corrections; the final O / l is the
 // same softmax.
@@ -36,22 +38,24 @@ namespace {
 constexpr int kPD = 128;        // head_size
 constexpr int kTileM = 128;     // query rows per CTA
 constexpr int kTileN = 128;     // keys per tile
-constexpr int kStages = 2;      // K / V ring depth
+constexpr int kStages = 2;      // K ring and V ring depth
 constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
 constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
 constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
-constexpr int kThreads = 192;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 320;          // load warp, MMA warp, 8 softmax warps
+constexpr int kSoftmaxThreads = 256;
 constexpr float kRebase = 8.0f;  // log2 units
 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kOpBytes;
 constexpr int kOffV = kOffK + kStages * kOpBytes;
-constexpr int kOffP = kOffV + kStages * kOpBytes;
-constexpr int kOffBar = kOffP + kOpBytes;
-// q_full, k_full[S], v_full[S], kv_empty[S], v_zero, s_full[2], s_free[2], p_full, o_done, drain
-constexpr int kNumBars = 1 + 3 * kStages + 1 + 2 + 2 + 3;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kOffBar = kOffV + kStages * kOpBytes;
+// q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_zero, s_full[2], p_full[2], o_done[2], drain,
+// pair[4 quarters][2 tile parities], pair_end[4]
+constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1 + 8 + 4;
+constexpr int kOffXch = kOffBar + kNumBars * 8;  // float [2 tile parities][2 halves][128]: tile maxima
+constexpr int kOffXl = kOffXch + 2 * 2 * kTileM * 4;  // float [2 halves][128]: row sums
+constexpr int kOffMisc = kOffXl + 2 * kTileM * 4;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -70,6 +74,34 @@ struct PrefillParams {
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand (M = 128 lanes) read from
+// tensor memory, two 16-bit elements per 32-bit column (column c of lane r
+// holds A[r][2c] in its low half, A[r][2c + 1] in its high half), so one
+// K = 16 step spans 8 columns.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Waits, in order, for the phases of o_done barrier `bar` (P V of tiles b,
+// b + 2, ... for the barrier of tile parity b) up to the one of tile `upto`;
+// `next` is the next tile of that parity to wait for.  The barrier is at
+// most one phase ahead of `next` whenever this runs, so parity waits stay
+// exact.
+__device__ __forceinline__ bool consume_pv(uint64_t* bar, int& next, int upto) {
+    bool ok = true;
+    while (ok && next <= upto) {
+        ok = mbar_wait(bar, (next >> 1) & 1);
+        next += 2;
+    }
+    return ok;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
@@ -79,14 +111,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + kOffBar);
     uint64_t* k_full = q_full + 1;
-    uint64_t* v_full = k_full + kStages;
-    uint64_t* kv_empty = v_full + kStages;
-    uint64_t* v_zero = kv_empty + kStages;
-    uint64_t* s_full = v_zero + 1;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
-    uint64_t* o_done = p_full + 1;
-    uint64_t* drain = o_done + 1;
+    uint64_t* k_empty = k_full + kStages;
+    uint64_t* v_full = k_empty + kStages;
+    uint64_t* v_empty = v_full + kStages;
+    uint64_t* v_zero = v_empty + kStages;
+    uint64_t* s_full = v_zero + 1;   // [2]
+    uint64_t* p_full = s_full + 2;   // [2], by tile parity
+    uint64_t* o_done = p_full + 2;   // [2], by tile parity
+    uint64_t* drain = o_done + 2;
+    uint64_t* pair = drain + 1;      // [4][2]
+    uint64_t* pair_end = pair + 8;   // [4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
@@ -114,17 +148,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(q_full, 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full + i, 1);
+            mbar_init(k_empty + i, 1);
             mbar_init(v_full + i, 1);
-            mbar_init(kv_empty + i, 1);
+            mbar_init(v_empty + i, 1);
         }
         mbar_init(v_zero, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
-            mbar_init(s_free + i, kSoftmaxThreads);
+            mbar_init(p_full + i, kSoftmaxThreads);
+            mbar_init(o_done + i, 1);
         }
-        mbar_init(p_full, kSoftmaxThreads);
-        mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(pair + i, 64);
+        for (int i = 0; i < 4; ++i) mbar_init(pair_end + i, 64);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -136,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256;  // columns [0, 256): S double buffer
+    // columns [0, 256): S of even / odd tiles (its first 64 columns then hold
+    // that tile's P, two 16-bit probabilities per column); [256, 384): O
+    const uint32_t tO = tmem + 256;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -150,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued = 0;
         for (int j = 0; j < nkt; ++j) {
             const int st = j % kStages;
+            const uint32_t empty_par = ((j / kStages) + 1) & 1;
             const int nb_tile = min(8, nblk - j * 8);
             int phys = 0;
             if (lane < nb_tile) {
@@ -159,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phys = 0;
                 }
             }
-            const bool waited = j < kStages || mbar_wait(kv_empty + st, ((j / kStages) + 1) & 1);
+            const int row = (phys * p.Hkv + h) * kBlockSize;
+            // keys: the stage is free once Q K^T of tile j - kStages is done
+            bool waited = j < kStages || mbar_wait(k_empty + st, empty_par);
             if (!warp_all(waited)) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
@@ -168,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (!warp_all(*abort_flag == 0)) break;  // uniform across the warp
-            const int row = (phys * p.Hkv + h) * kBlockSize;
             if (lane == 0) mbar_arrive_expect_tx(k_full + st, nb_tile * 2 * kBlockTileBytes);
             __syncwarp();
             if (lane < nb_tile) {
@@ -176,7 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_2d(d, &tmk, 0, row, k_full + st, pol_kv);
                 tc::tma_load_2d(d + kHalfBytes, &tmk, 64, row, k_full + st, pol_kv);
             }
-            __syncwarp();
+            // values: free once P V of tile j - kStages is done
+            waited = j < kStages || mbar_wait(v_empty + st, empty_par);
+            if (!warp_all(waited)) {
+                if (lane == 0) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                issued = -(j + 1);  // keys of tile j were issued, values not
+                break;
+            }
             if (lane == 0) mbar_arrive_expect_tx(v_full + st, nb_tile * 2 * kBlockTileBytes);
             __syncwarp();
             if (lane < nb_tile) {
@@ -215,25 +264,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // every copy this warp started has landed before the CTA can exit
-        for (int j = max(0, issued - kStages); j < issued; ++j) {
-            const int st = j % kStages;
-            const bool ok = mbar_wait(k_full + st, (j / kStages) & 1) && mbar_wait(v_full + st, (j / kStages) & 1);
-            if (!ok && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
-        }
+        const int kdone = issued < 0 ? -issued : issued;  // tiles whose keys were issued
+        const int vdone = issued < 0 ? -issued - 1 : issued;
+        for (int j = max(0, kdone - kStages); j < kdone; ++j)
+            if (!mbar_wait(k_full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+        for (int j = max(0, vdone - kStages); j < vdone; ++j)
+            if (!mbar_wait(v_full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
         if (lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
+        // Issue order S_0, S_1, P V_0, S_2, P V_1, ...: tcgen05.mma from one
+        // thread run in order, so S_{j+2} overwrites the tensor-memory buffer
+        // of S_j / P_j only after P V_j has read P_j.
         if (lane == 0) {
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
             const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
-            const uint32_t aQ = smem_addr(sm + kOffQ), aP = smem_addr(sm + kOffP);
+            const uint32_t aQ = smem_addr(sm + kOffQ);
             bool ok = mbar_wait(q_full, 0);
             for (int j = 0; ok && j <= nkt; ++j) {
                 if (*abort_flag) break;
                 if (j < nkt) {
                     const int st = j % kStages, sb = j & 1;
                     ok = mbar_wait(k_full + st, (j / kStages) & 1);
-                    if (ok && j >= 2) ok = mbar_wait(s_free + sb, ((j >> 1) + 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                     const uint32_t aK = smem_addr(sm + kOffK + st * kOpBytes);
@@ -244,23 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tc::sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
                     }
                     tc::commit(s_full + sb);
+                    tc::commit(k_empty + st);
                 }
                 if (j >= 1) {
                     const int i = j - 1, st = i % kStages;
                     ok = mbar_wait(v_full + st, (i / kStages) & 1);
                     if (ok && i == nkt - 1) ok = mbar_wait(v_zero, 0);
-                    if (ok) ok = mbar_wait(p_full, i & 1);
+                    if (ok) ok = mbar_wait(p_full + (i & 1), (i >> 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                     const uint32_t aV = smem_addr(sm + kOffV + st * kOpBytes);
+                    const uint32_t aP = tmem + (i & 1) * kTileN;
 #pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk) {
-                        tc::mma_f16(tO, tc::sdesc_sw128(aP + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024),
-                                    tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024), idO,
-                                    i > 0 || kk > 0);
-                    }
-                    tc::commit(o_done);
-                    tc::commit(kv_empty + st);
+                    for (int kk = 0; kk < kTileN / 16; ++kk)
+                        mma_f16_tmem_a(tO, aP + kk * 8, tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024),
+                                       idO, i > 0 || kk > 0);
+                    tc::commit(o_done + (i & 1));
+                    tc::commit(v_empty + st);
                 }
             }
             if (!ok) {
@@ -274,39 +326,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------- softmax, O, epilogue
-        const int wq = warp & 3;  // tensor-memory lane quarter of this warp
+        // Two threads per query row: warps 2-5 take keys / O columns 0-63,
+        // warps 6-9 columns 64-127, of the row in their tensor-memory lane
+        // quarter.  The two halves of a row exchange their tile maxima (and
+        // at the end their sums) through shared memory.  P_j goes back into
+        // tensor memory over S_j; the softmax waits for a P V only when it
+        // has to rescale O.
+        const int wq = warp & 3;            // tensor-memory lane quarter
+        const int hf = (warp - 2) >> 2;     // column half
         const int row = wq * 32 + lane;
         const int tt = row / p.G, g = row - tt * p.G;
         const bool row_valid = t0 + tt < n;
         const int pos = ctx + t0 + min(tt, n - 1 - t0);  // padding rows reuse the last position
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        unsigned char* Ps = sm + kOffP;
+        const uint32_t col0 = static_cast<uint32_t>(hf * 64);
+        float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2 tiles][2 halves][128 rows]
+        float* xl = reinterpret_cast<float*>(sm + kOffXl);    // [2 halves][128 rows]
+        const float c = p.qk_scale;
         float m_ref = -INFINITY, l = 0.f;
+        int next_even = 0, next_odd = 1;  // next P V (tile index) to wait for, per parity
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int sb = j & 1;
             ok = warp_all(mbar_wait(s_full + sb, (j >> 1) & 1));
             if (!ok || !warp_all(*abort_flag == 0)) break;
             tc::fence_after();
-            uint32_t x[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tc::ld32(tmem + lane_base + sb * kTileN + c * 32, x[c]);
+            uint32_t x[2][32];
+            tc::ld32(tmem + lane_base + sb * kTileN + col0, x[0]);
+            tc::ld32(tmem + lane_base + sb * kTileN + col0 + 32, x[1]);
             tc::wait_ld();
-            tc::fence_before();
-            tc::arrive(s_free + sb);
 
-            const int key0 = j * kTileN;
-            const bool masked = key0 + kTileN - 1 > ctx + t0;
-            float mt = -INFINITY;
+            // raw-score maximum (scale > 0 keeps the order); masked keys -inf
+            const int key0 = j * kTileN + hf * 64;
+            if (key0 + 63 > pos) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float v = __uint_as_float(x[c][i]) * p.qk_scale;
-                    if (masked && key0 + c * 32 + i > pos) v = -INFINITY;
-                    x[c][i] = __float_as_uint(v);
-                    mt = fmaxf(mt, v);
-                }
+                    for (int i = 0; i < 32; ++i)
+                        if (key0 + h2 * 32 + i > pos) x[h2][i] = __float_as_uint(-INFINITY);
+            }
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(x[h2][i]));
+            float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            xch[(sb * 2 + hf) * kTileM + row] = mt;
+            tc::arrive(pair + wq * 2 + sb);
+            ok = warp_all(mbar_wait(pair + wq * 2 + sb, (j >> 1) & 1));
+            if (!ok) break;
+            mt = fmaxf(mt, xch[(sb * 2 + (hf ^ 1)) * kTileM + row]) * c;
             const float m_new = fmaxf(m_ref, mt);
             const bool rebase = m_new > m_ref + kRebase;
             float alpha = 1.f;
@@ -314,61 +383,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 alpha = ex2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
                 m_ref = m_new;
             }
-            float lsum = 0.f;
-            uint32_t pk[4][16];
+            const float nm = -m_ref;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float a = ex2(__uint_as_float(x[c][2 * i]) - m_ref);
-                    const float b = ex2(__uint_as_float(x[c][2 * i + 1]) - m_ref);
-                    lsum += a + b;
-                    pk[c][i] = pack2<kBF>(a, b);
+                    const float e0 = ex2(fmaf(__uint_as_float(x[h2][2 * i]), c, nm));
+                    const float e1 = ex2(fmaf(__uint_as_float(x[h2][2 * i + 1]), c, nm));
+                    ls[i & 3] += e0 + e1;
+                    pk[h2 * 16 + i] = pack2<kBF>(e0, e1);
                 }
-            l = l * alpha + lsum;
+            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
+            tc::st32(tmem + lane_base + sb * kTileN + hf * 32, pk);
 
-            if (j > 0) {
-                // P V of the previous tile has finished: P may be rewritten
-                // and O rescaled
-                ok = warp_all(mbar_wait(o_done, (j - 1) & 1));
-                if (!ok) break;
-                tc::fence_after();
-            }
+            // keep both o_done barriers within one phase of this thread
+            if (j >= 2) ok = warp_all(sb ? consume_pv(o_done + 1, next_odd, j - 2) : consume_pv(o_done, next_even, j - 2));
+            if (ok && j > 0 && __any_sync(0xffffffffu, rebase)) {
+                // O must hold P V of tile j - 1 before it is rescaled
+                ok = warp_all(sb ? consume_pv(o_done, next_even, j - 1) : consume_pv(o_done + 1, next_odd, j - 1));
+                if (ok) {
+                    tc::fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t o[32];
+                        tc::ld32(tO + lane_base + col0 + h2 * 32, o);
+                        tc::wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = c * 4 + q4;  // 8 probabilities
-                    *reinterpret_cast<uint4*>(Ps + (chunk >> 3) * kHalfBytes + swz128(row, chunk & 7)) =
-                        make_uint4(pk[c][4 * q4], pk[c][4 * q4 + 1], pk[c][4 * q4 + 2], pk[c][4 * q4 + 3]);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tc::st32(tO + lane_base + col0 + h2 * 32, o);
+                    }
                 }
-            if (j > 0 && __any_sync(0xffffffffu, rebase)) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t o[32];
-                    tc::ld32(tO + lane_base + c * 32, o);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tc::st32(tO + lane_base + c * 32, o);
-                }
-                tc::wait_st();
             }
-            fence_proxy_async_smem();
+            tc::wait_st();
+            if (!ok) break;
             tc::fence_before();
-            tc::arrive(p_full);
+            tc::arrive(p_full + sb);
         }
         const bool live = ok && warp_all(*abort_flag == 0);
-        if (live) ok = warp_all(mbar_wait(o_done, (nkt - 1) & 1));
+        if (live) {
+            ok = warp_all(consume_pv(o_done, next_even, nkt - 1));
+            ok = warp_all(ok && consume_pv(o_done + 1, next_odd, nkt - 1));
+        }
         if (live && ok) {
             tc::fence_after();
-            const float inv = 1.f / l;
+            // row sum of both halves
+            xl[hf * kTileM + row] = l;
+            tc::arrive(pair_end + wq);
+            ok = warp_all(mbar_wait(pair_end + wq, 0));
+        }
+        if (live && ok) {
+            const float inv = 1.f / (l + xl[(hf ^ 1) * kTileM + row]);
             typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
-                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD;
+                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD + col0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t o[32];
-                tc::ld32(tO + lane_base + c * 32, o);
+                tc::ld32(tO + lane_base + col0 + h2 * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -378,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
                         w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
                         w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + v4 * 8) = w;
+                        *reinterpret_cast<uint4*>(orow + h2 * 32 + v4 * 8) = w;
                     }
                 }
             }
@@ -435,7 +507,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     if (desc->head_size != kPD || (G != 1 && G != 2 && G != 4 && G != 8)) return PKV_ERR_UNSUPPORTED;
     if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
-    if (!(scale == scale)) return PKV_ERR_INVALID;
+    if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID;  // finite, > 0 (max on raw scores)
     if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
     if (!q || !out || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start) return PKV_ERR_INVALID;
     if (max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
