@@ -15,8 +15,9 @@
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, fp32 in tensor memory
 //   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
 //   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory
-// Warp roles: warp 0 loads (TMA: Q once by a 3-D map, K and V per block by
-// the pool's 2-D map), warp 1 issues the MMAs and owns the tensor memory,
+// Warp roles: warp 0 loads Q (once, by a 3-D TMA map) and the key tiles,
+// warp 10 the value tiles (per pool block, by the pool's 2-D map), each
+// through a 3-stage ring; warp 1 issues the MMAs and owns the tensor memory;
 // warps 2-9 run the online softmax, the O corrections and the epilogue, two
 // threads per query row (64 keys / O columns each).
 // S is double-buffered in tensor memory and P_j is written back over S_j,
@@ -38,11 +39,12 @@ namespace {
 constexpr int kPD = 128;        // head_size
 constexpr int kTileM = 128;     // query rows per CTA
 constexpr int kTileN = 128;     // keys per tile
-constexpr int kStages = 2;      // K ring and V ring depth
+constexpr int kStages = 3;      // K ring and V ring depth
 constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
 constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
 constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
-constexpr int kThreads = 320;          // load warp, MMA warp, 8 softmax warps
+constexpr int kThreads = 352;          // K-load warp, MMA warp, 8 softmax warps, V-load warp
+constexpr int kVWarp = 10;
 constexpr int kSoftmaxThreads = 256;
 constexpr float kRebase = 8.0f;  // log2 units
 
@@ -51,11 +53,12 @@ constexpr int kOffK = kOffQ + kOpBytes;
 constexpr int kOffV = kOffK + kStages * kOpBytes;
 constexpr int kOffBar = kOffV + kStages * kOpBytes;
 // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_zero, s_full[2], p_full[2], o_done[2], drain,
-// pair[4 quarters][2 tile parities], pair_end[4]
-constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1 + 8 + 4;
-constexpr int kOffXch = kOffBar + kNumBars * 8;  // float [2 tile parities][2 halves][128]: tile maxima
-constexpr int kOffXl = kOffXch + 2 * 2 * kTileM * 4;  // float [2 halves][128]: row sums
-constexpr int kOffMisc = kOffXl + 2 * kTileM * 4;
+// pair_end[4 quarters]
+constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1 + 4;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+// float [2 halves][128 rows] of row sums at the end, over K stage 0 (free
+// by then: every MMA has completed)
+constexpr int kOffXl = kOffK;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -96,7 +99,7 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 __device__ __forceinline__ bool consume_pv(uint64_t* bar, int& next, int upto) {
     bool ok = true;
     while (ok && next <= upto) {
-        ok = mbar_wait(bar, (next >> 1) & 1);
+        ok = tc::wait_spin(bar, (next >> 1) & 1);
         next += 2;
     }
     return ok;
@@ -119,8 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;   // [2], by tile parity
     uint64_t* o_done = p_full + 2;   // [2], by tile parity
     uint64_t* drain = o_done + 2;
-    uint64_t* pair = drain + 1;      // [4][2]
-    uint64_t* pair_end = pair + 8;   // [4]
+    uint64_t* pair_end = drain + 1;  // [4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
@@ -159,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(o_done + i, 1);
         }
         mbar_init(drain, 1);
-        for (int i = 0; i < 8; ++i) mbar_init(pair + i, 64);
         for (int i = 0; i < 4; ++i) mbar_init(pair_end + i, 64);
         *abort_flag = 0;
         mbar_init_fence();
@@ -176,31 +177,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // that tile's P, two 16-bit probabilities per column); [256, 384): O
     const uint32_t tO = tmem + 256;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        const uint64_t pol_q = policy_evict_first();
+    if (warp == 0 || warp == kVWarp) {
+        // --------------------------------------------- TMA producers (K, V)
+        // Warp 0 streams Q and the key tiles, warp 10 the value tiles, each
+        // through its own 3-stage ring, so a key load never waits for a P V
+        // to free a value stage.  Block ids are read one tile ahead.
+        const bool is_k = warp == 0;
         const uint64_t pol_kv = policy_evict_last();  // re-read by the sequence's other query tiles
-        if (lane == 0) {
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        const CUtensorMap* map = is_k ? &tmk : &tmv;
+        unsigned char* ring = sm + (is_k ? kOffK : kOffV);
+        if (is_k && lane == 0) {
             mbar_arrive_expect_tx(q_full, kOpBytes);
             for (int dh = 0; dh < 2; ++dh)
-                tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * p.G, q0 + t0, q_full, pol_q);
+                tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * p.G, q0 + t0, q_full,
+                                policy_evict_first());
         }
-        int issued = 0;
-        for (int j = 0; j < nkt; ++j) {
-            const int st = j % kStages;
-            const uint32_t empty_par = ((j / kStages) + 1) & 1;
-            const int nb_tile = min(8, nblk - j * 8);
+        const int32_t* bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
+        auto block_id = [&](int j) {
             int phys = 0;
-            if (lane < nb_tile) {
-                phys = __ldg(p.block_tables + static_cast<int64_t>(s) * p.MB + j * 8 + lane);
+            if (lane < 8 && j * 8 + lane < nblk) {
+                phys = __ldg(bt + j * 8 + lane);
                 if (phys < 0 || phys >= p.NB) {
                     report(p.err, PKV_DEVERR_BLOCK_ID);
                     phys = 0;
                 }
             }
+            return phys;
+        };
+        int phys_next = block_id(0);
+        int issued = 0;
+        for (int j = 0; j < nkt; ++j) {
+            const int st = j % kStages;
+            const int nb_tile = min(8, nblk - j * 8);
+            const int phys = phys_next;
+            if (j + 1 < nkt) phys_next = block_id(j + 1);
             const int row = (phys * p.Hkv + h) * kBlockSize;
-            // keys: the stage is free once Q K^T of tile j - kStages is done
-            bool waited = j < kStages || mbar_wait(k_empty + st, empty_par);
+            // the stage is free once the MMA that read it (Q K^T or P V of
+            // tile j - kStages) has completed
+            const bool waited = j < kStages || mbar_wait(empty + st, ((j / kStages) + 1) & 1);
             if (!warp_all(waited)) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
@@ -209,32 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (!warp_all(*abort_flag == 0)) break;  // uniform across the warp
-            if (lane == 0) mbar_arrive_expect_tx(k_full + st, nb_tile * 2 * kBlockTileBytes);
+            if (lane == 0) mbar_arrive_expect_tx(full + st, nb_tile * 2 * kBlockTileBytes);
             __syncwarp();
             if (lane < nb_tile) {
-                unsigned char* d = sm + kOffK + st * kOpBytes + lane * kBlockTileBytes;
-                tc::tma_load_2d(d, &tmk, 0, row, k_full + st, pol_kv);
-                tc::tma_load_2d(d + kHalfBytes, &tmk, 64, row, k_full + st, pol_kv);
-            }
-            // values: free once P V of tile j - kStages is done
-            waited = j < kStages || mbar_wait(v_empty + st, empty_par);
-            if (!warp_all(waited)) {
-                if (lane == 0) {
-                    report(p.err, PKV_DEVERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                issued = -(j + 1);  // keys of tile j were issued, values not
-                break;
-            }
-            if (lane == 0) mbar_arrive_expect_tx(v_full + st, nb_tile * 2 * kBlockTileBytes);
-            __syncwarp();
-            if (lane < nb_tile) {
-                unsigned char* d = sm + kOffV + st * kOpBytes + lane * kBlockTileBytes;
-                tc::tma_load_2d(d, &tmv, 0, row, v_full + st, pol_kv);
-                tc::tma_load_2d(d + kHalfBytes, &tmv, 64, row, v_full + st, pol_kv);
+                unsigned char* d = ring + st * kOpBytes + lane * kBlockTileBytes;
+                tc::tma_load_2d(d, map, 0, row, full + st, pol_kv);
+                tc::tma_load_2d(d + kHalfBytes, map, 64, row, full + st, pol_kv);
             }
             issued = j + 1;
-            if (j == nkt - 1) {
+            if (!is_k && j == nkt - 1) {
                 // Value rows at or past kv_end get probability 0, but the
                 // pool slots past a sequence's end (and never-loaded rows)
                 // may hold any bits, NaN included, and 0 * NaN = NaN in the
@@ -264,13 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // every copy this warp started has landed before the CTA can exit
-        const int kdone = issued < 0 ? -issued : issued;  // tiles whose keys were issued
-        const int vdone = issued < 0 ? -issued - 1 : issued;
-        for (int j = max(0, kdone - kStages); j < kdone; ++j)
-            if (!mbar_wait(k_full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
-        for (int j = max(0, vdone - kStages); j < vdone; ++j)
-            if (!mbar_wait(v_full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
-        if (lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+        for (int j = max(0, issued - kStages); j < issued; ++j)
+            if (!mbar_wait(full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+        if (is_k && lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         // Issue order S_0, S_1, P V_0, S_2, P V_1, ...: tcgen05.mma from one
@@ -280,12 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
             const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
             const uint32_t aQ = smem_addr(sm + kOffQ);
-            bool ok = mbar_wait(q_full, 0);
+            bool ok = tc::wait_spin(q_full, 0);
             for (int j = 0; ok && j <= nkt; ++j) {
                 if (*abort_flag) break;
                 if (j < nkt) {
                     const int st = j % kStages, sb = j & 1;
-                    ok = mbar_wait(k_full + st, (j / kStages) & 1);
+                    ok = tc::wait_spin(k_full + st, (j / kStages) & 1);
                     if (!ok) break;
                     tc::fence_after();
                     const uint32_t aK = smem_addr(sm + kOffK + st * kOpBytes);
@@ -300,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (j >= 1) {
                     const int i = j - 1, st = i % kStages;
-                    ok = mbar_wait(v_full + st, (i / kStages) & 1);
-                    if (ok && i == nkt - 1) ok = mbar_wait(v_zero, 0);
-                    if (ok) ok = mbar_wait(p_full + (i & 1), (i >> 1) & 1);
+                    ok = tc::wait_spin(v_full + st, (i / kStages) & 1);
+                    if (ok && i == nkt - 1) ok = tc::wait_spin(v_zero, 0);
+                    if (ok) ok = tc::wait_spin(p_full + (i & 1), (i >> 1) & 1);
                     if (!ok) break;
                     tc::fence_after();
                     const uint32_t aV = smem_addr(sm + kOffV + st * kOpBytes);
@@ -321,17 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // the tensor core is idle before the memory it uses is released
             tc::commit(drain);
-            if (!mbar_wait(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+            if (!tc::wait_spin(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
         }
         __syncwarp();
     } else {
         // ------------------------------------------- softmax, O, epilogue
         // Two threads per query row: warps 2-5 take keys / O columns 0-63,
         // warps 6-9 columns 64-127, of the row in their tensor-memory lane
-        // quarter.  The two halves of a row exchange their tile maxima (and
-        // at the end their sums) through shared memory.  P_j goes back into
-        // tensor memory over S_j; the softmax waits for a P V only when it
-        // has to rescale O.
+        // quarter.  Both read the whole row of S for its maximum, so they
+        // take the same rebasing decisions without talking; they add their
+        // sums through shared memory at the end.  P_j goes back into tensor
+        // memory over S_j; the softmax waits for a P V only when it has to
+        // rescale O.
         const int wq = warp & 3;            // tensor-memory lane quarter
         const int hf = (warp - 2) >> 2;     // column half
         const int row = wq * 32 + lane;
@@ -340,15 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pos = ctx + t0 + min(tt, n - 1 - t0);  // padding rows reuse the last position
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t col0 = static_cast<uint32_t>(hf * 64);
-        float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2 tiles][2 halves][128 rows]
-        float* xl = reinterpret_cast<float*>(sm + kOffXl);    // [2 halves][128 rows]
+        float* xl = reinterpret_cast<float*>(sm + kOffXl);  // [2 halves][128 rows], used at the end
         const float c = p.qk_scale;
         float m_ref = -INFINITY, l = 0.f;
         int next_even = 0, next_odd = 1;  // next P V (tile index) to wait for, per parity
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int sb = j & 1;
-            ok = warp_all(mbar_wait(s_full + sb, (j >> 1) & 1));
+            ok = warp_all(tc::wait_spin(s_full + sb, (j >> 1) & 1));
             if (!ok || !warp_all(*abort_flag == 0)) break;
             tc::fence_after();
             uint32_t x[2][32];
@@ -356,7 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::ld32(tmem + lane_base + sb * kTileN + col0 + 32, x[1]);
             tc::wait_ld();
 
-            // raw-score maximum (scale > 0 keeps the order); masked keys -inf
+            // masked keys -inf; the row maximum over all 128 keys of the tile
+            // (this half's from registers, the other half's read again from
+            // tensor memory) -- raw scores, as scale > 0 keeps the order
             const int key0 = j * kTileN + hf * 64;
             if (key0 + 63 > pos) {
 #pragma unroll
@@ -370,12 +367,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(x[h2][i]));
-            float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            xch[(sb * 2 + hf) * kTileM + row] = mt;
-            tc::arrive(pair + wq * 2 + sb);
-            ok = warp_all(mbar_wait(pair + wq * 2 + sb, (j >> 1) & 1));
-            if (!ok) break;
-            mt = fmaxf(mt, xch[(sb * 2 + (hf ^ 1)) * kTileM + row]) * c;
+            const int okey0 = j * kTileN + (hf ^ 1) * 64;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t y[32];
+                tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64) + h2 * 32, y);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float v = okey0 + h2 * 32 + i > pos ? -INFINITY : __uint_as_float(y[i]);
+                    mx[i & 3] = fmaxf(mx[i & 3], v);
+                }
+            }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
             const float m_new = fmaxf(m_ref, mt);
             const bool rebase = m_new > m_ref + kRebase;
             float alpha = 1.f;
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // row sum of both halves
             xl[hf * kTileM + row] = l;
             tc::arrive(pair_end + wq);
-            ok = warp_all(mbar_wait(pair_end + wq, 0));
+            ok = warp_all(tc::wait_spin(pair_end + wq, 0));
         }
         if (live && ok) {
             const float inv = 1.f / (l + xl[(hf ^ 1) * kTileM + row]);

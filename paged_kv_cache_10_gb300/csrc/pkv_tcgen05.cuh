@@ -123,6 +123,36 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                  : "memory");
 }
 
+// Bounded spin on an mbarrier phase for latency-critical handoffs: polls
+// without a suspend hint (a suspended thread can resume late) and gives up
+// after about 2 s of global time; false on timeout.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool poll(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity) {
+    if (poll(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (poll(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
 // Plain arrival on an mbarrier (release, CTA scope).
 __device__ __forceinline__ void arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
