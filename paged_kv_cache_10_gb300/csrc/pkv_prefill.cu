@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------------------- TMA producers (K, V)
         // Warp 0 streams Q and the key tiles, warp 10 the value tiles, each
         // through its own 3-stage ring, so a key load never waits for a P V
-        // to free a value stage.  Block ids are read one tile ahead.
+        // to free a value stage.
         const bool is_k = warp == 0;
         const uint64_t pol_kv = policy_evict_last();  // re-read by the sequence's other query tiles
         uint64_t* full = is_k ? k_full : v_full;
@@ -194,25 +194,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * p.G, q0 + t0, q_full,
                                 policy_evict_first());
         }
+        // block ids 32 at a time (4 tiles), loaded 4 tiles before their use:
+        // lane l holds the id of block 32 * batch + l
         const int32_t* bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
-        auto block_id = [&](int j) {
-            int phys = 0;
-            if (lane < 8 && j * 8 + lane < nblk) {
-                phys = __ldg(bt + j * 8 + lane);
-                if (phys < 0 || phys >= p.NB) {
-                    report(p.err, PKV_DEVERR_BLOCK_ID);
-                    phys = 0;
-                }
-            }
-            return phys;
+        auto load_ids = [&](int batch) {
+            const int idx = batch * 32 + lane;
+            return idx < nblk ? __ldg(bt + idx) : 0;
         };
-        int phys_next = block_id(0);
+        int ids_cur = load_ids(0);
+        int ids_nxt = load_ids(1);
         int issued = 0;
         for (int j = 0; j < nkt; ++j) {
             const int st = j % kStages;
             const int nb_tile = min(8, nblk - j * 8);
-            const int phys = phys_next;
-            if (j + 1 < nkt) phys_next = block_id(j + 1);
+            if (j > 0 && (j & 3) == 0) {
+                ids_cur = ids_nxt;
+                ids_nxt = load_ids((j >> 2) + 1);
+            }
+            int phys = __shfl_sync(0xffffffffu, ids_cur, ((j & 3) << 3) + (lane & 7));
+            if (lane < nb_tile && (phys < 0 || phys >= p.NB)) {
+                report(p.err, PKV_DEVERR_BLOCK_ID);
+                phys = 0;
+            }
             const int row = (phys * p.Hkv + h) * kBlockSize;
             // the stage is free once the MMA that read it (Q K^T or P V of
             // tile j - kStages) has completed
@@ -346,15 +349,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = warp_all(tc::wait_spin(s_full + sb, (j >> 1) & 1));
             if (!ok || !warp_all(*abort_flag == 0)) break;
             tc::fence_after();
-            uint32_t x[2][32];
+            // this half's 64 scores, and the other half's for the row maximum
+            // (all four loads in flight before the one wait)
+            uint32_t x[2][32], y[2][32];
             tc::ld32(tmem + lane_base + sb * kTileN + col0, x[0]);
             tc::ld32(tmem + lane_base + sb * kTileN + col0 + 32, x[1]);
+            tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64), y[0]);
+            tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64) + 32, y[1]);
             tc::wait_ld();
 
-            // masked keys -inf; the row maximum over all 128 keys of the tile
-            // (this half's from registers, the other half's read again from
-            // tensor memory) -- raw scores, as scale > 0 keeps the order
-            const int key0 = j * kTileN + hf * 64;
+            // masked keys -inf; the row maximum over all 128 keys of the
+            // tile -- raw scores, as scale > 0 keeps the order
+            const int key0 = j * kTileN + hf * 64, okey0 = j * kTileN + (hf ^ 1) * 64;
             if (key0 + 63 > pos) {
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2)
@@ -366,19 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(x[h2][i]));
-            const int okey0 = j * kTileN + (hf ^ 1) * 64;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                uint32_t y[32];
-                tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64) + h2 * 32, y);
-                tc::wait_ld();
-#pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float v = okey0 + h2 * 32 + i > pos ? -INFINITY : __uint_as_float(y[i]);
-                    mx[i & 3] = fmaxf(mx[i & 3], v);
+                    const float v = okey0 + h2 * 32 + i > pos ? -INFINITY : __uint_as_float(y[h2][i]);
+                    mx[i & 3] = fmaxf(mx[i & 3], fmaxf(__uint_as_float(x[h2][i]), v));
                 }
-            }
             const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
             const float m_new = fmaxf(m_ref, mt);
             const bool rebase = m_new > m_ref + kRebase;
