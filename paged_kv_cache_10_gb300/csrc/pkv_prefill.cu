@@ -16,10 +16,10 @@
 //   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
 //   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory
 // Warp roles: warp 0 loads Q (once, by a 3-D TMA map) and the key tiles,
-// warp 10 the value tiles (per pool block, by the pool's 2-D map), each
+// warp 6 the value tiles (per pool block, by the pool's 2-D map), each
 // through a 3-stage ring; warp 1 issues the MMAs and owns the tensor memory;
-// warps 2-9 run the online softmax, the O corrections and the epilogue, two
-// threads per query row (64 keys / O columns each).
+// warps 2-5 run the online softmax, the O corrections and the epilogue, one
+// thread per query row, with packed two-lane fp32 arithmetic.
 // S is double-buffered in tensor memory and P_j is written back over S_j,
 // where the P V MMA reads it as its A operand; Q K^T of the next tile and
 // P V of the previous one run while the softmax works.  The running max is
@@ -43,22 +43,18 @@ constexpr int kStages = 3;      // K ring and V ring depth
 constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
 constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
 constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
-constexpr int kThreads = 352;          // K-load warp, MMA warp, 8 softmax warps, V-load warp
-constexpr int kVWarp = 10;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = 224;          // K-load warp, MMA warp, 4 softmax warps, V-load warp
+constexpr int kVWarp = 6;
+constexpr int kSoftmaxThreads = 128;
 constexpr float kRebase = 8.0f;  // log2 units
 
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kOpBytes;
 constexpr int kOffV = kOffK + kStages * kOpBytes;
 constexpr int kOffBar = kOffV + kStages * kOpBytes;
-// q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_zero, s_full[2], p_full[2], o_done[2], drain,
-// pair_end[4 quarters]
-constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1 + 4;
+// q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_zero, s_full[2], p_full[2], o_done[2], drain
+constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-// float [2 halves][128 rows] of row sums at the end, over K stage 0 (free
-// by then: every MMA has completed)
-constexpr int kOffXl = kOffK;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -76,6 +72,44 @@ struct PrefillParams {
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// Two-lane fp32 arithmetic (one instruction, each lane rounded as the scalar
+// operation) and a three-input maximum.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]: the A operand (M = 128 lanes) read from
 // tensor memory, two 16-bit elements per 32-bit column (column c of lane r
@@ -122,7 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;   // [2], by tile parity
     uint64_t* o_done = p_full + 2;   // [2], by tile parity
     uint64_t* drain = o_done + 2;
-    uint64_t* pair_end = drain + 1;  // [4]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
@@ -161,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(o_done + i, 1);
         }
         mbar_init(drain, 1);
-        for (int i = 0; i < 4; ++i) mbar_init(pair_end + i, 64);
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -179,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kVWarp) {
         // --------------------------------------------- TMA producers (K, V)
-        // Warp 0 streams Q and the key tiles, warp 10 the value tiles, each
+        // Warp 0 streams Q and the key tiles, warp 6 the value tiles, each
         // through its own 3-stage ring, so a key load never waits for a P V
         // to free a value stage.
         const bool is_k = warp == 0;
@@ -324,23 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------- softmax, O, epilogue
-        // Two threads per query row: warps 2-5 take keys / O columns 0-63,
-        // warps 6-9 columns 64-127, of the row in their tensor-memory lane
-        // quarter.  Both read the whole row of S for its maximum, so they
-        // take the same rebasing decisions without talking; they add their
-        // sums through shared memory at the end.  P_j goes back into tensor
-        // memory over S_j; the softmax waits for a P V only when it has to
-        // rescale O.
-        const int wq = warp & 3;            // tensor-memory lane quarter
-        const int hf = (warp - 2) >> 2;     // column half
+        // One thread per query row (its tensor-memory lane).  P_j goes back
+        // into tensor memory over S_j; the softmax waits for a P V only when
+        // it has to rescale O.
+        const int wq = warp & 3;  // tensor-memory lane quarter
         const int row = wq * 32 + lane;
         const int tt = row / p.G, g = row - tt * p.G;
         const bool row_valid = t0 + tt < n;
         const int pos = ctx + t0 + min(tt, n - 1 - t0);  // padding rows reuse the last position
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-        const uint32_t col0 = static_cast<uint32_t>(hf * 64);
-        float* xl = reinterpret_cast<float*>(sm + kOffXl);  // [2 halves][128 rows], used at the end
         const float c = p.qk_scale;
+        const float2 c2 = make_float2(c, c);
         float m_ref = -INFINITY, l = 0.f;
         int next_even = 0, next_odd = 1;  // next P V (tile index) to wait for, per parity
         bool ok = true;
@@ -349,34 +375,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = warp_all(tc::wait_spin(s_full + sb, (j >> 1) & 1));
             if (!ok || !warp_all(*abort_flag == 0)) break;
             tc::fence_after();
-            // this half's 64 scores, and the other half's for the row maximum
-            // (all four loads in flight before the one wait)
-            uint32_t x[2][32], y[2][32];
-            tc::ld32(tmem + lane_base + sb * kTileN + col0, x[0]);
-            tc::ld32(tmem + lane_base + sb * kTileN + col0 + 32, x[1]);
-            tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64), y[0]);
-            tc::ld32(tmem + lane_base + sb * kTileN + (col0 ^ 64) + 32, y[1]);
+            uint32_t x[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tc::ld32(tmem + lane_base + sb * kTileN + q * 32, x[q]);
             tc::wait_ld();
 
-            // masked keys -inf; the row maximum over all 128 keys of the
-            // tile -- raw scores, as scale > 0 keeps the order
-            const int key0 = j * kTileN + hf * 64, okey0 = j * kTileN + (hf ^ 1) * 64;
-            if (key0 + 63 > pos) {
+            // masked keys -inf; row maximum of the raw scores (scale > 0
+            // keeps the order)
+            const int key0 = j * kTileN;
+            if (key0 + kTileN - 1 > pos) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2)
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (key0 + h2 * 32 + i > pos) x[h2][i] = __float_as_uint(-INFINITY);
+                        if (key0 + q * 32 + i > pos) x[q][i] = __float_as_uint(-INFINITY);
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float v = okey0 + h2 * 32 + i > pos ? -INFINITY : __uint_as_float(y[h2][i]);
-                    mx[i & 3] = fmaxf(mx[i & 3], fmaxf(__uint_as_float(x[h2][i]), v));
-                }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
+                for (int i = 0; i < 32; i += 2)
+                    mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(x[q][i]), __uint_as_float(x[q][i + 1]));
+            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY) * c;
             const float m_new = fmaxf(m_ref, mt);
             const bool rebase = m_new > m_ref + kRebase;
             float alpha = 1.f;
@@ -384,20 +404,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 alpha = ex2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
                 m_ref = m_new;
             }
-            const float nm = -m_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];
+            const float2 nm2 = make_float2(-m_ref, -m_ref);
+            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            uint32_t pk[64];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2)
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float e0 = ex2(fmaf(__uint_as_float(x[h2][2 * i]), c, nm));
-                    const float e1 = ex2(fmaf(__uint_as_float(x[h2][2 * i + 1]), c, nm));
-                    ls[i & 3] += e0 + e1;
-                    pk[h2 * 16 + i] = pack2<kBF>(e0, e1);
+                    float2 a = ffma2(make_float2(__uint_as_float(x[q][2 * i]), __uint_as_float(x[q][2 * i + 1])), c2, nm2);
+                    a.x = ex2(a.x);
+                    a.y = ex2(a.y);
+                    ls[i & 3] = fadd2(ls[i & 3], a);
+                    pk[q * 16 + i] = pack2<kBF>(a.x, a.y);
                 }
-            l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
-            tc::st32(tmem + lane_base + sb * kTileN + hf * 32, pk);
+            const float2 lt = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+            l = l * alpha + (lt.x + lt.y);
+            tc::st32(tmem + lane_base + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(pk));
+            tc::st32(tmem + lane_base + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
 
             // keep both o_done barriers within one phase of this thread
             if (j >= 2) ok = warp_all(sb ? consume_pv(o_done + 1, next_odd, j - 2) : consume_pv(o_done, next_even, j - 2));
@@ -406,14 +429,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = warp_all(sb ? consume_pv(o_done, next_even, j - 1) : consume_pv(o_done + 1, next_odd, j - 1));
                 if (ok) {
                     tc::fence_after();
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
+                    for (int q = 0; q < 4; ++q) {
                         uint32_t o[32];
-                        tc::ld32(tO + lane_base + col0 + h2 * 32, o);
+                        tc::ld32(tO + lane_base + q * 32, o);
                         tc::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tc::st32(tO + lane_base + col0 + h2 * 32, o);
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+                            o[2 * i] = __float_as_uint(v.x);
+                            o[2 * i + 1] = __float_as_uint(v.y);
+                        }
+                        tc::st32(tO + lane_base + q * 32, o);
                     }
                 }
             }
@@ -429,19 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (live && ok) {
             tc::fence_after();
-            // row sum of both halves
-            xl[hf * kTileM + row] = l;
-            tc::arrive(pair_end + wq);
-            ok = warp_all(tc::wait_spin(pair_end + wq, 0));
-        }
-        if (live && ok) {
-            const float inv = 1.f / (l + xl[(hf ^ 1) * kTileM + row]);
+            const float inv = 1.f / l;
             typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
-                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD + col0;
+                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            for (int q = 0; q < 4; ++q) {
                 uint32_t o[32];
-                tc::ld32(tO + lane_base + col0 + h2 * 32, o);
+                tc::ld32(tO + lane_base + q * 32, o);
                 tc::wait_ld();
                 if (row_valid) {
 #pragma unroll
@@ -451,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
                         w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
                         w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + h2 * 32 + v4 * 8) = w;
+                        *reinterpret_cast<uint4*>(orow + q * 32 + v4 * 8) = w;
                     }
                 }
             }
