@@ -444,6 +444,56 @@ pkv_status pkv_alloc_swap_out(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, i
                               int32_t* n);
 pkv_status pkv_alloc_swap_in(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, int32_t* pairs, int32_t cap,
                              int32_t* n);
+/*
+ * Automatic prefix caching ([P1] "基于级联哈希的缓存结构设计" and "缓存分配、
+ * 触碰与驱逐闭环").  A full block is identified by its cascaded hash
+ *   hash(parent hash, the block's token ids, extra hashes)
+ * (the parent of the first block is 0; extra hashes carry whatever else fixes
+ * the block's KV, e.g. a LoRA adapter id; a per-request cache salt joins the
+ * first block's extra hashes only, so different salts never share blocks).
+ * The hash is 64-bit FNV-1a over the little-endian bytes of: parent (8),
+ * token count (4), each token id (4), extra count (4), each extra (8).
+ *
+ * Allocator side: commit registers a sequence's full blocks under their
+ * hashes; lookup counts the leading hashes of a prompt found in the table
+ * (get_computed_blocks); seq_new_prefix touches those blocks (a reference
+ * each; a block no sequence held becomes live again) and allocates the rest.
+ * A committed block whose count drops to zero stays cached and evictable.
+ * Allocation uses never-cached free blocks first, then evicts the cached
+ * block released longest ago; a sequence's blocks are released last to
+ * first, so the leaf end of a chain is evicted before its root.
+ * num_free counts never-cached and evictable blocks.
+ */
+uint64_t pkv_block_hash(uint64_t parent_hash, const int32_t* tokens, int32_t num_tokens, const uint64_t* extras,
+                        int32_t num_extras);
+/* Hashes of the num_tokens / block_size full blocks of a token sequence
+ * (capacity cap), the same extras for every block and *salt (if salt is not
+ * NULL) added to the first block's. */
+pkv_status pkv_prefix_block_hashes(const int32_t* tokens, int64_t num_tokens, int32_t block_size,
+                                   const uint64_t* extras, int32_t num_extras, const uint64_t* salt,
+                                   uint64_t* hashes, int64_t cap, int64_t* num_hashes);
+/* Leading hashes[0..n) present in the table (no state change); -1 on a bad
+ * argument. */
+int32_t pkv_alloc_lookup(const pkv_alloc* a, const uint64_t* hashes, int32_t n);
+/* New sequence of num_tokens tokens whose first full blocks have the given
+ * hashes (num_hashes * block_size <= num_tokens): the leading hits
+ * (*hit_blocks) are shared, the other blocks allocated.  All or nothing;
+ * PKV_ERR_OOM if the pool cannot hold the rest. */
+pkv_status pkv_alloc_seq_new_prefix(pkv_alloc* a, int64_t seq_id, const uint64_t* hashes, int32_t num_hashes,
+                                    int32_t num_tokens, int32_t* hit_blocks);
+/* Registers the sequence's first num_hashes blocks (all full) under the
+ * given hashes once their KV is written; a block already committed keeps its
+ * hash (a different one is PKV_ERR_INVALID), a hash already held by another
+ * block is skipped.  *committed (may be NULL) = blocks newly registered. */
+pkv_status pkv_alloc_commit(pkv_alloc* a, int64_t seq_id, const uint64_t* hashes, int32_t num_hashes,
+                            int32_t* committed);
+/* Cached blocks that no sequence holds (evictable). */
+int32_t pkv_alloc_num_cached(const pkv_alloc* a);
+/* 1 and *hash if the block is committed, 0 if not, -1 on a bad argument. */
+int64_t pkv_alloc_block_hash_of(const pkv_alloc* a, int32_t block, uint64_t* hash);
+/* Forgets every hash; evictable blocks become plain free blocks. */
+void pkv_alloc_reset_prefix_cache(pkv_alloc* a);
+
 /* Fault injection for tests: the k-th block allocation from now (k >= 1)
  * fails as if the pool were empty; k <= 0 disables. */
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k);

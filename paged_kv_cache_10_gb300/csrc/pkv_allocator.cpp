@@ -13,11 +13,25 @@
 // Copy-on-Write": shared blocks have reference count > 1 and are copied only
 // when modified.
 //
+// Automatic prefix caching ("vLLM 高性能大语言模型推理引擎深度技术评估与分布式
+// 架构展望", sections "基于级联哈希的缓存结构设计" and "缓存分配、触碰与驱逐闭环"):
+// a full block may be committed under its cascaded hash (parent hash, the
+// block's tokens, extra hashes; the cache salt enters the first block's
+// hash).  Lookup finds the longest run of leading blocks of a new prompt
+// that are already in the table; touch takes a reference on them (reviving
+// blocks no sequence holds any more); blocks whose count drops to zero keep
+// their hash and stay cached but evictable; allocation uses never-cached
+// free blocks first and then evicts the least recently released cached
+// block.  A sequence releases its blocks last to first, so of the blocks
+// freed together the leaf end of the chain goes first and the shared root
+// (a system prompt, say) stays longest.
+//
 // Every public call is all-or-nothing: failures leave the state unchanged
 // (OOM returns a status instead of throwing).
 #include <cstdint>
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -36,11 +50,20 @@ struct Seq {
 struct pkv_alloc {
     int32_t num_blocks = 0;
     int32_t block_size = 0;
-    std::vector<int32_t> free_stack;  // allocation pops the back
+    std::vector<int32_t> free_stack;  // never-cached free blocks; allocation pops the back
     std::vector<int32_t> ref;
     std::unordered_map<int64_t, Seq> seqs;
     int64_t fail_countdown = 0;  // >0: the fail_countdown-th allocation fails
+    // prefix cache
+    std::vector<uint64_t> bhash;           // hash of a committed block
+    std::vector<uint8_t> hashed;           // 1: committed (in `table`)
+    std::vector<int64_t> stamp;            // release stamp of an evictable block; -1 otherwise
+    std::vector<int64_t> took_stamp;       // stamp of the cached block a take() evicted; -1 otherwise
+    std::unordered_map<uint64_t, int32_t> table;  // hash -> block
+    std::map<int64_t, int32_t> evictable;  // release stamp -> cached block with count 0
+    int64_t clock = 0;
 
+    int64_t available() const { return static_cast<int64_t>(free_stack.size() + evictable.size()); }
     bool can_take() {
         if (fail_countdown > 0) {
             if (fail_countdown == 1) {
@@ -48,23 +71,59 @@ struct pkv_alloc {
                 return false;
             }
         }
-        return !free_stack.empty();
+        return available() > 0;
     }
-    // Only call after can_take() returned true.
+    // Only call after can_take() returned true.  Never-cached blocks first;
+    // else the least recently released cached block is evicted.
     int32_t take() {
         if (fail_countdown > 0) --fail_countdown;
-        int32_t id = free_stack.back();
-        free_stack.pop_back();
+        int32_t id;
+        if (!free_stack.empty()) {
+            id = free_stack.back();
+            free_stack.pop_back();
+            took_stamp[id] = -1;
+        } else {
+            auto it = evictable.begin();
+            id = it->second;
+            took_stamp[id] = it->first;
+            evictable.erase(it);
+            stamp[id] = -1;
+            table.erase(bhash[id]);
+            hashed[id] = 0;
+        }
         ref[id] = 1;
         return id;
     }
-    // Exact inverse of take() for rollback.
+    // Exact inverse of take() for rollback (takes are undone last first).
     void untake(int32_t id) {
         ref[id] = 0;
-        free_stack.push_back(id);
+        if (took_stamp[id] < 0) {
+            free_stack.push_back(id);
+        } else {
+            hashed[id] = 1;
+            table[bhash[id]] = id;
+            stamp[id] = took_stamp[id];
+            evictable.emplace(took_stamp[id], id);
+            took_stamp[id] = -1;
+        }
     }
     void release(int32_t id) {
-        if (--ref[id] == 0) free_stack.push_back(id);
+        if (--ref[id] == 0) {
+            if (hashed[id]) {
+                stamp[id] = clock++;
+                evictable.emplace(stamp[id], id);
+            } else {
+                free_stack.push_back(id);
+            }
+        }
+    }
+    // Reference on a block found by lookup; revives it if it was evictable.
+    void touch(int32_t id) {
+        if (ref[id] == 0) {
+            evictable.erase(stamp[id]);
+            stamp[id] = -1;
+        }
+        ref[id] += 1;
     }
 };
 
@@ -133,6 +192,10 @@ pkv_alloc* pkv_alloc_create(int32_t num_blocks, int32_t block_size, const int32_
     a->num_blocks = num_blocks;
     a->block_size = block_size;
     a->ref.assign(num_blocks, 0);
+    a->bhash.assign(num_blocks, 0);
+    a->hashed.assign(num_blocks, 0);
+    a->stamp.assign(num_blocks, -1);
+    a->took_stamp.assign(num_blocks, -1);
     a->free_stack.resize(num_blocks);
     if (free_order) {
         std::vector<char> seen(num_blocks, 0);
@@ -157,7 +220,7 @@ pkv_status pkv_alloc_seq_new(pkv_alloc* a, int64_t seq_id, int32_t num_tokens) {
     if (!a || num_tokens < 0) return PKV_ERR_INVALID;
     if (a->seqs.count(seq_id)) return PKV_ERR_INVALID;
     const int64_t need = (static_cast<int64_t>(num_tokens) + a->block_size - 1) / a->block_size;
-    if (need > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+    if (need > a->available()) return PKV_ERR_OOM;
     Seq s;
     s.blocks.reserve(need);
     for (int64_t i = 0; i < need; ++i) {
@@ -198,7 +261,7 @@ pkv_status pkv_alloc_seq_extend(pkv_alloc* a, int64_t seq_id, int32_t num_tokens
     if (s.len % a->block_size != 0 && a->ref[s.blocks.back()] > 1) return PKV_ERR_INVALID;
     const int64_t have = static_cast<int64_t>(s.blocks.size());
     const int64_t need = (s.len + num_tokens + a->block_size - 1) / a->block_size - have;
-    if (need > static_cast<int64_t>(a->free_stack.size())) return PKV_ERR_OOM;
+    if (need > a->available()) return PKV_ERR_OOM;
     for (int64_t i = 0; i < need; ++i) {
         if (!a->can_take()) {
             while (static_cast<int64_t>(s.blocks.size()) > have) {
@@ -347,7 +410,7 @@ int32_t pkv_alloc_refcount(const pkv_alloc* a, int32_t block) {
 }
 
 int32_t pkv_alloc_num_free(const pkv_alloc* a) {
-    return a ? static_cast<int32_t>(a->free_stack.size()) : -1;
+    return a ? static_cast<int32_t>(a->available()) : -1;
 }
 
 int32_t pkv_alloc_num_seqs(const pkv_alloc* a) {
@@ -427,7 +490,7 @@ pkv_status move_seq(pkv_alloc* from, pkv_alloc* to, int64_t seq_id, int32_t* pai
     if (nb > cap || (nb > 0 && !pairs)) return PKV_ERR_INVALID;
     for (int32_t b : s.blocks)
         if (from->ref[b] != 1) return PKV_ERR_INVALID;  // shared blocks cannot move
-    if (nb > static_cast<int32_t>(to->free_stack.size())) return PKV_ERR_OOM;
+    if (nb > to->available()) return PKV_ERR_OOM;
     Seq moved;
     moved.len = s.len;
     for (int32_t i = 0; i < nb; ++i) {
@@ -461,6 +524,140 @@ pkv_status pkv_alloc_swap_in(pkv_alloc* dev, pkv_alloc* host, int64_t seq_id, in
 
 void pkv_alloc_fail_after(pkv_alloc* a, int64_t k) {
     if (a) a->fail_countdown = k > 0 ? k : 0;
+}
+
+// ------------------------------------------------------------ prefix cache
+// FNV-1a, 64-bit (offset basis 14695981039346656037, prime 1099511628211),
+// over little-endian bytes.
+namespace {
+struct Fnv {
+    uint64_t h = 14695981039346656037ull;
+    void byte(uint8_t b) {
+        h ^= b;
+        h *= 1099511628211ull;
+    }
+    void u32(uint32_t v) {
+        for (int i = 0; i < 4; ++i) byte(static_cast<uint8_t>(v >> (8 * i)));
+    }
+    void u64(uint64_t v) {
+        for (int i = 0; i < 8; ++i) byte(static_cast<uint8_t>(v >> (8 * i)));
+    }
+};
+}  // namespace
+
+uint64_t pkv_block_hash(uint64_t parent_hash, const int32_t* tokens, int32_t num_tokens, const uint64_t* extras,
+                        int32_t num_extras) {
+    Fnv f;
+    f.u64(parent_hash);
+    const int32_t nt = tokens && num_tokens > 0 ? num_tokens : 0;
+    const int32_t ne = extras && num_extras > 0 ? num_extras : 0;
+    f.u32(static_cast<uint32_t>(nt));
+    for (int32_t i = 0; i < nt; ++i) f.u32(static_cast<uint32_t>(tokens[i]));
+    f.u32(static_cast<uint32_t>(ne));
+    for (int32_t i = 0; i < ne; ++i) f.u64(extras[i]);
+    return f.h;
+}
+
+pkv_status pkv_prefix_block_hashes(const int32_t* tokens, int64_t num_tokens, int32_t block_size,
+                                   const uint64_t* extras, int32_t num_extras, const uint64_t* salt,
+                                   uint64_t* hashes, int64_t cap, int64_t* num_hashes) {
+    if (num_tokens < 0 || block_size <= 0 || num_extras < 0 || (num_extras > 0 && !extras) || !num_hashes)
+        return PKV_ERR_INVALID;
+    const int64_t nb = num_tokens / block_size;
+    if (nb > 0 && (!tokens || !hashes || cap < nb)) return PKV_ERR_INVALID;
+    std::vector<uint64_t> ex(extras, extras + num_extras);
+    uint64_t parent = 0;
+    for (int64_t i = 0; i < nb; ++i) {
+        if (i == 0 && salt) ex.push_back(*salt);
+        hashes[i] = pkv_block_hash(parent, tokens + i * block_size, block_size, ex.data(),
+                                   static_cast<int32_t>(ex.size()));
+        if (i == 0 && salt) ex.pop_back();
+        parent = hashes[i];
+    }
+    *num_hashes = nb;
+    return PKV_OK;
+}
+
+int32_t pkv_alloc_lookup(const pkv_alloc* a, const uint64_t* hashes, int32_t n) {
+    if (!a || n < 0 || (n > 0 && !hashes)) return -1;
+    int32_t k = 0;
+    while (k < n && a->table.count(hashes[k])) ++k;
+    return k;
+}
+
+pkv_status pkv_alloc_seq_new_prefix(pkv_alloc* a, int64_t seq_id, const uint64_t* hashes, int32_t num_hashes,
+                                    int32_t num_tokens, int32_t* hit_blocks) {
+    if (!a || num_tokens < 0 || num_hashes < 0 || (num_hashes > 0 && !hashes) || !hit_blocks)
+        return PKV_ERR_INVALID;
+    if (a->seqs.count(seq_id)) return PKV_ERR_INVALID;
+    if (static_cast<int64_t>(num_hashes) * a->block_size > num_tokens) return PKV_ERR_INVALID;  // full blocks only
+    const int32_t k = pkv_alloc_lookup(a, hashes, num_hashes);
+    const int64_t total = (static_cast<int64_t>(num_tokens) + a->block_size - 1) / a->block_size;
+    const int64_t need = total - k;
+    int64_t revived = 0;  // hits that leave the evictable set
+    for (int32_t i = 0; i < k; ++i)
+        if (a->ref[a->table.at(hashes[i])] == 0) ++revived;
+    if (need > a->available() - revived) return PKV_ERR_OOM;
+    if (a->fail_countdown > 0 && a->fail_countdown <= need) {  // the injected failure falls in this call
+        a->fail_countdown = 0;
+        return PKV_ERR_OOM;
+    }
+    Seq s;
+    s.blocks.reserve(total);
+    for (int32_t i = 0; i < k; ++i) {
+        const int32_t id = a->table.at(hashes[i]);
+        a->touch(id);
+        s.blocks.push_back(id);
+    }
+    for (int64_t i = 0; i < need; ++i) s.blocks.push_back(a->take());
+    s.len = num_tokens;
+    a->seqs.emplace(seq_id, std::move(s));
+    *hit_blocks = k;
+    return PKV_OK;
+}
+
+pkv_status pkv_alloc_commit(pkv_alloc* a, int64_t seq_id, const uint64_t* hashes, int32_t num_hashes,
+                            int32_t* committed) {
+    if (!a || num_hashes < 0 || (num_hashes > 0 && !hashes)) return PKV_ERR_INVALID;
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PKV_ERR_NOT_FOUND;
+    const Seq& s = it->second;
+    if (static_cast<int64_t>(num_hashes) * a->block_size > s.len) return PKV_ERR_INVALID;  // full blocks only
+    for (int32_t i = 0; i < num_hashes; ++i) {
+        const int32_t id = s.blocks[i];
+        if (a->hashed[id] && a->bhash[id] != hashes[i]) return PKV_ERR_INVALID;
+    }
+    int32_t c = 0;
+    for (int32_t i = 0; i < num_hashes; ++i) {
+        const int32_t id = s.blocks[i];
+        if (a->hashed[id] || a->table.count(hashes[i])) continue;  // committed, or content held elsewhere
+        a->hashed[id] = 1;
+        a->bhash[id] = hashes[i];
+        a->table.emplace(hashes[i], id);
+        ++c;
+    }
+    if (committed) *committed = c;
+    return PKV_OK;
+}
+
+int32_t pkv_alloc_num_cached(const pkv_alloc* a) { return a ? static_cast<int32_t>(a->evictable.size()) : -1; }
+
+int64_t pkv_alloc_block_hash_of(const pkv_alloc* a, int32_t block, uint64_t* hash) {
+    if (!a || block < 0 || block >= a->num_blocks || !hash) return -1;
+    if (!a->hashed[block]) return 0;
+    *hash = a->bhash[block];
+    return 1;
+}
+
+void pkv_alloc_reset_prefix_cache(pkv_alloc* a) {
+    if (!a) return;
+    for (const auto& e : a->evictable) {
+        a->stamp[e.second] = -1;
+        a->free_stack.push_back(e.second);
+    }
+    a->evictable.clear();
+    a->table.clear();
+    std::fill(a->hashed.begin(), a->hashed.end(), 0);
 }
 
 }  // extern "C"

@@ -33,7 +33,9 @@ EXPORTED = [
     "pkv_alloc_seq_len", "pkv_alloc_refcount", "pkv_alloc_num_free", "pkv_alloc_num_seqs",
     "pkv_alloc_fail_after", "pkv_paged_attention_decode_cascade", "pkv_decode_cascade_workspace_bytes",
     "pkv_alloc_prefix_groups", "pkv_swap_blocks", "pkv_alloc_swap_out", "pkv_alloc_swap_in",
-    "pkv_paged_attention_prefill", "pkv_alloc_append_tokens",
+    "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
+    "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
+    "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache",
 ]
 
 
@@ -118,6 +120,14 @@ def lib():
         "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_append_tokens": (i32, [P, P, P, i32, P, i64, P, i32, P]),
+        "pkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, P, i32, P, i32]),
+        "pkv_prefix_block_hashes": (i32, [P, i64, i32, P, i32, P, P, i64, P]),
+        "pkv_alloc_lookup": (i32, [P, P, i32]),
+        "pkv_alloc_seq_new_prefix": (i32, [P, i64, P, i32, i32, P]),
+        "pkv_alloc_commit": (i32, [P, i64, P, i32, P]),
+        "pkv_alloc_num_cached": (i32, [P]),
+        "pkv_alloc_block_hash_of": (i64, [P, i32, P]),
+        "pkv_alloc_reset_prefix_cache": (None, [P]),
         "pkv_paged_attention_prefill": (i32, [P, i32, i32, i32, i32, P, i32, P, P, D, P, i32, P, ctypes.c_float,
                                               P, P]),
     }
@@ -326,6 +336,28 @@ def paged_attention_prefill(q, k_cache, v_cache, desc: CacheDesc, query_start, m
     _check(st, "paged_attention_prefill")
 
 
+def block_hash(parent: int, tokens, extras=()) -> int:
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    e = np.ascontiguousarray(extras, dtype=np.uint64)
+    return int(lib().pkv_block_hash(int(parent), _np_ptr(t) if t.size else None, int(t.size),
+                                    _np_ptr(e) if e.size else None, int(e.size)))
+
+
+def prefix_block_hashes(tokens, block_size: int = 16, extras=(), salt: int | None = None) -> np.ndarray:
+    """Cascaded hashes of the full blocks of a token sequence (uint64)."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    e = np.ascontiguousarray(extras, dtype=np.uint64)
+    nb = t.size // block_size
+    out = np.empty(max(nb, 1), np.uint64)
+    n = ctypes.c_int64(0)
+    sv = ctypes.c_uint64(int(salt)) if salt is not None else None
+    _check(lib().pkv_prefix_block_hashes(_np_ptr(t) if t.size else None, int(t.size), int(block_size),
+                                         _np_ptr(e) if e.size else None, int(e.size),
+                                         ctypes.byref(sv) if sv is not None else None, _np_ptr(out), nb,
+                                         ctypes.byref(n)), "prefix_block_hashes")
+    return out[: n.value].copy()
+
+
 SWAP_OUT, SWAP_IN = 0, 1
 
 
@@ -424,6 +456,42 @@ class Allocator:
         _check(lib().pkv_alloc_append_tokens(self._h, _np_ptr(ids), _np_ptr(cnt), n, _np_ptr(slots), total,
                                              _np_ptr(pairs), max(n, 1), ctypes.byref(npairs)), "alloc_append_tokens")
         return slots[:total].copy(), pairs[: npairs.value].copy()
+
+    # -- automatic prefix caching
+    def lookup(self, hashes) -> int:
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        k = lib().pkv_alloc_lookup(self._h, _np_ptr(h), int(h.shape[0]))
+        if k < 0:
+            raise PagedKVError(ERR_INVALID, "alloc_lookup")
+        return int(k)
+
+    def seq_new_prefix(self, seq: int, hashes, num_tokens: int) -> int:
+        """New sequence sharing its cached leading blocks; returns their count."""
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        hits = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_seq_new_prefix(self._h, int(seq), _np_ptr(h), int(h.shape[0]), int(num_tokens),
+                                              ctypes.byref(hits)), "alloc_seq_new_prefix")
+        return int(hits.value)
+
+    def commit(self, seq: int, hashes) -> int:
+        h = np.ascontiguousarray(hashes, dtype=np.uint64)
+        c = ctypes.c_int32(0)
+        _check(lib().pkv_alloc_commit(self._h, int(seq), _np_ptr(h), int(h.shape[0]), ctypes.byref(c)),
+               "alloc_commit")
+        return int(c.value)
+
+    def num_cached(self) -> int:
+        return int(lib().pkv_alloc_num_cached(self._h))
+
+    def block_hash_of(self, block: int):
+        out = ctypes.c_uint64(0)
+        r = lib().pkv_alloc_block_hash_of(self._h, int(block), ctypes.byref(out))
+        if r < 0:
+            raise PagedKVError(ERR_INVALID, "alloc_block_hash_of")
+        return int(out.value) if r else None
+
+    def reset_prefix_cache(self) -> None:
+        lib().pkv_alloc_reset_prefix_cache(self._h)
 
     def export(self, seq_ids, max_blocks: int):
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
