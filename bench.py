@@ -610,6 +610,52 @@ def run_prefill(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------------------ prefix-cache timing
+def run_apc(args):
+    """Host-side automatic prefix caching on a request stream: 16 system
+    prompts of 2048 tokens, each request one of them plus U[64, 1024] own
+    tokens; per request: block hashes, lookup + touch + allocation,
+    commit of its full blocks, release.  Times the library's C++ allocator
+    and reports the share of full blocks served from the cache."""
+    from paged_kv_cache_10_gb300 import pagedkv as pk
+    rng = np.random.default_rng(2024)
+    systems = [rng.integers(0, 128000, size=2048).astype(np.int32) for _ in range(16)]
+    reqs = []
+    for _ in range(max(args.steps, 1) * 20):
+        own = rng.integers(0, 128000, size=int(rng.integers(64, 1024, endpoint=True))).astype(np.int32)
+        reqs.append(np.concatenate([systems[int(rng.integers(0, 16))], own]))
+    NB = 40000
+    a = pk.Allocator(NB, 16)
+    live = []
+    hits = blocks = 0
+
+    def one(i, t):
+        nonlocal hits, blocks
+        h = pk.prefix_block_hashes(t)
+        hits += a.seq_new_prefix(i, h, len(t))
+        blocks += len(h)
+        a.commit(i, h)
+        live.append(i)
+        if len(live) > 64:  # 64 requests in flight; the oldest finishes
+            a.free(live.pop(0))
+
+    for i, t in enumerate(reqs[:50]):
+        one(i, t)
+    hits = blocks = 0
+    t0 = time.perf_counter()
+    for i, t in enumerate(reqs[50:], start=50):
+        one(i, t)
+    dt = time.perf_counter() - t0
+    n = len(reqs) - 50
+    toks = sum(len(t) for t in reqs[50:])
+    return {"metric": "automatic prefix caching, host allocator (hash + lookup + touch + allocate + commit + free)",
+            "value": round(n / dt, 1), "unit": "requests/s", "us_per_request": round(1e6 * dt / n, 2),
+            "blocks_per_s": round(blocks / dt, 1), "tokens_per_s": round(toks / dt, 1),
+            "cached_block_fraction": round(hits / max(blocks, 1), 4), "requests": n, "cores": 1,
+            "config": {"system_prompts": 16, "system_tokens": 2048, "own_tokens": "U[64,1024]",
+                       "in_flight": 64, "num_blocks": NB}}
+
+
 # ------------------------------------------------------------ swap timing
 def run_swap(args, local_rank):
     """Times pkv_swap_blocks on the workload's pool: all blocks of the first
@@ -703,6 +749,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--partition", type=int, default=None, help="tokens per split-K partition (0 = auto)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--apc", action="store_true",
+                    help="time host-side automatic prefix caching on a request stream (no GPU work)")
     ap.add_argument("--swap", action="store_true",
                     help="time block swap to / from a pinned host pool instead of the decode step")
     ap.add_argument("--graph", action="store_true",
@@ -717,7 +765,9 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.swap:
+    if args.apc:
+        line = run_apc(args) if rank == 0 else None
+    elif args.swap:
         line = run_swap(args, local_rank) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, rank, world)
