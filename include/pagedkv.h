@@ -254,6 +254,7 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
  *   max_group_members, max_group_blocks: host bounds of the two (size the
  *     launch).
  * workspace must hold pkv_decode_cascade_workspace_bytes(...) bytes.
+ * scale must be finite and > 0 (else PKV_ERR_INVALID).
  * Implemented for f16 / bf16 pools (q of the same type), head_size 128,
  * num_q_heads / num_kv_heads in {1, 2, 4, 8}; fp8 pools return
  * PKV_ERR_UNSUPPORTED.  A member index or block count out of range sets

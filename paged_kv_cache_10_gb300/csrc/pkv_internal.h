@@ -83,6 +83,22 @@ cudaError_t launch_decode_mma_fp8_bf16q(const DecodeParams& p, int G, const CUte
 cudaError_t launch_decode_mma_fp8_f16q(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                                        cudaStream_t st);
 
+// Shared-prefix (cascade) decode: the prefix pass over each group's shared
+// leading blocks, kPrefixPartitionBlocks blocks per prefix partition.
+constexpr int kPrefixPartitionBlocks = 32;  // 512 tokens
+int prefix_partitions(int blocks);
+struct CascadeParams {
+    DecodeParams base;
+    const int32_t* group_offsets;  // [num_groups + 1] into group_members
+    const int32_t* group_members;  // batch rows, group by group
+    int32_t G;
+    int32_t row_chunks;  // CTAs per (group, KV head, prefix partition) along rows (128 rows each)
+    int32_t npp;         // prefix partitions (partition indices [0, npp))
+};
+// tq: q as [S][Hq][128] with a box of 64 x G x 1 (encode_token_head_map).
+cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int kv_dtype, const CUtensorMap& tq,
+                                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+
 // Log-sum-exp merge of split-K partials into out (q dtype).
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);
 

@@ -69,6 +69,14 @@ struct PrefillParams {
     int32_t max_query_len;       // the caller's bound on every chunk
     float qk_scale;              // scale * log2(e)
     unsigned int* err;
+    // cascade prefix pass only
+    const int32_t* group_offsets;  // [groups + 1]
+    const int32_t* group_members;  // batch rows
+    const int32_t* group_blocks;   // shared leading blocks per group
+    float* part_m;                 // partials [S][Hq][NP] (log2 units), [S][Hq][NP], [S][Hq][NP][D]
+    float* part_l;
+    float* part_o;
+    int32_t NP, row_chunks;
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -139,7 +147,12 @@ __device__ __forceinline__ bool consume_pv(uint64_t* bar, int& next, int upto) {
     return ok;
 }
 
-template <typename T>
+// kPrefix = false: causal prefill, 128 rows = 128 / G tokens x G heads of one
+// (sequence, KV head), keys 0 .. each row's position, normalised output.
+// kPrefix = true: the cascade decode's shared-prefix pass, 128 rows = 128 / G
+// members x G heads of one (group, KV head), keys = one 512-token partition
+// of the group's shared blocks (no causal mask), split-K partials out.
+template <typename T, bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
@@ -160,24 +173,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int s = blockIdx.z, h = blockIdx.y;
-    const int qt = p.num_qtiles - 1 - static_cast<int>(blockIdx.x);  // longest key ranges first
-
-    // ---- this CTA's rows and keys (uniform across the CTA)
-    const int q0 = __ldg(p.query_start + s), q1 = __ldg(p.query_start + s + 1);
-    const int n = q1 - q0;
-    const int L = __ldg(p.seq_lens + s);
-    if (q0 < 0 || n < 0 || q1 > p.T || L < n || L > p.MB * kBlockSize) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-        return;
+    const int h = blockIdx.y;
+    const int G = p.G;
+    // ---- this CTA's rows and keys (uniform across the CTA).  Keys are
+    // counted from the CTA's first block `bt` points at; a row attends to
+    // keys 0 .. its limit (prefill: its position; prefix pass: all).
+    const int32_t* bt;
+    int nblk, kv_end;
+    // prefill
+    int q0 = 0, n = 0, ctx = 0, t0 = 0;
+    // prefix pass
+    int m0 = 0, members = 0, mrow0 = 0, seq0 = 0, pp = 0;
+    if constexpr (!kPrefix) {
+        const int s = blockIdx.z;
+        const int qt = p.num_qtiles - 1 - static_cast<int>(blockIdx.x);  // longest key ranges first
+        q0 = __ldg(p.query_start + s);
+        const int q1 = __ldg(p.query_start + s + 1);
+        n = q1 - q0;
+        const int L = __ldg(p.seq_lens + s);
+        if (q0 < 0 || n < 0 || q1 > p.T || L < n || L > p.MB * kBlockSize) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+            return;
+        }
+        if (n > p.max_query_len && threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+        t0 = qt * p.TT;
+        if (t0 >= n) return;
+        ctx = L - n;                                  // tokens before this chunk
+        kv_end = ctx + t0 + min(p.TT, n - t0);        // keys [0, kv_end)
+        nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+        bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
+    } else {
+        pp = blockIdx.x;
+        const int grp = blockIdx.z / p.row_chunks, chunk = blockIdx.z % p.row_chunks;
+        m0 = __ldg(p.group_offsets + grp);
+        members = __ldg(p.group_offsets + grp + 1) - m0;
+        mrow0 = chunk * (kTileM / G);  // first member of this CTA
+        if (mrow0 >= members) return;
+        int nb = __ldg(p.group_blocks + grp);
+        if (nb < 0 || nb > p.MB) {
+            if (threadIdx.x == 0 && pp == 0 && h == 0 && chunk == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+            nb = nb < 0 ? 0 : p.MB;
+        }
+        seq0 = __ldg(p.group_members + m0);
+        const bool bad = seq0 < 0 || seq0 >= p.S;
+        if (bad && threadIdx.x == 0 && pp == 0 && h == 0 && chunk == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+        const int b0 = pp * kPrefixPartitionBlocks;
+        if (b0 >= nb || bad) {
+            // this partition lies past the group's prefix (another group's
+            // prefix is longer): empty partials, so the merge reads no stale
+            // workspace
+            for (int r = threadIdx.x; r < kTileM; r += kThreads) {
+                const int mi = mrow0 + r / G;
+                if (mi >= members) continue;
+                const int b = __ldg(p.group_members + m0 + mi);
+                if (b < 0 || b >= p.S) continue;
+                const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + r % G) * p.NP + pp;
+                p.part_m[prow] = -INFINITY;
+                p.part_l[prow] = 0.f;
+                float4* po = reinterpret_cast<float4*>(p.part_o + prow * kPD);
+                for (int d4 = 0; d4 < kPD / 4; ++d4) po[d4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            return;
+        }
+        nblk = min(nb, b0 + kPrefixPartitionBlocks) - b0;
+        kv_end = nblk * kBlockSize;
+        bt = p.block_tables + static_cast<int64_t>(seq0) * p.MB + b0;
     }
-    if (n > p.max_query_len && threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-    const int t0 = qt * p.TT;
-    if (t0 >= n) return;
-    const int ctx = L - n;                                // tokens before this chunk
-    const int kv_end = ctx + t0 + min(p.TT, n - t0);      // keys [0, kv_end)
     const int nkt = (kv_end + kTileN - 1) / kTileN;
-    const int nblk = (kv_end + kBlockSize - 1) / kBlockSize;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -220,15 +282,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* empty = is_k ? k_empty : v_empty;
         const CUtensorMap* map = is_k ? &tmk : &tmv;
         unsigned char* ring = sm + (is_k ? kOffK : kOffV);
-        if (is_k && lane == 0) {
-            mbar_arrive_expect_tx(q_full, kOpBytes);
-            for (int dh = 0; dh < 2; ++dh)
-                tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * p.G, q0 + t0, q_full,
-                                policy_evict_first());
+        if (is_k) {
+            const uint64_t pol_q = policy_evict_first();
+            if constexpr (!kPrefix) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(q_full, kOpBytes);
+                    for (int dh = 0; dh < 2; ++dh)
+                        tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * G, q0 + t0, q_full, pol_q);
+                }
+            } else {
+                // G query rows of each member (its batch row in q); rows of
+                // members past the group's end repeat the first member
+                if (lane == 0) mbar_arrive_expect_tx(q_full, kOpBytes);
+                __syncwarp();
+                for (int mi = lane; mi < kTileM / G; mi += 32) {
+                    int b = seq0;
+                    if (mrow0 + mi < members) {
+                        b = __ldg(p.group_members + m0 + mrow0 + mi);
+                        if (b < 0 || b >= p.S) {
+                            report(p.err, PKV_DEVERR_SEQ_LEN);
+                            b = seq0;
+                        }
+                    }
+                    for (int dh = 0; dh < 2; ++dh)
+                        tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes + mi * G * 128, &tmq, dh * 64, h * G, b, q_full,
+                                        pol_q);
+                }
+            }
         }
         // block ids 32 at a time (4 tiles), loaded 4 tiles before their use:
         // lane l holds the id of block 32 * batch + l
-        const int32_t* bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
         auto load_ids = [&](int batch) {
             const int idx = batch * 32 + lane;
             return idx < nblk ? __ldg(bt + idx) : 0;
@@ -361,9 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // it has to rescale O.
         const int wq = warp & 3;  // tensor-memory lane quarter
         const int row = wq * 32 + lane;
-        const int tt = row / p.G, g = row - tt * p.G;
-        const bool row_valid = t0 + tt < n;
-        const int pos = ctx + t0 + min(tt, n - 1 - t0);  // padding rows reuse the last position
+        const int rq = row / G, g = row - rq * G;  // token (prefill) or member (prefix) in the tile, head
+        bool row_valid;
+        int pos;  // last key this row attends to
+        if constexpr (!kPrefix) {
+            row_valid = t0 + rq < n;
+            pos = ctx + t0 + min(rq, n - 1 - t0);  // padding rows reuse the last position
+        } else {
+            row_valid = mrow0 + rq < members;
+            pos = kv_end - 1;
+        }
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const float c = p.qk_scale;
         const float2 c2 = make_float2(c, c);
@@ -458,22 +548,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (live && ok) {
             tc::fence_after();
             const float inv = 1.f / l;
-            typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
-                                        (static_cast<int64_t>(q0 + t0 + tt) * p.Hq + h * p.G + g) * kPD;
+            if constexpr (!kPrefix) {
+                typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
+                                            (static_cast<int64_t>(q0 + t0 + rq) * p.Hq + h * G + g) * kPD;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t o[32];
-                tc::ld32(tO + lane_base + q * 32, o);
-                tc::wait_ld();
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[32];
+                    tc::ld32(tO + lane_base + q * 32, o);
+                    tc::wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 w;
+                            w.x = pack2<kBF>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                            w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                            w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                            w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + q * 32 + v4 * 8) = w;
+                        }
+                    }
+                }
+            } else {
+                // partial of this prefix partition: reference maximum (log2
+                // units), the sum relative to it, and O / l
+                int b = -1;
                 if (row_valid) {
+                    b = __ldg(p.group_members + m0 + mrow0 + rq);
+                    if (b < 0 || b >= p.S) b = -1;
+                }
+                const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + g) * p.NP + pp;
+                if (b >= 0) {
+                    p.part_m[prow] = m_ref;
+                    p.part_l[prow] = l;
+                }
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack2<kBF>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                        w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                        w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                        w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + q * 32 + v4 * 8) = w;
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[32];
+                    tc::ld32(tO + lane_base + q * 32, o);
+                    tc::wait_ld();
+                    if (b >= 0) {
+                        float4* po = reinterpret_cast<float4*>(p.part_o + prow * kPD + q * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 8; ++v4)
+                            po[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                                 __uint_as_float(o[4 * v4 + 2]) * inv,
+                                                 __uint_as_float(o[4 * v4 + 3]) * inv);
                     }
                 }
             }
@@ -492,9 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <typename T>
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           cudaStream_t st) {
+template <typename T, bool kPrefix>
+cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, cudaStream_t st) {
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -502,17 +621,53 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const 
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaError_t attr = cudaSuccess;
     std::call_once(once[dev], [&] {
-        attr = cudaFuncSetAttribute(prefill_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr = cudaFuncSetAttribute(prefill_tc_kernel<T, kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
-    const dim3 grid(p.num_qtiles, p.Hkv, p.S);
-    prefill_tc_kernel<T><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
+    prefill_tc_kernel<T, kPrefix><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           cudaStream_t st) {
+    return launch_tile<T, false>(p, dim3(p.num_qtiles, p.Hkv, p.S), tq, tk, tv, st);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 }  // namespace
+
+int prefix_partitions(int blocks) { return (blocks + kPrefixPartitionBlocks - 1) / kPrefixPartitionBlocks; }
+
+cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int kv_dtype, const CUtensorMap& tq,
+                                     const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+    const DecodeParams& b = cp.base;
+    PrefillParams p{};
+    p.block_tables = b.block_tables;
+    p.S = b.S;
+    p.Hq = b.Hq;
+    p.Hkv = b.Hkv;
+    p.MB = b.MB;
+    p.NB = b.NB;
+    p.G = cp.G;
+    p.TT = kTileM / cp.G;
+    p.qk_scale = b.qk_scale;
+    p.err = b.err;
+    p.group_offsets = cp.group_offsets;
+    p.group_members = cp.group_members;
+    p.group_blocks = b.group_blocks;
+    p.part_m = b.part_m;
+    p.part_l = b.part_l;
+    p.part_o = b.part_o;
+    p.NP = b.NP;
+    p.row_chunks = cp.row_chunks;
+    const dim3 grid(cp.npp, b.Hkv, num_groups * cp.row_chunks);
+    return kv_dtype == PKV_BF16 ? launch_tile<BF16, true>(p, grid, tq, tk, tv, st)
+                                : launch_tile<F16, true>(p, grid, tq, tk, tv, st);
+}
+
 }  // namespace pkv
 
 using namespace pkv;
