@@ -31,24 +31,24 @@ unsigned int* error_word() {
 
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st) {
     const int64_t rows = static_cast<int64_t>(p.S) * p.Hq;
+    if (p.NP <= kMergeNarrowMaxParts) {
+        const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
+        if (q_dtype == PKV_BF16) {
+            if (p.D == 128) merge_warp_kernel<128, BF16><<<grid, 256, 0, st>>>(p);
+            else merge_warp_kernel<64, BF16><<<grid, 256, 0, st>>>(p);
+        } else {
+            if (p.D == 128) merge_warp_kernel<128, F16><<<grid, 256, 0, st>>>(p);
+            else merge_warp_kernel<64, F16><<<grid, 256, 0, st>>>(p);
+        }
+        return cudaGetLastError();
+    }
     const dim3 grid(static_cast<unsigned>(rows));
-    const bool narrow = p.NP <= kMergeNarrowMaxParts;
     if (q_dtype == PKV_BF16) {
-        if (p.D == 128) {
-            if (narrow) merge_kernel<128, BF16, 128><<<grid, 128, 0, st>>>(p);
-            else merge_kernel<128, BF16, 256><<<grid, 256, 0, st>>>(p);
-        } else {
-            if (narrow) merge_kernel<64, BF16, 128><<<grid, 128, 0, st>>>(p);
-            else merge_kernel<64, BF16, 256><<<grid, 256, 0, st>>>(p);
-        }
+        if (p.D == 128) merge_kernel<128, BF16, 256><<<grid, 256, 0, st>>>(p);
+        else merge_kernel<64, BF16, 256><<<grid, 256, 0, st>>>(p);
     } else {
-        if (p.D == 128) {
-            if (narrow) merge_kernel<128, F16, 128><<<grid, 128, 0, st>>>(p);
-            else merge_kernel<128, F16, 256><<<grid, 256, 0, st>>>(p);
-        } else {
-            if (narrow) merge_kernel<64, F16, 128><<<grid, 128, 0, st>>>(p);
-            else merge_kernel<64, F16, 256><<<grid, 256, 0, st>>>(p);
-        }
+        if (p.D == 128) merge_kernel<128, F16, 256><<<grid, 256, 0, st>>>(p);
+        else merge_kernel<64, F16, 256><<<grid, 256, 0, st>>>(p);
     }
     return cudaGetLastError();
 }

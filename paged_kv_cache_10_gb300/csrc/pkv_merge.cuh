@@ -109,9 +109,94 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     }
 }
 
-// Threads per merge CTA: rows with few partitions are latency-bound on the
-// CTA's own steps, so they get a narrow CTA; many partitions get two groups
-// per head dimension to double the loads in flight.
+// The same merge with one warp per row, 8 rows per CTA, for rows with few
+// partitions (latency-bound: a CTA per row spends its time on its own
+// barriers).  Lanes hold the partitions' weights (computed once, broadcast
+// by shuffles); each lane accumulates D / 32 consecutive head dimensions
+// with vector loads, four partitions in flight.
+template <int D, typename QT>
+__global__ void __launch_bounds__(256) merge_warp_kernel(const DecodeParams p) {
+    constexpr int VD = D / 32;  // head dimensions per lane (4 or 2)
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (row >= static_cast<int64_t>(p.S) * p.Hq) return;
+    const int s = static_cast<int>(row / p.Hq);
+    // same clamping as the main kernels
+    int L = __ldg(p.seq_lens + s);
+    const int Lcap = p.MB * kBlockSize;
+    L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
+    bool bad = false;
+    const int start = own_start(p.seq_group, p.group_blocks, s, L, &bad);
+    const int Lown = min(L - start, (p.NP - p.part_base) * p.P);
+    const int nown = Lown > 0 ? (Lown + p.P - 1) / p.P : 0;
+    int first, nparts;  // partitions [first, first + nparts) of this row
+    if (!p.cascade) {
+        first = 0;
+        nparts = nown > 0 ? nown : 1;
+        if (nparts <= 1) return;  // written by the main kernel
+    } else {
+        first = start > 0 ? 0 : p.part_base;  // prefix partials only for group members
+        nparts = p.part_base + nown - first;
+    }
+    const float* pm = p.part_m + row * p.NP + first;
+    const float* pl = p.part_l + row * p.NP + first;
+    const float* po = p.part_o + (row * p.NP + first) * D + lane * VD;
+
+    float acc[VD];
+#pragma unroll
+    for (int v = 0; v < VD; ++v) acc[v] = 0.f;
+    float den = 0.f;
+    // partitions in chunks of 32: lane i owns partition base + i
+    float M = -INFINITY;
+    for (int i = lane; i < nparts; i += 32) M = fmaxf(M, __ldg(pl + i) > 0.f ? __ldg(pm + i) : -INFINITY);
+#pragma unroll
+    for (int mask = 16; mask > 0; mask >>= 1) M = fmaxf(M, __shfl_xor_sync(kMergeFull, M, mask));
+    if (M != -INFINITY) {
+        for (int base = 0; base < nparts; base += 32) {
+            const int cnt = min(32, nparts - base);
+            float w = 0.f;
+            if (lane < cnt) {
+                const float l = __ldg(pl + base + lane);
+                w = l > 0.f ? l * exp2f(__ldg(pm + base + lane) - M) : 0.f;
+            }
+            for (int j = 0; j < cnt; j += 4) {
+                float wj[4];
+                float o[4][VD];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    wj[u] = __shfl_sync(kMergeFull, w, (j + u) & 31);
+                    if (j + u < cnt && wj[u] > 0.f) {
+                        const float* src = po + static_cast<int64_t>(base + j + u) * D;
+                        if constexpr (VD == 4) {
+                            const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+                            o[u][0] = x.x; o[u][1] = x.y; o[u][2] = x.z; o[u][3] = x.w;
+                        } else {
+                            const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+                            o[u][0] = x.x; o[u][1] = x.y;
+                        }
+                    } else {
+                        wj[u] = 0.f;  // past the chunk or an empty partial: no data
+#pragma unroll
+                        for (int v = 0; v < VD; ++v) o[u][v] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    den += wj[u];
+#pragma unroll
+                    for (int v = 0; v < VD; ++v) acc[v] = fmaf(wj[u], o[u][v], acc[v]);
+                }
+            }
+        }
+    }
+    auto* out = reinterpret_cast<typename QT::storage*>(p.out) + row * D + lane * VD;
+#pragma unroll
+    for (int v = 0; v < VD; ++v) out[v] = from_float<QT>(den > 0.f ? acc[v] / den : 0.f);
+}
+
+// Rows with at most this many partitions are merged a warp per row; more
+// partitions get the CTA-per-row kernel with two thread groups per head
+// dimension (more loads in flight per row).
 constexpr int kMergeNarrowMaxParts = 16;
 
 }  // namespace pkv

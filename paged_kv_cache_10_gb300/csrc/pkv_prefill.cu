@@ -282,6 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* empty = is_k ? k_empty : v_empty;
         const CUtensorMap* map = is_k ? &tmk : &tmv;
         unsigned char* ring = sm + (is_k ? kOffK : kOffV);
+        // block ids 32 at a time (4 tiles), loaded 4 tiles before their use:
+        // lane l holds the id of block 32 * batch + l
+        auto load_ids = [&](int batch) {
+            const int idx = batch * 32 + lane;
+            return idx < nblk ? __ldg(bt + idx) : 0;
+        };
+        int ids_cur = load_ids(0);
+        int ids_nxt = load_ids(1);
         if (is_k) {
             const uint64_t pol_q = policy_evict_first();
             if constexpr (!kPrefix) {
@@ -292,17 +300,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // G query rows of each member (its batch row in q); rows of
-                // members past the group's end repeat the first member
+                // members past the group's end repeat the first member.  All
+                // of a lane's member rows are read before any copy is issued.
+                constexpr int kMaxPerLane = kTileM / 32;  // G = 1: 4 members per lane
+                int bs[kMaxPerLane];
+#pragma unroll
+                for (int k = 0; k < kMaxPerLane; ++k) {
+                    const int mi = lane + 32 * k;
+                    bs[k] = seq0;
+                    if (mi < kTileM / G && mrow0 + mi < members) bs[k] = __ldg(p.group_members + m0 + mrow0 + mi);
+                }
                 if (lane == 0) mbar_arrive_expect_tx(q_full, kOpBytes);
                 __syncwarp();
-                for (int mi = lane; mi < kTileM / G; mi += 32) {
-                    int b = seq0;
-                    if (mrow0 + mi < members) {
-                        b = __ldg(p.group_members + m0 + mrow0 + mi);
-                        if (b < 0 || b >= p.S) {
-                            report(p.err, PKV_DEVERR_SEQ_LEN);
-                            b = seq0;
-                        }
+#pragma unroll
+                for (int k = 0; k < kMaxPerLane; ++k) {
+                    const int mi = lane + 32 * k;
+                    if (mi >= kTileM / G) break;
+                    int b = bs[k];
+                    if (b < 0 || b >= p.S) {
+                        report(p.err, PKV_DEVERR_SEQ_LEN);
+                        b = seq0;
                     }
                     for (int dh = 0; dh < 2; ++dh)
                         tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes + mi * G * 128, &tmq, dh * 64, h * G, b, q_full,
@@ -310,14 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // block ids 32 at a time (4 tiles), loaded 4 tiles before their use:
-        // lane l holds the id of block 32 * batch + l
-        auto load_ids = [&](int batch) {
-            const int idx = batch * 32 + lane;
-            return idx < nblk ? __ldg(bt + idx) : 0;
-        };
-        int ids_cur = load_ids(0);
-        int ids_nxt = load_ids(1);
         int issued = 0;
         for (int j = 0; j < nkt; ++j) {
             const int st = j % kStages;
@@ -454,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             row_valid = mrow0 + rq < members;
             pos = kv_end - 1;
         }
+        // prefix pass: this row's batch row, read now so the epilogue does
+        // not wait for it
+        const int member_row = kPrefix && row_valid ? __ldg(p.group_members + m0 + mrow0 + rq) : -1;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const float c = p.qk_scale;
         const float2 c2 = make_float2(c, c);
@@ -571,11 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // partial of this prefix partition: reference maximum (log2
                 // units), the sum relative to it, and O / l
-                int b = -1;
-                if (row_valid) {
-                    b = __ldg(p.group_members + m0 + mrow0 + rq);
-                    if (b < 0 || b >= p.S) b = -1;
-                }
+                const int b = member_row >= 0 && member_row < p.S ? member_row : -1;
                 const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + g) * p.NP + pp;
                 if (b >= 0) {
                     p.part_m[prow] = m_ref;
