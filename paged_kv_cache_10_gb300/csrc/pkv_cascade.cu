@@ -78,7 +78,7 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     const int npp = num_groups > 0 ? prefix_partitions(max_group_blocks) : 0;
     const int64_t nps = max_seq_len > 0 ? cdiv(max_seq_len, P) : 1;
     const int64_t NP = npp + nps;
-    const int64_t row_chunks = cdiv(static_cast<int64_t>(max_group_members) * G, 128);
+    const int64_t row_chunks = cdiv(static_cast<int64_t>(max_group_members) * G, 128);  // one 128-row Q tile per CTA
     if (NP > 0x7fffffff || static_cast<int64_t>(num_groups) * row_chunks > 65535) return PKV_ERR_UNSUPPORTED;
     const size_t need = partials_bytes(num_seqs, num_q_heads, d->head_size, NP);
     if (!workspace || ws_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;

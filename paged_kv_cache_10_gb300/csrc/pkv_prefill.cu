@@ -37,23 +37,31 @@ namespace pkv {
 namespace {
 
 constexpr int kPD = 128;        // head_size
-constexpr int kTileM = 128;     // query rows per CTA
+constexpr int kTileM = 128;     // query rows per Q tile (two Q tiles per CTA)
 constexpr int kTileN = 128;     // keys per tile
-constexpr int kStages = 3;      // K ring and V ring depth
+constexpr int kKStages = 3;     // key ring depth
+constexpr int kVStages = 2;     // value ring depth
 constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
 constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
 constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
-constexpr int kThreads = 224;          // K-load warp, MMA warp, 4 softmax warps, V-load warp
-constexpr int kVWarp = 6;
-constexpr int kSoftmaxThreads = 128;
-constexpr float kRebase = 8.0f;  // log2 units
+// Three warpgroups: warps 0-3 load (0: Q and keys, 2: values), issue the
+// MMAs (1) or idle (3); warps 4-7 run the softmax of Q tile A, warps 8-11 of
+// Q tile B.  setmaxnreg moves registers from the first to the other two:
+// 128 x 64 + 256 x 216 <= 384 x 168, the launch's allocation.
+constexpr int kThreads = 384;
+constexpr int kLoadRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(128 * kLoadRegs + 256 * kSoftmaxRegs <= kThreads * (65536 / kThreads / 8 * 8), "register split");
+constexpr int kSoftmaxWarps = 4;  // per Q tile
+constexpr float kRebase = 8.0f;   // log2 units
 
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kOpBytes;
-constexpr int kOffV = kOffK + kStages * kOpBytes;
-constexpr int kOffBar = kOffV + kStages * kOpBytes;
-// q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], v_zero, s_full[2], p_full[2], o_done[2], drain
-constexpr int kNumBars = 1 + 4 * kStages + 1 + 2 + 2 + 2 + 1;
+constexpr int kOffQ = 0;                               // Q tiles A, B
+constexpr int kOffK = kOffQ + 2 * kOpBytes;
+constexpr int kOffV = kOffK + kKStages * kOpBytes;
+constexpr int kOffBar = kOffV + kVStages * kOpBytes;
+// q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], v_zero, s_full[2 tiles], p_full[2 tiles],
+// o_done[2 tiles], drain
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 1 + 2 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -133,25 +141,19 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
         : "memory");
 }
 
-// Waits, in order, for the phases of o_done barrier `bar` (P V of tiles b,
-// b + 2, ... for the barrier of tile parity b) up to the one of tile `upto`;
-// `next` is the next tile of that parity to wait for.  The barrier is at
-// most one phase ahead of `next` whenever this runs, so parity waits stay
-// exact.
-__device__ __forceinline__ bool consume_pv(uint64_t* bar, int& next, int upto) {
-    bool ok = true;
-    while (ok && next <= upto) {
-        ok = tc::wait_spin(bar, (next >> 1) & 1);
-        next += 2;
-    }
-    return ok;
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
+}
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
 }
 
-// kPrefix = false: causal prefill, 128 rows = 128 / G tokens x G heads of one
-// (sequence, KV head), keys 0 .. each row's position, normalised output.
-// kPrefix = true: the cascade decode's shared-prefix pass, 128 rows = 128 / G
-// members x G heads of one (group, KV head), keys = one 512-token partition
-// of the group's shared blocks (no causal mask), split-K partials out.
+// kPrefix = false: causal prefill; Q tile X (X = 0, 1) holds 128 / G tokens x
+// the G heads of one (sequence, KV head), tokens [t0 + X * TT, ...); keys 0 ..
+// each row's position; normalised output.
+// kPrefix = true: the cascade decode's shared-prefix pass; Q tile X holds
+// 128 / G members x G heads of one (group, KV head); keys = one 512-token
+// partition of the group's shared blocks (no causal mask); split-K partials.
 template <typename T, bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
@@ -160,14 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + kOffBar);
-    uint64_t* k_full = q_full + 1;
-    uint64_t* k_empty = k_full + kStages;
-    uint64_t* v_full = k_empty + kStages;
-    uint64_t* v_empty = v_full + kStages;
-    uint64_t* v_zero = v_empty + kStages;
-    uint64_t* s_full = v_zero + 1;   // [2]
-    uint64_t* p_full = s_full + 2;   // [2], by tile parity
-    uint64_t* o_done = p_full + 2;   // [2], by tile parity
+    uint64_t* k_full = q_full + 1;           // [kKStages]
+    uint64_t* k_empty = k_full + kKStages;   // [kKStages]
+    uint64_t* v_full = k_empty + kKStages;   // [kVStages]
+    uint64_t* v_empty = v_full + kVStages;   // [kVStages]
+    uint64_t* v_zero = v_empty + kVStages;
+    uint64_t* s_full = v_zero + 1;   // [Q tile]
+    uint64_t* p_full = s_full + 2;   // [Q tile]
+    uint64_t* o_done = p_full + 2;   // [Q tile]
     uint64_t* drain = o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
@@ -175,11 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y;
     const int G = p.G;
+    const int RQ = kTileM / G;  // tokens (prefill) or members (prefix) per Q tile
     // ---- this CTA's rows and keys (uniform across the CTA).  Keys are
-    // counted from the CTA's first block `bt` points at; a row attends to
-    // keys 0 .. its limit (prefill: its position; prefix pass: all).
+    // counted from the block `bt` points at.  kv_end[X]: keys Q tile X needs
+    // (0 when the tile is empty); the CTA loads max(kv_end) keys.
     const int32_t* bt;
-    int nblk, kv_end;
+    int kv_end[2];
     // prefill
     int q0 = 0, n = 0, ctx = 0, t0 = 0;
     // prefix pass
@@ -196,18 +199,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             return;
         }
         if (n > p.max_query_len && threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-        t0 = qt * p.TT;
+        t0 = qt * 2 * RQ;
         if (t0 >= n) return;
-        ctx = L - n;                                  // tokens before this chunk
-        kv_end = ctx + t0 + min(p.TT, n - t0);        // keys [0, kv_end)
-        nblk = (kv_end + kBlockSize - 1) / kBlockSize;
+        ctx = L - n;  // tokens before this chunk
+        for (int X = 0; X < 2; ++X) {
+            const int tx = t0 + X * RQ;
+            kv_end[X] = tx < n ? ctx + tx + min(RQ, n - tx) : 0;
+        }
         bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
     } else {
         pp = blockIdx.x;
         const int grp = blockIdx.z / p.row_chunks, chunk = blockIdx.z % p.row_chunks;
         m0 = __ldg(p.group_offsets + grp);
         members = __ldg(p.group_offsets + grp + 1) - m0;
-        mrow0 = chunk * (kTileM / G);  // first member of this CTA
+        // One Q tile per CTA: the prefix pass is short (a few key tiles per
+        // CTA), so more CTAs beat the second tile's overlap.
+        mrow0 = chunk * RQ;  // first member of this CTA
         if (mrow0 >= members) return;
         int nb = __ldg(p.group_blocks + grp);
         if (nb < 0 || nb > p.MB) {
@@ -235,24 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return;
         }
-        nblk = min(nb, b0 + kPrefixPartitionBlocks) - b0;
-        kv_end = nblk * kBlockSize;
+        const int keys = (min(nb, b0 + kPrefixPartitionBlocks) - b0) * kBlockSize;
+        kv_end[0] = keys;
+        kv_end[1] = 0;
         bt = p.block_tables + static_cast<int64_t>(seq0) * p.MB + b0;
     }
-    const int nkt = (kv_end + kTileN - 1) / kTileN;
+    const bool has_b = kv_end[1] > 0;
+    const int kv_max = max(kv_end[0], kv_end[1]);
+    const int nkt = (kv_max + kTileN - 1) / kTileN;      // key tiles loaded
+    const int nblk = (kv_max + kBlockSize - 1) / kBlockSize;
+    const int nt[2] = {(kv_end[0] + kTileN - 1) / kTileN, (kv_end[1] + kTileN - 1) / kTileN};  // per Q tile
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             mbar_init(k_full + i, 1);
             mbar_init(k_empty + i, 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             mbar_init(v_full + i, 1);
             mbar_init(v_empty + i, 1);
         }
         mbar_init(v_zero, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
-            mbar_init(p_full + i, kSoftmaxThreads);
+            mbar_init(p_full + i, kSoftmaxWarps);  // one arrival per softmax warp
             mbar_init(o_done + i, 1);
         }
         mbar_init(drain, 1);
@@ -267,22 +281,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    // columns [0, 256): S of even / odd tiles (its first 64 columns then hold
-    // that tile's P, two 16-bit probabilities per column); [256, 384): O
-    const uint32_t tO = tmem + 256;
-
-    if (warp == 0 || warp == kVWarp) {
+    // tensor-memory columns: S of Q tile X at X * 128 (its first 64 columns
+    // then hold that tile's P, two 16-bit probabilities per column); O of Q
+    // tile X at 256 + X * 128
+    if (warp < 4) {
+      setmaxnreg_dec();
+      if (warp == 0 || warp == 2) {
         // --------------------------------------------- TMA producers (K, V)
-        // Warp 0 streams Q and the key tiles, warp 6 the value tiles, each
-        // through its own 3-stage ring, so a key load never waits for a P V
-        // to free a value stage.
+        // Warp 0 streams Q and the key tiles, warp 2 the value tiles, each
+        // through its own ring, so a key load never waits for a P V to free
+        // a value stage.
         const bool is_k = warp == 0;
-        const uint64_t pol_kv = policy_evict_last();  // re-read by the sequence's other query tiles
+        const int nst = is_k ? kKStages : kVStages;
+        const uint64_t pol_kv = policy_evict_last();  // re-read by other CTAs of the sequence / group
         uint64_t* full = is_k ? k_full : v_full;
         uint64_t* empty = is_k ? k_empty : v_empty;
         const CUtensorMap* map = is_k ? &tmk : &tmv;
         unsigned char* ring = sm + (is_k ? kOffK : kOffV);
-        // block ids 32 at a time (4 tiles), loaded 4 tiles before their use:
+        // block ids 32 at a time (4 tiles), read 4 tiles before their use:
         // lane l holds the id of block 32 * batch + l
         auto load_ids = [&](int batch) {
             const int idx = batch * 32 + lane;
@@ -292,44 +308,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ids_nxt = load_ids(1);
         if (is_k) {
             const uint64_t pol_q = policy_evict_first();
+            const int ntiles = has_b ? 2 : 1;
             if constexpr (!kPrefix) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(q_full, kOpBytes);
-                    for (int dh = 0; dh < 2; ++dh)
-                        tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes, &tmq, dh * 64, h * G, q0 + t0, q_full, pol_q);
+                    mbar_arrive_expect_tx(q_full, ntiles * kOpBytes);
+                    for (int X = 0; X < ntiles; ++X)
+                        for (int dh = 0; dh < 2; ++dh)
+                            tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kHalfBytes, &tmq, dh * 64, h * G,
+                                            q0 + t0 + X * RQ, q_full, pol_q);
                 }
             } else {
                 // G query rows of each member (its batch row in q); rows of
                 // members past the group's end repeat the first member.  All
                 // of a lane's member rows are read before any copy is issued.
-                constexpr int kMaxPerLane = kTileM / 32;  // G = 1: 4 members per lane
+                constexpr int kMaxPerLane = 2 * kTileM / 32;  // G = 1: 8 members per lane
                 int bs[kMaxPerLane];
 #pragma unroll
                 for (int k = 0; k < kMaxPerLane; ++k) {
                     const int mi = lane + 32 * k;
                     bs[k] = seq0;
-                    if (mi < kTileM / G && mrow0 + mi < members) bs[k] = __ldg(p.group_members + m0 + mrow0 + mi);
+                    if (mi < ntiles * RQ && mrow0 + mi < members) bs[k] = __ldg(p.group_members + m0 + mrow0 + mi);
                 }
-                if (lane == 0) mbar_arrive_expect_tx(q_full, kOpBytes);
+                if (lane == 0) mbar_arrive_expect_tx(q_full, ntiles * kOpBytes);
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < kMaxPerLane; ++k) {
                     const int mi = lane + 32 * k;
-                    if (mi >= kTileM / G) break;
+                    if (mi >= ntiles * RQ) break;
                     int b = bs[k];
                     if (b < 0 || b >= p.S) {
                         report(p.err, PKV_DEVERR_SEQ_LEN);
                         b = seq0;
                     }
+                    const int X = mi / RQ, mx = mi - X * RQ;
                     for (int dh = 0; dh < 2; ++dh)
-                        tc::tma_load_3d(sm + kOffQ + dh * kHalfBytes + mi * G * 128, &tmq, dh * 64, h * G, b, q_full,
-                                        pol_q);
+                        tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kHalfBytes + mx * G * 128, &tmq, dh * 64,
+                                        h * G, b, q_full, pol_q);
                 }
             }
         }
         int issued = 0;
         for (int j = 0; j < nkt; ++j) {
-            const int st = j % kStages;
+            const int st = j % nst;
             const int nb_tile = min(8, nblk - j * 8);
             if (j > 0 && (j & 3) == 0) {
                 ids_cur = ids_nxt;
@@ -341,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 phys = 0;
             }
             const int row = (phys * p.Hkv + h) * kBlockSize;
-            // the stage is free once the MMA that read it (Q K^T or P V of
-            // tile j - kStages) has completed
-            const bool waited = j < kStages || mbar_wait(empty + st, ((j / kStages) + 1) & 1);
+            // the stage is free once the MMAs that read it (Q K^T or P V of
+            // tile j - nst) have completed
+            const bool waited = j < nst || mbar_wait(empty + st, ((j / nst) + 1) & 1);
             if (!warp_all(waited)) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
@@ -361,14 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issued = j + 1;
             if (!is_k && j == nkt - 1) {
-                // Value rows at or past kv_end get probability 0, but the
-                // pool slots past a sequence's end (and never-loaded rows)
-                // may hold any bits, NaN included, and 0 * NaN = NaN in the
-                // MMA: clear them once the tile has landed.
-                const int r0 = kv_end - j * kTileN;
+                // Value rows at or past the last key get probability 0, but
+                // the pool slots past a sequence's end (and never-loaded
+                // rows) may hold any bits, NaN included, and 0 * NaN = NaN in
+                // the MMA: clear them once the tile has landed.
+                const int r0 = kv_max - j * kTileN;
                 bool okv = true;
                 if (r0 < kTileN) {
-                    okv = warp_all(mbar_wait(v_full + st, (j / kStages) & 1));
+                    okv = warp_all(mbar_wait(v_full + st, (j / nst) & 1));
                     if (okv) {
                         unsigned char* vb = sm + kOffV + st * kOpBytes;
                         for (int idx = lane; idx < (kTileN - r0) * 16; idx += 32) {
@@ -390,52 +410,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // every copy this warp started has landed before the CTA can exit
-        for (int j = max(0, issued - kStages); j < issued; ++j)
-            if (!mbar_wait(full + j % kStages, (j / kStages) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+        for (int j = max(0, issued - nst); j < issued; ++j)
+            if (!mbar_wait(full + j % nst, (j / nst) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
         if (is_k && lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        // Issue order S_0, S_1, P V_0, S_2, P V_1, ...: tcgen05.mma from one
-        // thread run in order, so S_{j+2} overwrites the tensor-memory buffer
-        // of S_j / P_j only after P V_j has read P_j.
+        // Order S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
+        // P V_B(j), S_B(j+1).  tcgen05.mma from one thread run in order, so
+        // S_X(j+1) overwrites Q tile X's S / P columns only after P V_X(j)
+        // has read P_X(j), and the softmax of one Q tile overlaps the MMAs
+        // of the other.
         if (lane == 0) {
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
             const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
-            const uint32_t aQ = smem_addr(sm + kOffQ);
             bool ok = tc::wait_spin(q_full, 0);
-            for (int j = 0; ok && j <= nkt; ++j) {
+            auto issue_s = [&](int X, int j) {
+                const uint32_t aQ = smem_addr(sm + kOffQ + X * kOpBytes);
+                const uint32_t aK = smem_addr(sm + kOffK + (j % kKStages) * kOpBytes);
+#pragma unroll
+                for (int kk = 0; kk < kPD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                    tc::mma_f16(tmem + X * kTileN, tc::sdesc_sw128(aQ + off, 16, 1024),
+                                tc::sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
+                }
+                tc::commit(s_full + X);
+            };
+            auto issue_pv = [&](int X, int j) {
+                const uint32_t aV = smem_addr(sm + kOffV + (j % kVStages) * kOpBytes);
+#pragma unroll
+                for (int kk = 0; kk < kTileN / 16; ++kk)
+                    mma_f16_tmem_a(tmem + 256 + X * kTileN, tmem + X * kTileN + kk * 8,
+                                   tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024), idO, j > 0 || kk > 0);
+                tc::commit(o_done + X);
+            };
+            // tile 0's keys, then S of both Q tiles
+            if (ok) ok = tc::wait_spin(k_full, 0);
+            if (ok) {
+                tc::fence_after();
+                for (int X = 0; X < 2; ++X)
+                    if (nt[X] > 0) issue_s(X, 0);
+                tc::commit(k_empty);
+            }
+            for (int j = 0; ok && j < nkt; ++j) {
                 if (*abort_flag) break;
-                if (j < nkt) {
-                    const int st = j % kStages, sb = j & 1;
-                    ok = tc::wait_spin(k_full + st, (j / kStages) & 1);
-                    if (!ok) break;
-                    tc::fence_after();
-                    const uint32_t aK = smem_addr(sm + kOffK + st * kOpBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kPD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        tc::mma_f16(tmem + sb * kTileN, tc::sdesc_sw128(aQ + off, 16, 1024),
-                                    tc::sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
+                // values of tile j (and, for the last tile, its cleared rows)
+                ok = tc::wait_spin(v_full + j % kVStages, (j / kVStages) & 1);
+                if (ok && j == nkt - 1) ok = tc::wait_spin(v_zero, 0);
+                bool kn = false;  // keys of tile j + 1 waited for
+                for (int X = 0; ok && X < 2; ++X) {
+                    if (j < nt[X]) {
+                        ok = tc::wait_spin(p_full + X, j & 1);
+                        if (!ok) break;
+                        tc::fence_after();
+                        issue_pv(X, j);
                     }
-                    tc::commit(s_full + sb);
-                    tc::commit(k_empty + st);
+                    if (j + 1 < nt[X]) {
+                        if (!kn) {
+                            ok = tc::wait_spin(k_full + (j + 1) % kKStages, ((j + 1) / kKStages) & 1);
+                            if (!ok) break;
+                            tc::fence_after();
+                            kn = true;
+                        }
+                        issue_s(X, j + 1);
+                    }
                 }
-                if (j >= 1) {
-                    const int i = j - 1, st = i % kStages;
-                    ok = tc::wait_spin(v_full + st, (i / kStages) & 1);
-                    if (ok && i == nkt - 1) ok = tc::wait_spin(v_zero, 0);
-                    if (ok) ok = tc::wait_spin(p_full + (i & 1), (i >> 1) & 1);
-                    if (!ok) break;
-                    tc::fence_after();
-                    const uint32_t aV = smem_addr(sm + kOffV + st * kOpBytes);
-                    const uint32_t aP = tmem + (i & 1) * kTileN;
-#pragma unroll
-                    for (int kk = 0; kk < kTileN / 16; ++kk)
-                        mma_f16_tmem_a(tO, aP + kk * 8, tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024),
-                                       idO, i > 0 || kk > 0);
-                    tc::commit(o_done + (i & 1));
-                    tc::commit(v_empty + st);
-                }
+                if (!ok) break;
+                tc::commit(v_empty + j % kVStages);
+                if (j + 1 < nkt) tc::commit(k_empty + (j + 1) % kKStages);
             }
             if (!ok) {
                 report(p.err, PKV_DEVERR_TIMEOUT);
@@ -446,40 +487,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!tc::wait_spin(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
         }
         __syncwarp();
+      }
     } else {
+        setmaxnreg_inc();
         // ------------------------------------------- softmax, O, epilogue
-        // One thread per query row (its tensor-memory lane).  P_j goes back
-        // into tensor memory over S_j; the softmax waits for a P V only when
-        // it has to rescale O.
-        const int wq = warp & 3;  // tensor-memory lane quarter
+        // One thread per query row (its tensor-memory lane) of Q tile X.
+        // P_j goes back into tensor memory over S_j.  S_X(j) is issued after
+        // P V_X(j - 1), so when it is complete O holds every earlier tile and
+        // can be rescaled without waiting.
+        const int X = (warp - 4) >> 2;     // Q tile
+        const int wq = warp & 3;           // tensor-memory lane quarter
         const int row = wq * 32 + lane;
-        const int rq = row / G, g = row - rq * G;  // token (prefill) or member (prefix) in the tile, head
+        const int rq = row / G, g = row - rq * G;
+        const int ntx = nt[X];
         bool row_valid;
         int pos;  // last key this row attends to
         if constexpr (!kPrefix) {
-            row_valid = t0 + rq < n;
-            pos = ctx + t0 + min(rq, n - 1 - t0);  // padding rows reuse the last position
+            const int tx = t0 + X * RQ;
+            row_valid = tx + rq < n;
+            pos = ctx + tx + min(rq, max(n - 1 - tx, 0));  // padding rows reuse the last position
         } else {
-            row_valid = mrow0 + rq < members;
-            pos = kv_end - 1;
+            row_valid = mrow0 + X * RQ + rq < members;
+            pos = kv_end[0] - 1;
         }
         // prefix pass: this row's batch row, read now so the epilogue does
         // not wait for it
-        const int member_row = kPrefix && row_valid ? __ldg(p.group_members + m0 + mrow0 + rq) : -1;
+        const int member_row = kPrefix && row_valid ? __ldg(p.group_members + m0 + mrow0 + X * RQ + rq) : -1;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + X * kTileN + lane_base;
+        const uint32_t tO = tmem + 256 + X * kTileN + lane_base;
         const float c = p.qk_scale;
         const float2 c2 = make_float2(c, c);
         float m_ref = -INFINITY, l = 0.f;
-        int next_even = 0, next_odd = 1;  // next P V (tile index) to wait for, per parity
         bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            const int sb = j & 1;
-            ok = warp_all(tc::wait_spin(s_full + sb, (j >> 1) & 1));
+        for (int j = 0; j < ntx; ++j) {
+            ok = warp_all(tc::wait_spin(s_full + X, j & 1));
             if (!ok || !warp_all(*abort_flag == 0)) break;
             tc::fence_after();
+            // P V_X(j - 1) is complete (it precedes S_X(j)): take its phase
+            if (j > 0) ok = warp_all(tc::wait_spin(o_done + X, (j - 1) & 1));
+            if (!ok) break;
             uint32_t x[4][32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tc::ld32(tmem + lane_base + sb * kTileN + q * 32, x[q]);
+            for (int q = 0; q < 4; ++q) tc::ld32(tS + q * 32, x[q]);
             tc::wait_ld();
 
             // masked keys -inf; row maximum of the raw scores (scale > 0
@@ -521,52 +571,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             const float2 lt = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
             l = l * alpha + (lt.x + lt.y);
-            tc::st32(tmem + lane_base + sb * kTileN, *reinterpret_cast<uint32_t(*)[32]>(pk));
-            tc::st32(tmem + lane_base + sb * kTileN + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-
-            // keep both o_done barriers within one phase of this thread
-            if (j >= 2) ok = warp_all(sb ? consume_pv(o_done + 1, next_odd, j - 2) : consume_pv(o_done, next_even, j - 2));
-            if (ok && j > 0 && __any_sync(0xffffffffu, rebase)) {
-                // O must hold P V of tile j - 1 before it is rescaled
-                ok = warp_all(sb ? consume_pv(o_done, next_even, j - 1) : consume_pv(o_done + 1, next_odd, j - 1));
-                if (ok) {
-                    tc::fence_after();
-                    const float2 a2 = make_float2(alpha, alpha);
+            tc::st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+            tc::st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+            if (j > 0 && __any_sync(0xffffffffu, rebase)) {
+                const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t o[32];
-                        tc::ld32(tO + lane_base + q * 32, o);
-                        tc::wait_ld();
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[32];
+                    tc::ld32(tO + q * 32, o);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
-                            o[2 * i] = __float_as_uint(v.x);
-                            o[2 * i + 1] = __float_as_uint(v.y);
-                        }
-                        tc::st32(tO + lane_base + q * 32, o);
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 v = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+                        o[2 * i] = __float_as_uint(v.x);
+                        o[2 * i + 1] = __float_as_uint(v.y);
                     }
+                    tc::st32(tO + q * 32, o);
                 }
             }
             tc::wait_st();
-            if (!ok) break;
             tc::fence_before();
-            tc::arrive(p_full + sb);
+            __syncwarp();
+            if (lane == 0) tc::arrive(p_full + X);
         }
-        const bool live = ok && warp_all(*abort_flag == 0);
-        if (live) {
-            ok = warp_all(consume_pv(o_done, next_even, nkt - 1));
-            ok = warp_all(ok && consume_pv(o_done + 1, next_odd, nkt - 1));
-        }
+        const bool live = ntx > 0 && ok && warp_all(*abort_flag == 0);
+        if (live) ok = warp_all(tc::wait_spin(o_done + X, (ntx - 1) & 1));
         if (live && ok) {
             tc::fence_after();
             const float inv = 1.f / l;
             if constexpr (!kPrefix) {
-                typename T::storage* orow = reinterpret_cast<typename T::storage*>(p.out) +
-                                            (static_cast<int64_t>(q0 + t0 + rq) * p.Hq + h * G + g) * kPD;
+                typename T::storage* orow =
+                    reinterpret_cast<typename T::storage*>(p.out) +
+                    (static_cast<int64_t>(q0 + t0 + X * RQ + rq) * p.Hq + h * G + g) * kPD;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t o[32];
-                    tc::ld32(tO + lane_base + q * 32, o);
+                    tc::ld32(tO + q * 32, o);
                     tc::wait_ld();
                     if (row_valid) {
 #pragma unroll
@@ -592,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t o[32];
-                    tc::ld32(tO + lane_base + q * 32, o);
+                    tc::ld32(tO + q * 32, o);
                     tc::wait_ld();
                     if (b >= 0) {
                         float4* po = reinterpret_cast<float4*>(p.part_o + prow * kPD + q * 32);
@@ -716,7 +756,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     p.NB = desc->num_blocks;
     p.G = G;
     p.TT = kTileM / G;
-    p.num_qtiles = (max_query_len + p.TT - 1) / p.TT;
+    p.num_qtiles = (max_query_len + 2 * p.TT - 1) / (2 * p.TT);  // CTAs of two Q tiles
     p.max_query_len = max_query_len;
     p.qk_scale = scale * 1.4426950408889634f;
     p.err = err;
