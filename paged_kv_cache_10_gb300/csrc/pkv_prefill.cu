@@ -47,10 +47,10 @@ constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
 // Three warpgroups: warps 0-3 load (0: Q and keys, 2: values), issue the
 // MMAs (1) or idle (3); warps 4-7 run the softmax of Q tile A, warps 8-11 of
 // Q tile B.  setmaxnreg moves registers from the first to the other two:
-// 128 x 64 + 256 x 216 <= 384 x 168, the launch's allocation.
+// 128 x 72 + 256 x 208 <= 384 x 168, the launch's allocation.
 constexpr int kThreads = 384;
-constexpr int kLoadRegs = 64;
-constexpr int kSoftmaxRegs = 216;
+constexpr int kLoadRegs = 72;
+constexpr int kSoftmaxRegs = 208;
 static_assert(128 * kLoadRegs + 256 * kSoftmaxRegs <= kThreads * (65536 / kThreads / 8 * 8), "register split");
 constexpr int kSoftmaxWarps = 4;  // per Q tile
 constexpr float kRebase = 8.0f;   // log2 units
@@ -424,23 +424,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
             const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
             bool ok = tc::wait_spin(q_full, 0);
+            // Descriptors: bases per Q tile and ring stage, computed once; the
+            // k-th 16-element step adds a constant (the start address field
+            // is the low 14 bits, >> 4, and every operand sits below 256 KB).
+            // Building a descriptor per MMA would make issue, not the tensor
+            // core, the limit.
+            const uint64_t dQ0 = tc::sdesc_sw128(smem_addr(sm + kOffQ), 16, 1024);
+            const uint64_t dQ1 = tc::sdesc_sw128(smem_addr(sm + kOffQ + kOpBytes), 16, 1024);
+            const uint64_t dK0 = tc::sdesc_sw128(smem_addr(sm + kOffK), 16, 1024);
+            const uint64_t dK1 = tc::sdesc_sw128(smem_addr(sm + kOffK + kOpBytes), 16, 1024);
+            const uint64_t dK2 = tc::sdesc_sw128(smem_addr(sm + kOffK + 2 * kOpBytes), 16, 1024);
+            const uint64_t dV0 = tc::sdesc_sw128(smem_addr(sm + kOffV), kHalfBytes, 1024);
+            const uint64_t dV1 = tc::sdesc_sw128(smem_addr(sm + kOffV + kOpBytes), kHalfBytes, 1024);
             auto issue_s = [&](int X, int j) {
-                const uint32_t aQ = smem_addr(sm + kOffQ + X * kOpBytes);
-                const uint32_t aK = smem_addr(sm + kOffK + (j % kKStages) * kOpBytes);
+                const int st = j % kKStages;
+                const uint64_t q = X ? dQ1 : dQ0;
+                const uint64_t k = st == 0 ? dK0 : (st == 1 ? dK1 : dK2);
+                const uint32_t d = tmem + X * kTileN;
 #pragma unroll
                 for (int kk = 0; kk < kPD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    tc::mma_f16(tmem + X * kTileN, tc::sdesc_sw128(aQ + off, 16, 1024),
-                                tc::sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                    tc::mma_f16(d, q + off, k + off, idS, kk > 0);
                 }
                 tc::commit(s_full + X);
             };
             auto issue_pv = [&](int X, int j) {
-                const uint32_t aV = smem_addr(sm + kOffV + (j % kVStages) * kOpBytes);
+                const uint64_t v = (j % kVStages) ? dV1 : dV0;
+                const uint32_t d = tmem + 256 + X * kTileN, pa = tmem + X * kTileN;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk)
-                    mma_f16_tmem_a(tmem + 256 + X * kTileN, tmem + X * kTileN + kk * 8,
-                                   tc::sdesc_sw128(aV + kk * kBlockTileBytes, kHalfBytes, 1024), idO, j > 0 || kk > 0);
+                    mma_f16_tmem_a(d, pa + kk * 8, v + static_cast<uint64_t>((kk * kBlockTileBytes) >> 4), idO,
+                                   j > 0 || kk > 0);
                 tc::commit(o_done + X);
             };
             // tile 0's keys, then S of both Q tiles
