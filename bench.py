@@ -48,7 +48,9 @@ KERNEL_SOURCES = {
     "cuda_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh"],
     "tensor_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh"],
     "cascade": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh",
-                _CSRC + "pkv_cascade.cu"],
+                _CSRC + "pkv_cascade.cu", _CSRC + "pkv_prefill.cu", _CSRC + "pkv_tcgen05.cuh", _CSRC + "pkv_merge.cuh"],
+    "prefill": [_CSRC + "pkv_prefill.cu", _CSRC + "pkv_tcgen05.cuh", _CSRC + "pkv_device.cuh",
+                _CSRC + "pkv_decode_mma.cuh"],
 }
 
 
@@ -599,8 +601,9 @@ def run_prefill(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "prefill_tc_kernel", "mean_launch_us": round(a_ms * 1e3, 2),
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, "prefill"),
+                     "peak_kind": peak_kind, "kernel": "prefill_tc_kernel",
+                     "kernel_sources_hash": kernel_hash("prefill"), "mean_launch_us": round(a_ms * 1e3, 2),
                      "algorithmic_flops_per_launch": flops,
                      "hbm_gbs_at_min_bytes": round(nbytes / (a_ms / 1e3) / 1e9, 1)},
         "clocks": clocks,
