@@ -697,6 +697,51 @@ def run_swap(args, local_rank):
 
 
 # ----------------------------------------------------------- reference arm
+def run_reference_prefill(args, wl):
+    """The oracle as the reference arm of a prefill workload: per step, the
+    float64 causal attention of the first tokens of one chunk (all heads,
+    every key they see), rotating through the sequences."""
+    import oracle
+    from paged_kv_cache_10_gb300.pagedkv import Allocator
+    a = Allocator(wl.NB, wl.b, wl.free_order)
+    for s, c in enumerate(wl.ctx):
+        a.seq_new(s, int(c))
+    slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
+    tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
+    kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
+    m = 4
+
+    def one(i):
+        s = i % wl.S
+        n = min(m, wl.qlens[s])
+        ctx = int(lens[s]) - wl.qlens[s]
+        oracle.paged_prefill(np.ascontiguousarray(wl.q[qs[s]:qs[s] + n]), wl.dtype, np.array([0, n], np.int32), kp, vp,
+                             wl.dtype, tables[s:s + 1], np.array([ctx + n], np.int32), wl.scale)
+        return 4.0 * wl.D * wl.Hq * (n * ctx + n * (n + 1) // 2)
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        one(i)
+    flops, t = 0.0, 0.0
+    for i in range(K):
+        t0 = time.perf_counter()
+        flops += one(W + i)
+        t += time.perf_counter() - t0
+    value = flops / t / 1e12
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": K, "warmup": W, "ms_per_step": round(1e3 * t / K, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"the first {m} tokens of one chunk of {wl.name} per step (all heads), rotating: "
+                                   f"float64 causal attention"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -705,6 +750,8 @@ def run_reference(args, rank, world):
     from paged_kv_cache_10_gb300.pagedkv import Allocator, apply_setup
 
     oracle.build()
+    if args.workload in workloads.PREFILL:
+        return run_reference_prefill(args, workloads.PREFILL[args.workload]())
     wl = workloads.NAMED[args.workload]()
 
     class HostStep:  # the host bookkeeping of the step, through the C++ allocator

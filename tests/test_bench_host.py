@@ -70,3 +70,16 @@ def test_step_bytes_counts_the_gathered_kv():
     # distinct tokens: block 7 (16), block 3 (1), block 9 (16), block 4 (8)
     assert nb["unique_kv"] == (16 + 1 + 16 + 8) * 2 * 2 * 128 * 2
     assert nb["decode_unique"] == nb["decode"] - nb["kv"] + nb["unique_kv"]
+
+
+def test_prefill_flops_count_every_causal_pair():
+    import bench
+
+    class WL:
+        D, Hq = 128, 8
+        ctx = [0, 5, 33]
+        qlens = [3, 4, 1]
+
+    # brute force: each new row at position p sees keys 0..p; 4 * D flops per key and head
+    pairs = sum(c + j + 1 for c, n in zip(WL.ctx, WL.qlens) for j in range(n))
+    assert bench.prefill_flops(WL()) == 4.0 * 128 * 8 * pairs
