@@ -255,7 +255,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl = workloads.NAMED[args.workload]()
-    step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=args.cascade)
+    step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=args.cascade,
+                      fused=not args.unfused)
     nbytes = step_bytes(step)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -348,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
             from paged_kv_cache_10_gb300 import pagedkv as pk
             pk.copy_blocks(step.k_cache, step.v_cache, step.desc, d["pairs"])
         step.append(k=d["k"], v=d["v"], slots=d["slots"])
-        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"])
+        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"], k=d["k"], v=d["v"], slots=d["slots"])
         out_h.copy_(step.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -379,6 +380,8 @@ def run_ours(args, rank, world, local_rank):
     # credit L2 hits or skipped re-reads as HBM bandwidth).
     shared = nbytes["unique_kv"] < nbytes["kv"]
     roof_bytes = nbytes["decode_unique"] if shared else nbytes["decode"]
+    if step.fused:  # the timed decode launch also writes the step's new tokens
+        roof_bytes += nbytes["append"]
     achieved = roof_bytes / (dec_ms / 1e3) / 1e9
     kind = decode_kernel_kind(wl) if not args.cascade else "cascade"
     traffic = recorded_traffic(args.workload, kind)
@@ -411,16 +414,18 @@ def run_ours(args, rank, world, local_rank):
                                              f"inputs larger than L2 ({working_set / 2**20:.0f} MiB vs "
                                              f"{l2 / 2**20:.0f} MiB), no flush"),
             "parallelism": f"replicas x{world}",
-            "launch": "CUDA graph replay per step" if args.graph else "eager launches",
+            "launch": ("CUDA graph replay per step" if args.graph else "eager launches")
+                      + ("; append fused into the decode kernel" if step.fused else ""),
         },
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": {"tensor_core": "decode_mma_kernel (+ merge_kernel when split)",
-                                "cuda_core": "decode_kernel (+ merge_kernel when split)",
-                                "cascade": "cascade_prefix_kernel + decode kernel + merge_kernel"}[kind],
+                     "kernel": {"tensor_core": "decode_mma_kernel (+ merge when split)",
+                                "cuda_core": "decode_kernel (+ merge when split)",
+                                "cascade": "prefill_tc_kernel prefix pass + decode kernel + merge"}[kind]
+                               + (", with the step's append fused in" if step.fused else ""),
                      "kernel_sources_hash": kernel_hash(kind),
                      "mean_launch_us": round(dec_ms * 1e3, 2),
                      "algorithmic_bytes_per_launch": roof_bytes,
@@ -805,6 +810,8 @@ def main(argv=None):
                     help="time block swap to / from a pinned host pool instead of the decode step")
     ap.add_argument("--graph", action="store_true",
                     help="time steps as CUDA-graph replays (one launch per step)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="append with its own kernel before the decode (default: fused into the decode kernel)")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -233,6 +233,31 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
                                               int32_t partition_tokens, void* stream);
 
 /*
+ * One decode step's append and attention in one launch: the same result as
+ *   pkv_paged_kv_append(k_new, v_new, in_dtype, num_seqs, slot_mapping, ...)
+ *   followed by pkv_paged_attention_decode(q, ...),
+ * with one new token per batch row (row s of k_new / v_new, [num_seqs]
+ * [Hkv][head_size]; slot_mapping[s] < 0: row s appends nothing).  Each
+ * decode CTA that covers a row's last position (seq_lens[s] - 1) writes its
+ * KV head's part of that token before reading the pool, which saves the
+ * append kernel's launch and its pass over the slot rows.  slot_mapping[s]
+ * must be the slot of position seq_lens[s] - 1 in row s's block table (what
+ * the allocator's append returned); otherwise PKV_DEVERR_SLOT is set and
+ * nothing is written for that row.  in_dtype: the cache's 16-bit type, or
+ * f16 / bf16 for an fp8 cache (encoded as pkv_paged_kv_append does); an fp8
+ * input returns PKV_ERR_UNSUPPORTED.  Copy-on-write copies for the step
+ * (pkv_copy_blocks) must be enqueued before this call.  Other arguments,
+ * errors and workspace as for pkv_paged_attention_decode.
+ */
+pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
+                                             const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                             int32_t num_seqs, int32_t num_q_heads, void* k_cache, void* v_cache,
+                                             const pkv_cache_desc* desc, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                             int32_t max_seq_len, float scale, void* out, void* workspace,
+                                             size_t workspace_bytes, int32_t partition_tokens, void* stream);
+
+/*
  * Shared-prefix ("cascade") decode attention: the same function as
  * pkv_paged_attention_decode, computed so that blocks shared by a group of
  * sequences are read once per group rather than once per sequence.  Shared

@@ -188,12 +188,20 @@ extern "C" int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_hea
     return auto_partition(num_seqs, num_kv_heads, max_seq_len);
 }
 
-extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t num_seqs,
-                                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
-                                                 const pkv_cache_desc* d, const int32_t* block_tables,
-                                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                                 int32_t max_seq_len, float scale, void* out, void* workspace,
-                                                 size_t ws_bytes, int32_t partition_tokens, void* stream) {
+namespace {
+// The step's new tokens for the decode with a fused append (null: plain decode).
+struct FusedAppend {
+    const void* k;
+    const void* v;
+    int32_t in_dtype;
+    const int64_t* slots;  // [num_seqs]
+};
+
+pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
+                         const void* k_cache, const void* v_cache, const pkv_cache_desc* d,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                         int32_t max_seq_len, float scale, void* out, void* workspace, size_t ws_bytes,
+                         int32_t partition_tokens, void* stream, const FusedAppend* app) {
     // ---- validation (host, before any launch)
     if (!d || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
         partition_tokens < 0)
@@ -218,6 +226,15 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return PKV_ERR_INVALID;
+    if (app) {
+        if (!app->k || !app->v || !app->slots || !aligned16(app->k) || !aligned16(app->v) ||
+            (reinterpret_cast<uintptr_t>(app->slots) & 7u))
+            return PKV_ERR_INVALID;
+        if (app->in_dtype < PKV_F16 || app->in_dtype > PKV_FP8_E4M3) return PKV_ERR_INVALID;
+        const bool same16 = d->kv_dtype != PKV_FP8_E4M3 && app->in_dtype == d->kv_dtype;
+        const bool to_fp8 = d->kv_dtype == PKV_FP8_E4M3 && (app->in_dtype == PKV_BF16 || app->in_dtype == PKV_F16);
+        if (!same16 && !to_fp8) return PKV_ERR_UNSUPPORTED;
+    }
 
     const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len);
     const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
@@ -248,6 +265,14 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
     p.v_scale = d->kv_dtype == PKV_FP8_E4M3 ? d->v_scale : 1.f;
     p.err = err;
     if (need > 0) partials_layout(p, workspace);
+    if (app) {
+        p.k_new = app->k;
+        p.v_new = app->v;
+        p.slots = app->slots;
+        p.in_dtype = app->in_dtype;
+        p.k_enc_scale = d->k_scale;
+        p.v_enc_scale = d->v_scale;
+    }
 
     // Tensor-core kernel for grouped-query heads at head_size 128; CUDA
     // cores otherwise (one query row per KV head is not a dense tile).
@@ -288,6 +313,31 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
         if (e != cudaSuccess) return PKV_ERR_CUDA;
     }
     return PKV_OK;
+}
+}  // namespace
+
+extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t num_seqs,
+                                                 int32_t num_q_heads, const void* k_cache, const void* v_cache,
+                                                 const pkv_cache_desc* d, const int32_t* block_tables,
+                                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                                 int32_t max_seq_len, float scale, void* out, void* workspace,
+                                                 size_t ws_bytes, int32_t partition_tokens, void* stream) {
+    return decode_common(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, d, block_tables, max_blocks_per_seq,
+                         seq_lens, max_seq_len, scale, out, workspace, ws_bytes, partition_tokens, stream, nullptr);
+}
+
+extern "C" pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
+                                                        const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                                        int32_t num_seqs, int32_t num_q_heads, void* k_cache,
+                                                        void* v_cache, const pkv_cache_desc* d,
+                                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                        const int32_t* seq_lens, int32_t max_seq_len, float scale,
+                                                        void* out, void* workspace, size_t ws_bytes,
+                                                        int32_t partition_tokens, void* stream) {
+    const FusedAppend app{k_new, v_new, in_dtype, slot_mapping};
+    return decode_common(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, d, block_tables, max_blocks_per_seq,
+                         seq_lens, max_seq_len, scale, out, workspace, ws_bytes, partition_tokens, stream,
+                         num_seqs > 0 ? &app : nullptr);
 }
 
 extern "C" pkv_status pkv_get_device_error(uint32_t* flags, void* stream) {

@@ -12,7 +12,7 @@
 // contiguous Hkv*16*D-element run.  Threads move 16-byte vectors.
 #include <cstdint>
 
-#include "pkv_device.cuh"
+#include "pkv_append.cuh"
 
 namespace pkv {
 namespace {
@@ -76,21 +76,8 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const unsigned char* __
         const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
         const int64_t drow = (blk * Hkv + h) * kBlockSize + off;
         const uint4 x = __ldg(reinterpret_cast<const uint4*>(src + row * D * 2) + c);
-        float f[8];
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        Unpack<IT, 8>::run(w, f);
-        uint32_t out[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float2 pr = make_float2(__fdiv_rn(f[4 * j + 2 * e], sc), __fdiv_rn(f[4 * j + 2 * e + 1], sc));
-                const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(pr, __NV_SATFINITE, __NV_E4M3);
-                word |= static_cast<uint32_t>(c2) << (16 * e);
-            }
-            out[j] = word;
-        }
+        const uint2 out2 = encode_e4m3x8<IT>(x, sc);
+        const uint32_t out[2] = {out2.x, out2.y};
         *reinterpret_cast<uint2*>(dst + drow * D + c * 8) = make_uint2(out[0], out[1]);
     }
 }

@@ -34,6 +34,7 @@
 #include <cfloat>
 #include <cstdint>
 
+#include "pkv_append.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -118,6 +119,10 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     const int j0 = t0 / kBlockSize;
     const int nblk = (t1 + kBlockSize - 1) / kBlockSize - j0;
     const int nb_w = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
+    // fused append: the warp that streams the partition's last block writes
+    // the new token's row just before copying that block
+    const bool append_here = p.slots && t1 == L && !bad && nblk > 0 && warp == (nblk - 1) % NW;
+    const FusedRow frow = fused_prefetch(p, s, h, L, append_here);
 
     unsigned char* wbase = smem + warp * NST * STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOffset) + warp * NST;
@@ -146,6 +151,10 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
         }
         const int phys = __shfl_sync(kFull, tbl, k_issue & 31);
         const int stage = k_issue % NST;
+        if (append_here && k_issue == nb_w - 1) {
+            fused_commit<KT>(p, frow);
+            __syncwarp();
+        }
         if (lane == 0) {
             stage_phys[stage] = phys;
             if (phys >= 0 && phys < p.NB) {

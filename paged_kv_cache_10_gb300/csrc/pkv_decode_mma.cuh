@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     const int j0 = t0 / kBlockSize;
     const int nblk = (t1 + kBlockSize - 1) / kBlockSize - j0;
     const int nb_w = warp < nblk ? (nblk - warp + NW - 1) / NW : 0;
+    // fused append: the warp that streams the partition's last block writes
+    // the new token's row just before copying that block
+    const bool append_here = p.slots && t1 == L && !bad && nblk > 0 && warp == (nblk - 1) % NW;
+    const FusedRow frow = fused_prefetch(p, s, h, L, append_here);
 
     unsigned char* wbase = smem + warp * NST * STAGE;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBarOffset) + warp * NST;
@@ -212,6 +216,10 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
         }
         const int phys = __shfl_sync(kFull, tbl, k_issue & 31);
         const int stage = k_issue % NST;
+        if (append_here && k_issue == nb_w - 1) {
+            fused_commit<KT>(p, frow);
+            __syncwarp();
+        }
         if (lane == 0) {
             fence_proxy_async_smem();  // generic writes to this stage (row zeroing) before the TMA
             stage_phys[stage] = phys;

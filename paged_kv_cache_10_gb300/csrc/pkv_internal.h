@@ -43,6 +43,14 @@ struct DecodeParams {
     const int32_t* group_blocks = nullptr;
     int32_t part_base = 0;
     int32_t cascade = 0;
+    // Fused append (pkv_paged_attention_decode_append): one new token per
+    // batch row, slots[s] < 0 for none.  All null for plain decode.
+    const void* k_new = nullptr;  // [S][Hkv][D], in_dtype
+    const void* v_new = nullptr;
+    const int64_t* slots = nullptr;
+    int32_t in_dtype = 0;
+    float k_enc_scale = 1.f;  // fp8 caches: code = e4m3(x / scale)
+    float v_enc_scale = 1.f;
 };
 
 // First token of a sequence's own (non-shared) attention range, clamped

@@ -35,7 +35,7 @@ EXPORTED = [
     "pkv_alloc_prefix_groups", "pkv_swap_blocks", "pkv_alloc_swap_out", "pkv_alloc_swap_in",
     "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
-    "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache",
+    "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
 ]
 
 
@@ -120,6 +120,8 @@ def lib():
         "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_append_tokens": (i32, [P, P, P, i32, P, i64, P, i32, P]),
+        "pkv_paged_attention_decode_append": (i32, [P, P, i32, P, P, i32, i32, i32, P, P, D, P, i32, P, i32,
+                                                    ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
         "pkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, P, i32, P, i32]),
         "pkv_prefix_block_hashes": (i32, [P, i64, i32, P, i32, P, P, i64, P]),
         "pkv_alloc_lookup": (i32, [P, P, i32]),
@@ -299,6 +301,25 @@ class PrefixGroups:
     @property
     def num_groups(self) -> int:
         return int(self.group_blocks.shape[0])
+
+
+def paged_attention_decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cache, desc: CacheDesc, block_tables,
+                                  seq_lens, max_seq_len: int, scale: float, out, workspace=None,
+                                  partition_tokens: int = 0, q_dtype: str | None = None, in_dtype: str | None = None,
+                                  stream=None) -> None:
+    """Append (one token per batch row, slot_mapping int64 [S]) and decode in one launch."""
+    S, Hq = int(q.shape[0]), int(q.shape[1])
+    if slot_mapping.dtype != torch.int64 or int(slot_mapping.shape[0]) != S:
+        raise ValueError("slot_mapping must be int64 with one entry per batch row")
+    ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pkv_paged_attention_decode_append(
+        _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), _dtype_code(k_new, in_dtype),
+        _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
+        _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
+        _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
+        int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes, int(partition_tokens), _stream(stream))
+    _check(st, "paged_attention_decode_append")
 
 
 def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_tables, seq_lens, max_seq_len: int,

@@ -4,8 +4,10 @@ Host side (C++ allocator): ``append_batch`` reserves one slot per sequence
 (copy-on-write pairs where a sequence writes into a shared partial block),
 ``export`` writes the padded block tables and lengths.  Device side, in
 stream order: ``copy_blocks`` (only when there are pairs) ->
-``paged_kv_append`` -> ``paged_attention_decode`` (+ its merge kernel when a
-sequence spans several partitions).
+``paged_attention_decode_append`` (the decode kernel writes the new tokens'
+K/V itself; + its merge kernel when a sequence spans several partitions).
+With ``fused=False`` (or for cascade decode) the append is its own kernel,
+``paged_kv_append``, before the decode.
 
 Re-running the device part is idempotent (the same slots get the same
 values, the same copies are made), which is what timing loops rely on.
@@ -30,7 +32,7 @@ class DecodeStep:
     """Device state and launch sequence of one workload's decode step."""
 
     def __init__(self, wl, device="cuda", partition_tokens=None, alloc: pk.Allocator | None = None,
-                 cascade: bool = False, cascade_min_blocks: int = 16):
+                 cascade: bool = False, cascade_min_blocks: int = 16, fused: bool = True):
         self.wl = wl
         self.device = torch.device(device)
         self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.kv_dtype,
@@ -59,6 +61,7 @@ class DecodeStep:
         self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
         self.out = torch.empty((wl.S, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
         self.cascade = cascade
+        self.fused = fused and not cascade
         if cascade:
             # groups of rows sharing leading blocks (host), decoded with one
             # pass over each shared prefix
@@ -82,7 +85,7 @@ class DecodeStep:
 
     def kernel_launches(self) -> int:
         """Number of kernels one ``run`` enqueues."""
-        n = 2  # append + decode
+        n = 1 if self.fused else 2  # (append +) decode
         if len(self.pairs):
             n += 1
         if self.cascade:
@@ -99,11 +102,22 @@ class DecodeStep:
             pk.copy_blocks(self.k_cache, self.v_cache, self.desc, self.d_pairs, stream=stream)
 
     def append(self, stream=None, k=None, v=None, slots=None):
+        if self.fused:
+            return  # done by decode()
         pk.paged_kv_append(self.k_new if k is None else k, self.v_new if v is None else v,
                            self.d_slots if slots is None else slots, self.k_cache, self.v_cache, self.desc,
                            in_dtype=self.wl.in_dtype, stream=stream)
 
-    def decode(self, stream=None, q=None, tables=None, lens=None, out=None):
+    def decode(self, stream=None, q=None, tables=None, lens=None, out=None, k=None, v=None, slots=None):
+        if self.fused:
+            pk.paged_attention_decode_append(
+                self.k_new if k is None else k, self.v_new if v is None else v, self.d_slots if slots is None else slots,
+                self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
+                self.d_tables if tables is None else tables, self.d_lens if lens is None else lens, self.max_seq_len,
+                self.wl.scale, self.out if out is None else out, workspace=self.workspace,
+                partition_tokens=self.partition_tokens, q_dtype=self.wl.q_dtype, in_dtype=self.wl.in_dtype,
+                stream=stream)
+            return
         if self.cascade:
             g = self.groups
             pk.paged_attention_decode_cascade(

@@ -23,9 +23,9 @@ def lib():
     return pagedkv
 
 
-def run(wl, partition=None):
+def run(wl, partition=None, fused=True):
     from paged_kv_cache_10_gb300.step import DecodeStep
-    st = DecodeStep(wl, device="cuda", partition_tokens=partition)
+    st = DecodeStep(wl, device="cuda", partition_tokens=partition, fused=fused)
     st.run()
     torch.cuda.synchronize()
     return st
@@ -191,7 +191,7 @@ def test_device_errors_are_reported_not_trapped(lib):
     assert lib.get_device_error() & lib.DEVERR_SEQ_LEN
     # a slot outside the pool; -1 is padding and silent
     slots = torch.tensor([wl.NB * 16 + 3, -1], dtype=torch.int64, device="cuda")
-    st.append(slots=slots)
+    lib.paged_kv_append(st.k_new, st.v_new, slots, st.k_cache, st.v_cache, st.desc, in_dtype="bf16")
     assert lib.get_device_error() == lib.DEVERR_SLOT
     # a copy pair outside the pool
     pairs = torch.tensor([[0, wl.NB]], dtype=torch.int32, device="cuda")
@@ -302,3 +302,41 @@ def test_swap_rejects_unpinned_host_memory(lib):
     with pytest.raises(ValueError):
         lib.swap_blocks(st.k_cache, st.v_cache, st.desc, k_host, k_host,
                         torch.zeros((1, 2), dtype=torch.int32, device="cuda"), lib.SWAP_OUT)
+
+
+@pytest.mark.parametrize("kv,qd,D,G", [("f16", "f16", 64, 1), ("bf16", "bf16", 128, 4), ("e4m3", "bf16", 128, 8),
+                                       ("e4m3", "f16", 64, 2)])
+def test_separate_append_kernel_matches_oracle(lib, kv, qd, D, G):
+    """The step with the append as its own kernel (the fused path is the
+    default everywhere else): pools bit for bit, attention within tolerance."""
+    from paged_kv_cache_10_gb300 import workloads
+    Hkv = 2
+    wl = workloads.custom(f"unfused_{kv}_{D}_{G}", 40 + G, EDGE_LENS, Hkv * G, Hkv, D, kv_dtype=kv, q_dtype=qd)
+    st = run(wl, fused=False)
+    assert lib.get_device_error() == 0
+    err, mx = check_step(st)
+    assert err <= TOL[kv], (err, mx)
+
+
+def test_fused_append_rejects_a_slot_off_the_last_position(lib):
+    """A slot that is not the block table's slot of position seq_len - 1 is
+    flagged and not written; the other rows are unaffected."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.custom("fused_bad_slot", 77, [20, 40, 9], 8, 2, 128, kv_dtype="bf16")
+    st = DecodeStep(wl, device="cuda")
+    k_before = st.k_cache.clone()
+    bad = st.d_slots.clone()
+    bad[1] = bad[1] + 1  # next offset in the same block: not position L - 1
+    lib.paged_attention_decode_append(st.k_new, st.v_new, bad, st.q, st.k_cache, st.v_cache, st.desc, st.d_tables,
+                                      st.d_lens, st.max_seq_len, wl.scale, st.out, workspace=st.workspace,
+                                      q_dtype="bf16", in_dtype="bf16")
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_SLOT
+    # row 1's slot (and the wrong one) untouched, rows 0 and 2 written
+    b, o = int(bad[1]) // 16, int(bad[1]) % 16
+    assert torch.equal(st.k_cache[b, :, o], k_before[b, :, o])
+    b1, o1 = int(st.d_slots[1]) // 16, int(st.d_slots[1]) % 16
+    assert torch.equal(st.k_cache[b1, :, o1], k_before[b1, :, o1])
+    b0, o0 = int(st.d_slots[0]) // 16, int(st.d_slots[0]) % 16
+    assert torch.equal(st.k_cache[b0, :, o0], st.k_new[0])
