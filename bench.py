@@ -328,9 +328,11 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public API from pinned host buffers
     h = {
         "q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(), "v": step.v_new.cpu().pin_memory(),
-        "slots": step.d_slots.cpu().pin_memory(), "pairs": step.d_pairs.cpu().pin_memory(),
-        "tables": step.d_tables.cpu().pin_memory(), "lens": step.d_lens.cpu().pin_memory(),
+        "slots": step.d_slots.cpu().pin_memory(), "tables": step.d_tables.cpu().pin_memory(),
+        "lens": step.d_lens.cpu().pin_memory(),
     }
+    if len(step.pairs):  # the step's copy-on-write: per-row sources (fused) or the pair list
+        h["cow"] = (step.d_cow_src if step.fused else step.d_pairs).cpu().pin_memory()
     d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
@@ -345,11 +347,12 @@ def run_ours(args, rank, world, local_rank):
             flush_buf.zero_()
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
-        if len(step.pairs):
+        if len(step.pairs) and not step.fused:
             from paged_kv_cache_10_gb300 import pagedkv as pk
-            pk.copy_blocks(step.k_cache, step.v_cache, step.desc, d["pairs"])
+            pk.copy_blocks(step.k_cache, step.v_cache, step.desc, d["cow"])
         step.append(k=d["k"], v=d["v"], slots=d["slots"])
-        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"], k=d["k"], v=d["v"], slots=d["slots"])
+        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"], k=d["k"], v=d["v"], slots=d["slots"],
+                    cow_src=d["cow"] if (len(step.pairs) and step.fused) else None)
         out_h.copy_(step.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -380,8 +383,8 @@ def run_ours(args, rank, world, local_rank):
     # credit L2 hits or skipped re-reads as HBM bandwidth).
     shared = nbytes["unique_kv"] < nbytes["kv"]
     roof_bytes = nbytes["decode_unique"] if shared else nbytes["decode"]
-    if step.fused:  # the timed decode launch also writes the step's new tokens
-        roof_bytes += nbytes["append"]
+    if step.fused:  # the timed decode launch also writes the step's new tokens and copy-on-write copies
+        roof_bytes += nbytes["append"] + nbytes["copy"]
     achieved = roof_bytes / (dec_ms / 1e3) / 1e9
     kind = decode_kernel_kind(wl) if not args.cascade else "cascade"
     traffic = recorded_traffic(args.workload, kind)

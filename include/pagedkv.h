@@ -233,9 +233,11 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
                                               int32_t partition_tokens, void* stream);
 
 /*
- * One decode step's append and attention in one launch: the same result as
- *   pkv_paged_kv_append(k_new, v_new, in_dtype, num_seqs, slot_mapping, ...)
- *   followed by pkv_paged_attention_decode(q, ...),
+ * One decode step's copy-on-write copies, append and attention in one
+ * launch: the same result as
+ *   pkv_copy_blocks(pairs (cow_src[s], the block of slot_mapping[s]) ...),
+ *   pkv_paged_kv_append(k_new, v_new, in_dtype, num_seqs, slot_mapping, ...),
+ *   pkv_paged_attention_decode(q, ...),
  * with one new token per batch row (row s of k_new / v_new, [num_seqs]
  * [Hkv][head_size]; slot_mapping[s] < 0: row s appends nothing).  Each
  * decode CTA that covers a row's last position (seq_lens[s] - 1) writes its
@@ -245,12 +247,21 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
  * the allocator's append returned); otherwise PKV_DEVERR_SLOT is set and
  * nothing is written for that row.  in_dtype: the cache's 16-bit type, or
  * f16 / bf16 for an fp8 cache (encoded as pkv_paged_kv_append does); an fp8
- * input returns PKV_ERR_UNSUPPORTED.  Copy-on-write copies for the step
- * (pkv_copy_blocks) must be enqueued before this call.  Other arguments,
- * errors and workspace as for pkv_paged_attention_decode.
+ * input returns PKV_ERR_UNSUPPORTED.
+ * cow_src (device int32 [num_seqs], may be NULL): for a row whose append
+ *   took a fresh copy of a shared partial block (the allocator's copy-on-
+ *   write pair (src, dst) with dst the block of slot_mapping[s]), src; else
+ *   -1.  The CTA copies its head's tile of src into dst, except the appended
+ *   row, before writing the row (other sharers write only that row of src,
+ *   in place).  An src outside the pool, or equal to dst, sets
+ *   PKV_DEVERR_COPY_PAIR and nothing is written for the row.  Other
+ *   copy-on-write pairs (not into an appending row's last block) must be
+ *   copied with pkv_copy_blocks first.  Other arguments, errors and
+ *   workspace as for pkv_paged_attention_decode.
  */
 pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
-                                             const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                             const int64_t* slot_mapping, const int32_t* cow_src,
+                                             const void* q, int32_t q_dtype,
                                              int32_t num_seqs, int32_t num_q_heads, void* k_cache, void* v_cache,
                                              const pkv_cache_desc* desc, const int32_t* block_tables,
                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,

@@ -194,7 +194,8 @@ struct FusedAppend {
     const void* k;
     const void* v;
     int32_t in_dtype;
-    const int64_t* slots;  // [num_seqs]
+    const int64_t* slots;    // [num_seqs]
+    const int32_t* cow_src;  // [num_seqs] or null
 };
 
 pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads,
@@ -228,7 +229,7 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
         return PKV_ERR_INVALID;
     if (app) {
         if (!app->k || !app->v || !app->slots || !aligned16(app->k) || !aligned16(app->v) ||
-            (reinterpret_cast<uintptr_t>(app->slots) & 7u))
+            (reinterpret_cast<uintptr_t>(app->slots) & 7u) || (reinterpret_cast<uintptr_t>(app->cow_src) & 3u))
             return PKV_ERR_INVALID;
         if (app->in_dtype < PKV_F16 || app->in_dtype > PKV_FP8_E4M3) return PKV_ERR_INVALID;
         const bool same16 = d->kv_dtype != PKV_FP8_E4M3 && app->in_dtype == d->kv_dtype;
@@ -269,6 +270,7 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
         p.k_new = app->k;
         p.v_new = app->v;
         p.slots = app->slots;
+        p.cow_src = app->cow_src;
         p.in_dtype = app->in_dtype;
         p.k_enc_scale = d->k_scale;
         p.v_enc_scale = d->v_scale;
@@ -327,14 +329,15 @@ extern "C" pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype,
 }
 
 extern "C" pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
-                                                        const int64_t* slot_mapping, const void* q, int32_t q_dtype,
+                                                        const int64_t* slot_mapping, const int32_t* cow_src,
+                                                        const void* q, int32_t q_dtype,
                                                         int32_t num_seqs, int32_t num_q_heads, void* k_cache,
                                                         void* v_cache, const pkv_cache_desc* d,
                                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                                                         const int32_t* seq_lens, int32_t max_seq_len, float scale,
                                                         void* out, void* workspace, size_t ws_bytes,
                                                         int32_t partition_tokens, void* stream) {
-    const FusedAppend app{k_new, v_new, in_dtype, slot_mapping};
+    const FusedAppend app{k_new, v_new, in_dtype, slot_mapping, cow_src};
     return decode_common(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, d, block_tables, max_blocks_per_seq,
                          seq_lens, max_seq_len, scale, out, workspace, ws_bytes, partition_tokens, stream,
                          num_seqs > 0 ? &app : nullptr);

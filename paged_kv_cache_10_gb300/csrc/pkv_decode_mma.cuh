@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
         const int phys = __shfl_sync(kFull, tbl, k_issue & 31);
         const int stage = k_issue % NST;
         if (append_here && k_issue == nb_w - 1) {
-            fused_commit<KT>(p, frow);
+            fused_commit<KT>(p, h, frow);
             __syncwarp();
         }
         if (lane == 0) {

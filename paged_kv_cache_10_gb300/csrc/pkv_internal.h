@@ -48,6 +48,7 @@ struct DecodeParams {
     const void* k_new = nullptr;  // [S][Hkv][D], in_dtype
     const void* v_new = nullptr;
     const int64_t* slots = nullptr;
+    const int32_t* cow_src = nullptr;  // [S]: block copied into the row's last block first, or -1
     int32_t in_dtype = 0;
     float k_enc_scale = 1.f;  // fp8 caches: code = e4m3(x / scale)
     float v_enc_scale = 1.f;

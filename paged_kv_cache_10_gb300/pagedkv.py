@@ -120,7 +120,7 @@ def lib():
         "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_append_tokens": (i32, [P, P, P, i32, P, i64, P, i32, P]),
-        "pkv_paged_attention_decode_append": (i32, [P, P, i32, P, P, i32, i32, i32, P, P, D, P, i32, P, i32,
+        "pkv_paged_attention_decode_append": (i32, [P, P, i32, P, P, P, i32, i32, i32, P, P, D, P, i32, P, i32,
                                                     ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
         "pkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, P, i32, P, i32]),
         "pkv_prefix_block_hashes": (i32, [P, i64, i32, P, i32, P, P, i64, P]),
@@ -306,16 +306,21 @@ class PrefixGroups:
 def paged_attention_decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cache, desc: CacheDesc, block_tables,
                                   seq_lens, max_seq_len: int, scale: float, out, workspace=None,
                                   partition_tokens: int = 0, q_dtype: str | None = None, in_dtype: str | None = None,
-                                  stream=None) -> None:
-    """Append (one token per batch row, slot_mapping int64 [S]) and decode in one launch."""
+                                  cow_src=None, stream=None) -> None:
+    """Copy-on-write copies into the appending rows' last blocks (cow_src
+    int32 [S], -1 for none), append (one token per batch row, slot_mapping
+    int64 [S]) and decode, in one launch."""
     S, Hq = int(q.shape[0]), int(q.shape[1])
     if slot_mapping.dtype != torch.int64 or int(slot_mapping.shape[0]) != S:
         raise ValueError("slot_mapping must be int64 with one entry per batch row")
+    if cow_src is not None and (cow_src.dtype != torch.int32 or int(cow_src.shape[0]) != S):
+        raise ValueError("cow_src must be int32 with one entry per batch row")
     ws_ptr = _dev_ptr(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().pkv_paged_attention_decode_append(
         _dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), _dtype_code(k_new, in_dtype),
-        _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
+        _dev_ptr(slot_mapping, "slot_mapping"), _dev_ptr(cow_src, "cow_src") if cow_src is not None else None,
+        _dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
         _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
         int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes, int(partition_tokens), _stream(stream))

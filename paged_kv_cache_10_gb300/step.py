@@ -4,8 +4,9 @@ Host side (C++ allocator): ``append_batch`` reserves one slot per sequence
 (copy-on-write pairs where a sequence writes into a shared partial block),
 ``export`` writes the padded block tables and lengths.  Device side, in
 stream order: ``copy_blocks`` (only when there are pairs) ->
-``paged_attention_decode_append`` (the decode kernel writes the new tokens'
-K/V itself; + its merge kernel when a sequence spans several partitions).
+``paged_attention_decode_append`` (the decode kernel makes the copy-on-write
+copies and writes the new tokens' K/V itself; + its merge kernel when a
+sequence spans several partitions).
 With ``fused=False`` (or for cascade decode) the append is its own kernel,
 ``paged_kv_append``, before the decode.
 
@@ -57,6 +58,15 @@ class DecodeStep:
         self.v_new = _to_dev(wl.v_new, dev)
         self.d_slots = torch.from_numpy(self.slots).to(dev)
         self.d_pairs = torch.from_numpy(np.ascontiguousarray(self.pairs)).to(dev)
+        # per batch row: the copy-on-write source of its last block (the
+        # pair whose destination is the block its new token goes to), or -1
+        cow = np.full(wl.S, -1, np.int32)
+        if len(self.pairs):
+            dst_row = {int(self.slots[r]) // wl.b: r for r in range(wl.S) if self.slots[r] >= 0}
+            for src, dst in np.asarray(self.pairs).reshape(-1, 2):
+                cow[dst_row[int(dst)]] = src
+        self.cow_src = cow
+        self.d_cow_src = torch.from_numpy(cow).to(dev)
         self.d_tables = torch.from_numpy(self.tables).to(dev)
         self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
         self.out = torch.empty((wl.S, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
@@ -86,7 +96,7 @@ class DecodeStep:
     def kernel_launches(self) -> int:
         """Number of kernels one ``run`` enqueues."""
         n = 1 if self.fused else 2  # (append +) decode
-        if len(self.pairs):
+        if len(self.pairs) and not self.fused:
             n += 1
         if self.cascade:
             n += 1 + (1 if self.groups.num_groups else 0)  # merge, prefix
@@ -98,7 +108,7 @@ class DecodeStep:
 
     # -- device work (stream order)
     def copy(self, stream=None):
-        if len(self.pairs):
+        if len(self.pairs) and not self.fused:  # the fused decode copies itself
             pk.copy_blocks(self.k_cache, self.v_cache, self.desc, self.d_pairs, stream=stream)
 
     def append(self, stream=None, k=None, v=None, slots=None):
@@ -108,7 +118,8 @@ class DecodeStep:
                            self.d_slots if slots is None else slots, self.k_cache, self.v_cache, self.desc,
                            in_dtype=self.wl.in_dtype, stream=stream)
 
-    def decode(self, stream=None, q=None, tables=None, lens=None, out=None, k=None, v=None, slots=None):
+    def decode(self, stream=None, q=None, tables=None, lens=None, out=None, k=None, v=None, slots=None,
+               cow_src=None):
         if self.fused:
             pk.paged_attention_decode_append(
                 self.k_new if k is None else k, self.v_new if v is None else v, self.d_slots if slots is None else slots,
@@ -116,7 +127,7 @@ class DecodeStep:
                 self.d_tables if tables is None else tables, self.d_lens if lens is None else lens, self.max_seq_len,
                 self.wl.scale, self.out if out is None else out, workspace=self.workspace,
                 partition_tokens=self.partition_tokens, q_dtype=self.wl.q_dtype, in_dtype=self.wl.in_dtype,
-                stream=stream)
+                cow_src=(self.d_cow_src if cow_src is None else cow_src) if len(self.pairs) else None, stream=stream)
             return
         if self.cascade:
             g = self.groups

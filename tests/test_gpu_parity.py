@@ -340,3 +340,25 @@ def test_fused_append_rejects_a_slot_off_the_last_position(lib):
     assert torch.equal(st.k_cache[b1, :, o1], k_before[b1, :, o1])
     b0, o0 = int(st.d_slots[0]) // 16, int(st.d_slots[0]) % 16
     assert torch.equal(st.k_cache[b0, :, o0], st.k_new[0])
+
+
+def test_fused_copy_on_write_rejects_a_bad_source(lib):
+    """A copy-on-write source outside the pool is flagged and the row is not
+    written; the context stays usable."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.prefix_share(pairs=4, prefix=64)
+    st = DecodeStep(wl, device="cuda")
+    assert len(st.pairs) > 0
+    bad = st.d_cow_src.clone()
+    row = int(np.nonzero(st.cow_src >= 0)[0][0])
+    bad[row] = wl.NB + 1
+    st.decode(cow_src=bad)
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_COPY_PAIR
+    st2 = DecodeStep(wl, device="cuda")
+    st2.run()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    err, _ = check_step(st2)
+    assert err <= TOL["bf16"]
