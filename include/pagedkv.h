@@ -334,8 +334,8 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   PKV_DEVERR_SEQ_LEN and its rows past the bound may be left unwritten.
  * Rows of out outside every sequence's range are not written.
  * scale must be finite and > 0 (else PKV_ERR_INVALID).
- * Implemented for f16 / bf16 pools with q of the same type, head_size 128,
- * num_q_heads / num_kv_heads in {1, 2, 4, 8}; others return
+ * Implemented for f16 / bf16 pools with q of the same type, head_size 64 or
+ * 128, num_q_heads / num_kv_heads in {1, 2, 4, 8}; others return
  * PKV_ERR_UNSUPPORTED.  Inconsistent query_start / seq_lens (n_s < 0,
  * n_s > seq_lens[s], past num_tokens or the block table) set
  * PKV_DEVERR_SEQ_LEN and the sequence is skipped; a block id outside the pool

@@ -36,35 +36,42 @@
 namespace pkv {
 namespace {
 
-constexpr int kPD = 128;        // head_size
 constexpr int kTileM = 128;     // query rows per Q tile (two Q tiles per CTA)
 constexpr int kTileN = 128;     // keys per tile
 constexpr int kKStages = 3;     // key ring depth
 constexpr int kVStages = 2;     // value ring depth
-constexpr int kOpBytes = kTileM * kPD * 2;  // one 128 x 128 16-bit operand (32 KB)
-constexpr int kHalfBytes = kOpBytes / 2;    // one 64-column block
+constexpr int kColBlock = kTileM * 128;  // one 64-column block of a 128-row 16-bit operand (16 KB)
 constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
 // Three warpgroups: warps 0-3 load (0: Q and keys, 2: values), issue the
 // MMAs (1) or idle (3); warps 4-7 run the softmax of Q tile A, warps 8-11 of
 // Q tile B.  setmaxnreg moves registers from the first to the other two:
-// 128 x 72 + 256 x 208 <= 384 x 168, the launch's allocation.
+// 128 x 88 + 256 x 208 = 384 x 168, the launch's allocation.
 constexpr int kThreads = 384;
-constexpr int kLoadRegs = 72;
+constexpr int kLoadRegs = 88;
 constexpr int kSoftmaxRegs = 208;
 static_assert(128 * kLoadRegs + 256 * kSoftmaxRegs <= kThreads * (65536 / kThreads / 8 * 8), "register split");
 constexpr int kSoftmaxWarps = 4;  // per Q tile
 constexpr float kRebase = 8.0f;   // log2 units
 
-constexpr int kOffQ = 0;                               // Q tiles A, B
-constexpr int kOffK = kOffQ + 2 * kOpBytes;
-constexpr int kOffV = kOffK + kKStages * kOpBytes;
-constexpr int kOffBar = kOffV + kVStages * kOpBytes;
 // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], v_zero, s_full[2 tiles], p_full[2 tiles],
 // o_done[2 tiles], drain
 constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 1 + 2 + 2 + 2 + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+// Shared-memory layout for head_size D (64 or 128): operands are 128 rows x
+// D 16-bit elements in D / 64 column blocks of 128-byte rows.
+template <int D>
+struct Tile {
+    static_assert(D == 64 || D == 128, "head_size");
+    static constexpr int kDB = D / 64;          // 64-column blocks per row
+    static constexpr int kOp = kTileM * D * 2;  // one 128 x D operand
+    static constexpr int kOffQ = 0;             // Q tiles A, B
+    static constexpr int kOffK = kOffQ + 2 * kOp;
+    static constexpr int kOffV = kOffK + kKStages * kOp;
+    static constexpr int kOffBar = kOffV + kVStages * kOp;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 
 struct PrefillParams {
     const int32_t* query_start;  // [S + 1]
@@ -154,14 +161,17 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 // kPrefix = true: the cascade decode's shared-prefix pass; Q tile X holds
 // 128 / G members x G heads of one (group, KV head); keys = one 512-token
 // partition of the group's shared blocks (no causal mask); split-K partials.
-template <typename T, bool kPrefix>
+template <typename T, int D, bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBF = std::is_same<T, BF16>::value;
+    using TL = Tile<D>;
+    constexpr int kOffQ = TL::kOffQ, kOffK = TL::kOffK, kOffV = TL::kOffV, kOffMisc = TL::kOffMisc;
+    constexpr int kOpBytes = TL::kOp, kDB = TL::kDB;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-    uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + TL::kOffBar);
     uint64_t* k_full = q_full + 1;           // [kKStages]
     uint64_t* k_empty = k_full + kKStages;   // [kKStages]
     uint64_t* v_full = k_empty + kKStages;   // [kVStages]
@@ -237,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + r % G) * p.NP + pp;
                 p.part_m[prow] = -INFINITY;
                 p.part_l[prow] = 0.f;
-                float4* po = reinterpret_cast<float4*>(p.part_o + prow * kPD);
-                for (int d4 = 0; d4 < kPD / 4; ++d4) po[d4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+                for (int d4 = 0; d4 < D / 4; ++d4) po[d4] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             return;
         }
@@ -313,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(q_full, ntiles * kOpBytes);
                     for (int X = 0; X < ntiles; ++X)
-                        for (int dh = 0; dh < 2; ++dh)
-                            tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kHalfBytes, &tmq, dh * 64, h * G,
+                        for (int dh = 0; dh < kDB; ++dh)
+                            tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kColBlock, &tmq, dh * 64, h * G,
                                             q0 + t0 + X * RQ, q_full, pol_q);
                 }
             } else {
@@ -341,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         b = seq0;
                     }
                     const int X = mi / RQ, mx = mi - X * RQ;
-                    for (int dh = 0; dh < 2; ++dh)
-                        tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kHalfBytes + mx * G * 128, &tmq, dh * 64,
+                    for (int dh = 0; dh < kDB; ++dh)
+                        tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kColBlock + mx * G * 128, &tmq, dh * 64,
                                         h * G, b, q_full, pol_q);
                 }
             }
@@ -372,12 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (!warp_all(*abort_flag == 0)) break;  // uniform across the warp
-            if (lane == 0) mbar_arrive_expect_tx(full + st, nb_tile * 2 * kBlockTileBytes);
+            if (lane == 0) mbar_arrive_expect_tx(full + st, nb_tile * kDB * kBlockTileBytes);
             __syncwarp();
             if (lane < nb_tile) {
                 unsigned char* d = ring + st * kOpBytes + lane * kBlockTileBytes;
-                tc::tma_load_2d(d, map, 0, row, full + st, pol_kv);
-                tc::tma_load_2d(d + kHalfBytes, map, 64, row, full + st, pol_kv);
+                for (int dh = 0; dh < kDB; ++dh) tc::tma_load_2d(d + dh * kColBlock, map, dh * 64, row, full + st, pol_kv);
             }
             issued = j + 1;
             if (!is_k && j == nkt - 1) {
@@ -391,9 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     okv = warp_all(mbar_wait(v_full + st, (j / nst) & 1));
                     if (okv) {
                         unsigned char* vb = sm + kOffV + st * kOpBytes;
-                        for (int idx = lane; idx < (kTileN - r0) * 16; idx += 32) {
-                            const int r = r0 + (idx >> 4), c = idx & 15;
-                            *reinterpret_cast<uint4*>(vb + (c >> 3) * kHalfBytes + swz128(r, c & 7)) =
+                        constexpr int kRowChunks = D / 8;  // 16-byte chunks of a row
+                        for (int idx = lane; idx < (kTileN - r0) * kRowChunks; idx += 32) {
+                            const int r = r0 + idx / kRowChunks, c = idx % kRowChunks;
+                            *reinterpret_cast<uint4*>(vb + (c >> 3) * kColBlock + swz128(r, c & 7)) =
                                 make_uint4(0u, 0u, 0u, 0u);
                         }
                         fence_proxy_async_smem();
@@ -422,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the other.
         if (lane == 0) {
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
-            const uint32_t idO = tc::idesc_f16(kBF, kTileM, kPD, true);
+            const uint32_t idO = tc::idesc_f16(kBF, kTileM, D, true);
             bool ok = tc::wait_spin(q_full, 0);
             // Descriptors: bases per Q tile and ring stage, computed once; the
             // k-th 16-element step adds a constant (the start address field
@@ -434,16 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dK0 = tc::sdesc_sw128(smem_addr(sm + kOffK), 16, 1024);
             const uint64_t dK1 = tc::sdesc_sw128(smem_addr(sm + kOffK + kOpBytes), 16, 1024);
             const uint64_t dK2 = tc::sdesc_sw128(smem_addr(sm + kOffK + 2 * kOpBytes), 16, 1024);
-            const uint64_t dV0 = tc::sdesc_sw128(smem_addr(sm + kOffV), kHalfBytes, 1024);
-            const uint64_t dV1 = tc::sdesc_sw128(smem_addr(sm + kOffV + kOpBytes), kHalfBytes, 1024);
+            const uint64_t dV0 = tc::sdesc_sw128(smem_addr(sm + kOffV), kColBlock, 1024);
+            const uint64_t dV1 = tc::sdesc_sw128(smem_addr(sm + kOffV + kOpBytes), kColBlock, 1024);
             auto issue_s = [&](int X, int j) {
                 const int st = j % kKStages;
                 const uint64_t q = X ? dQ1 : dQ0;
                 const uint64_t k = st == 0 ? dK0 : (st == 1 ? dK1 : dK2);
                 const uint32_t d = tmem + X * kTileN;
 #pragma unroll
-                for (int kk = 0; kk < kPD / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kColBlock + (kk & 3) * 32) >> 4);
                     tc::mma_f16(d, q + off, k + off, idS, kk > 0);
                 }
                 tc::commit(s_full + X);
@@ -590,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j > 0 && __any_sync(0xffffffffu, rebase)) {
                 const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
                     tc::ld32(tO + q * 32, o);
                     tc::wait_ld();
@@ -616,9 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (!kPrefix) {
                 typename T::storage* orow =
                     reinterpret_cast<typename T::storage*>(p.out) +
-                    (static_cast<int64_t>(q0 + t0 + X * RQ + rq) * p.Hq + h * G + g) * kPD;
+                    (static_cast<int64_t>(q0 + t0 + X * RQ + rq) * p.Hq + h * G + g) * D;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
                     tc::ld32(tO + q * 32, o);
                     tc::wait_ld();
@@ -644,12 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.part_l[prow] = l;
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
                     tc::ld32(tO + q * 32, o);
                     tc::wait_ld();
                     if (b >= 0) {
-                        float4* po = reinterpret_cast<float4*>(p.part_o + prow * kPD + q * 32);
+                        float4* po = reinterpret_cast<float4*>(p.part_o + prow * D + q * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
                             po[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
@@ -673,9 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <typename T, bool kPrefix>
+template <typename T, int D, bool kPrefix>
 cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, cudaStream_t st) {
+    constexpr int kSmemBytes = Tile<D>::kSmemBytes;
     static std::once_flag once[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -683,18 +694,20 @@ cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     cudaError_t attr = cudaSuccess;
     std::call_once(once[dev], [&] {
-        attr = cudaFuncSetAttribute(prefill_tc_kernel<T, kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr = cudaFuncSetAttribute(prefill_tc_kernel<T, D, kPrefix>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     kSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
-    prefill_tc_kernel<T, kPrefix><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
+    prefill_tc_kernel<T, D, kPrefix><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           cudaStream_t st) {
-    return launch_tile<T, false>(p, dim3(p.num_qtiles, p.Hkv, p.S), tq, tk, tv, st);
+cudaError_t launch_prefill(const PrefillParams& p, int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t st) {
+    const dim3 grid(p.num_qtiles, p.Hkv, p.S);
+    return D == 64 ? launch_tile<T, 64, false>(p, grid, tq, tk, tv, st)
+                   : launch_tile<T, 128, false>(p, grid, tq, tk, tv, st);
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -726,8 +739,8 @@ cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, in
     p.NP = b.NP;
     p.row_chunks = cp.row_chunks;
     const dim3 grid(cp.npp, b.Hkv, num_groups * cp.row_chunks);
-    return kv_dtype == PKV_BF16 ? launch_tile<BF16, true>(p, grid, tq, tk, tv, st)
-                                : launch_tile<F16, true>(p, grid, tq, tk, tv, st);
+    return kv_dtype == PKV_BF16 ? launch_tile<BF16, 128, true>(p, grid, tq, tk, tv, st)
+                                : launch_tile<F16, 128, true>(p, grid, tq, tk, tv, st);
 }
 
 }  // namespace pkv
@@ -744,7 +757,8 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     if (desc->block_size != kBlockSize || desc->num_kv_heads <= 0 || desc->num_blocks <= 0) return PKV_ERR_INVALID;
     if (num_q_heads % desc->num_kv_heads) return PKV_ERR_INVALID;
     const int G = num_q_heads / desc->num_kv_heads;
-    if (desc->head_size != kPD || (G != 1 && G != 2 && G != 4 && G != 8)) return PKV_ERR_UNSUPPORTED;
+    const int D = desc->head_size;
+    if ((D != 64 && D != 128) || (G != 1 && G != 2 && G != 4 && G != 8)) return PKV_ERR_UNSUPPORTED;
     if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
     if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID;  // finite, > 0 (max on raw scores)
@@ -777,11 +791,11 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
 
     CUtensorMap tq, tk, tv;
     const int64_t pool_rows = static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize;
-    if (!encode_token_head_map(&tq, q, kPD, num_q_heads, num_tokens, G, kTileM / G) || !encode_pool_map(&tk, k_cache, 2, pool_rows, kPD) ||
-        !encode_pool_map(&tv, v_cache, 2, pool_rows, kPD))
+    if (!encode_token_head_map(&tq, q, D, num_q_heads, num_tokens, G, kTileM / G) ||
+        !encode_pool_map(&tk, k_cache, 2, pool_rows, D) || !encode_pool_map(&tv, v_cache, 2, pool_rows, D))
         return PKV_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = desc->kv_dtype == PKV_BF16 ? launch_prefill<BF16>(p, tq, tk, tv, st)
-                                                      : launch_prefill<F16>(p, tq, tk, tv, st);
+    const cudaError_t e = desc->kv_dtype == PKV_BF16 ? launch_prefill<BF16>(p, D, tq, tk, tv, st)
+                                                      : launch_prefill<F16>(p, D, tq, tk, tv, st);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

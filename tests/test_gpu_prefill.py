@@ -81,11 +81,12 @@ CASES = [
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("case", [0, 1])
-def test_prefill_matches_oracle_every_element(lib, dtype, G, case):
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_matches_oracle_every_element(lib, dtype, G, case, D):
     from paged_kv_cache_10_gb300 import workloads
     ctx, qlens = CASES[case]
     Hkv = 2
-    wl = workloads.prefill("prefill_small", 2000 + 10 * G + case, ctx, qlens, Hkv * G, Hkv, dtype=dtype)
+    wl = workloads.prefill("prefill_small", 2000 + 10 * G + case + D, ctx, qlens, Hkv * G, Hkv, D=D, dtype=dtype)
     st = run(wl)
     assert lib.get_device_error() == 0
     err, mx = check_full(st)
@@ -167,13 +168,13 @@ def test_prefill_rejects_bad_arguments(lib):
                                 bad_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
     torch.cuda.synchronize()
     assert lib.get_device_error() & lib.DEVERR_BLOCK_ID
-    # unsupported: q type differing from the pool, head_size 64
+    # unsupported: q type differing from the pool, head_size 96
     with pytest.raises(lib.PagedKVError):
         lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
                                     st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="f16")
-    d64 = lib.CacheDesc(num_blocks=wl.NB, num_kv_heads=2, head_size=64, kv_dtype="bf16")
+    d96 = lib.CacheDesc(num_blocks=wl.NB, num_kv_heads=2, head_size=96, kv_dtype="bf16")
     with pytest.raises(lib.PagedKVError):
-        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, d64, st.d_query_start, wl.max_query_len,
+        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, d96, st.d_query_start, wl.max_query_len,
                                     st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
     # the context is still usable and the correct call still matches
     st.attend()
