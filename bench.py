@@ -45,9 +45,11 @@ _CSRC = "paged_kv_cache_10_gb300/csrc/"
 # Sources of the decode kernel a workload runs (CUDA-core kernel for one
 # query head per KV head or head_size 64; tensor-core kernel for GQA at 128).
 KERNEL_SOURCES = {
-    "cuda_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh"],
-    "tensor_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh"],
+    "cuda_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_append.cuh"],
+    "tensor_core": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh",
+                    _CSRC + "pkv_append.cuh"],
     "cascade": [_CSRC + "pkv_decode_impl.cuh", _CSRC + "pkv_device.cuh", _CSRC + "pkv_decode_mma.cuh",
+                _CSRC + "pkv_append.cuh",
                 _CSRC + "pkv_cascade.cu", _CSRC + "pkv_prefill.cu", _CSRC + "pkv_tcgen05.cuh", _CSRC + "pkv_merge.cuh"],
     "prefill": [_CSRC + "pkv_prefill.cu", _CSRC + "pkv_tcgen05.cuh", _CSRC + "pkv_device.cuh",
                 _CSRC + "pkv_decode_mma.cuh"],

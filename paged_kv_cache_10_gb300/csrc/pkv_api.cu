@@ -29,28 +29,51 @@ unsigned int* error_word() {
     return ptrs[dev];
 }
 
+namespace {
+// Launches the merge as a programmatic dependent of the kernel before it on
+// the stream (the decode that wrote the partials): its CTAs may start while
+// that kernel's last CTAs run and wait in griddepcontrol.wait for its
+// completion, which hides the launch gap.  A driver that refuses the
+// attribute gets a plain launch.
+template <int D, typename QT, int WPR>
+cudaError_t launch_merge_t(const DecodeParams& p, int64_t rows, cudaStream_t st) {
+    constexpr int RPC = 8 / WPR;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + RPC - 1) / RPC));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<D, QT, WPR>, p);
+    if (e == cudaErrorNotSupported || e == cudaErrorInvalidValue) {
+        (void)cudaGetLastError();
+        merge_kernel<D, QT, WPR><<<cfg.gridDim, 256, 0, st>>>(p);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
+template <int D, typename QT>
+cudaError_t launch_merge_d(const DecodeParams& p, int64_t rows, cudaStream_t st) {
+    switch (merge_warps_per_row(p.NP)) {
+    case 1: return launch_merge_t<D, QT, 1>(p, rows, st);
+    case 2: return launch_merge_t<D, QT, 2>(p, rows, st);
+    case 4: return launch_merge_t<D, QT, 4>(p, rows, st);
+    default: return launch_merge_t<D, QT, 8>(p, rows, st);
+    }
+}
+}  // namespace
+
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st) {
     const int64_t rows = static_cast<int64_t>(p.S) * p.Hq;
-    if (p.NP <= kMergeNarrowMaxParts) {
-        const dim3 grid(static_cast<unsigned>((rows + 7) / 8));
-        if (q_dtype == PKV_BF16) {
-            if (p.D == 128) merge_warp_kernel<128, BF16><<<grid, 256, 0, st>>>(p);
-            else merge_warp_kernel<64, BF16><<<grid, 256, 0, st>>>(p);
-        } else {
-            if (p.D == 128) merge_warp_kernel<128, F16><<<grid, 256, 0, st>>>(p);
-            else merge_warp_kernel<64, F16><<<grid, 256, 0, st>>>(p);
-        }
-        return cudaGetLastError();
-    }
-    const dim3 grid(static_cast<unsigned>(rows));
-    if (q_dtype == PKV_BF16) {
-        if (p.D == 128) merge_kernel<128, BF16, 256><<<grid, 256, 0, st>>>(p);
-        else merge_kernel<64, BF16, 256><<<grid, 256, 0, st>>>(p);
-    } else {
-        if (p.D == 128) merge_kernel<128, F16, 256><<<grid, 256, 0, st>>>(p);
-        else merge_kernel<64, F16, 256><<<grid, 256, 0, st>>>(p);
-    }
-    return cudaGetLastError();
+    if (rows <= 0) return cudaSuccess;
+    if (q_dtype == PKV_BF16)
+        return p.D == 128 ? launch_merge_d<128, BF16>(p, rows, st) : launch_merge_d<64, BF16>(p, rows, st);
+    return p.D == 128 ? launch_merge_d<128, F16>(p, rows, st) : launch_merge_d<64, F16>(p, rows, st);
 }
 
 int num_sms() {

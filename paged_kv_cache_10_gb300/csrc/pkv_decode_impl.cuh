@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    allow_dependent_launch();  // the merge may stage its CTAs behind this grid's last wave
     const int hf = lane >> 4, li = lane & 15;
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
 

@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    allow_dependent_launch();  // the merge may stage its CTAs behind this grid's last wave
     const int g8 = lane >> 2, qd = lane & 3;  // fragment row group / quad member
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
 

@@ -176,4 +176,16 @@ __device__ __forceinline__ __half from_float<F16>(float x) { return __float2half
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_float<BF16>(float x) { return __float2bfloat16_rn(x); }
 
+// ------------------------------------------- programmatic dependent launch
+// Waits until the grid this launch programmatically depends on (the decode
+// kernel that wrote the partials) has completed and its writes are
+// visible; returns at once for a launch without that dependency.
+__device__ __forceinline__ void wait_primary_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the launch that programmatically depends on this grid start its
+// CTAs once every CTA of this grid has made this call (or exited).
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace pkv

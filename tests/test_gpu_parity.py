@@ -124,7 +124,9 @@ def test_zero_length_rows_and_padding_slots(lib):
     assert st.slots[0] == -1 and st.slots[2] == -1
 
 
-@pytest.mark.parametrize("P", [16, 48, 160, 0])
+# 2049 tokens in P-token partitions: 129 (three merge chunks of a warp), 43,
+# 26, 13 and 5 partitions, i.e. every warps-per-row choice of the merge
+@pytest.mark.parametrize("P", [16, 48, 80, 160, 512, 0])
 def test_split_and_unsplit_agree(lib, P):
     from paged_kv_cache_10_gb300 import workloads
     wl = workloads.custom("split", 11, [700, 1300, 64, 2049], 32, 8, 128, kv_dtype="bf16", partition_tokens=P)
