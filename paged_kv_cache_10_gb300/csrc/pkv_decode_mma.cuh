@@ -132,6 +132,7 @@ __device__ __forceinline__ uint32_t swz128(int r, int c) {
 // share the same bytes (its per-block instruction count is higher).
 template <typename KT>
 struct MmaCfg {
+    static constexpr int kWarps = 4;
     static constexpr int kStages = KT::bytes == 1 ? 3 : 2;
     static constexpr int kCtasPerSm = KT::bytes == 1 ? 4 : 3;
 };
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
 template <int G, typename KT, typename QT>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                 cudaStream_t st) {
-    constexpr int NW = kDecodeWarps;
+    constexpr int NW = MmaCfg<KT>::kWarps;
     constexpr int NST = MmaCfg<KT>::kStages;
     constexpr int SMEM = MmaSmem<KT, NW, NST>::kBytes;
     auto kern = decode_mma_kernel<G, KT, QT, NW, NST>;
