@@ -335,6 +335,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if len(step.pairs):  # the step's copy-on-write: per-row sources (fused) or the pair list
         h["cow"] = (step.d_cow_src if step.fused else step.d_pairs).cpu().pin_memory()
+    if step.work is not None:  # the host plan, rebuilt from the host arrays every step
+        h["work"] = torch.from_numpy(step.work_host.copy()).pin_memory()
     d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
@@ -515,7 +517,7 @@ def run_prefill(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl = workloads.PREFILL[args.workload]()
-    step = PrefillStep(wl, device=dev)
+    step = PrefillStep(wl, device=dev, plan=not args.no_plan)
     flops = prefill_flops(wl)
     nbytes = prefill_bytes(wl)
     stream = torch.cuda.current_stream()
@@ -558,6 +560,8 @@ def run_prefill(args, rank, world, local_rank):
     h = {"q": step.q.cpu().pin_memory(), "k": step.k_new.cpu().pin_memory(), "v": step.v_new.cpu().pin_memory(),
          "slots": step.d_slots.cpu().pin_memory(), "tables": step.d_tables.cpu().pin_memory(),
          "lens": step.d_lens.cpu().pin_memory(), "qs": step.d_query_start.cpu().pin_memory()}
+    if step.work is not None:  # the host plan, rebuilt from the host arrays every step
+        h["work"] = torch.from_numpy(step.work_host.copy()).pin_memory()
     d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
@@ -570,11 +574,16 @@ def run_prefill(args, rank, world, local_rank):
     for _ in range(Ke):
         if flush:
             flush_buf.zero_()
+        if "work" in h:  # planning is host work of the step; the batch (so the plan) never changes here
+            wk = pk.prefill_plan(step.query_start, step.seq_lens, wl.Hq, wl.Hkv, wl.max_query_len)
+            if not np.array_equal(wk, step.work_host):
+                raise RuntimeError("prefill plan changed between steps")
         for k in h:
             d[k].copy_(h[k], non_blocking=True)
         pk.paged_kv_append(d["k"], d["v"], d["slots"], step.k_cache, step.v_cache, step.desc, in_dtype=wl.dtype)
         pk.paged_attention_prefill(d["q"], step.k_cache, step.v_cache, step.desc, d["qs"], wl.max_query_len,
-                                   d["tables"], d["lens"], wl.scale, step.out, q_dtype=wl.dtype)
+                                   d["tables"], d["lens"], wl.scale, step.out, q_dtype=wl.dtype,
+                                   work_units=d.get("work"))
         out_h.copy_(step.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -606,6 +615,8 @@ def run_prefill(args, rank, world, local_rank):
                    "new_tokens": wl.T, "chunk_tokens": wl.qlens, "context_tokens": wl.ctx, "num_blocks": wl.NB,
                    "flops_per_step": flops, "min_bytes_per_step": nbytes,
                    "l2": ("flushed between steps (2x L2 write)" if flush else "inputs larger than L2, no flush"),
+                   "cta_order": ("host plan, longest causal key range first" if step.work is not None
+                                 else "grid order"),
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
@@ -820,6 +831,8 @@ def main(argv=None):
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="prefill: CTAs in grid order instead of the host plan's longest-first order")
     ap.add_argument("--profile", action="store_true",
                     help="timed steps only (no e2e loop, clock-window extension or CPU baseline): for ncu runs")
     args = ap.parse_args(argv)

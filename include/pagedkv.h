@@ -335,8 +335,18 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * Rows of out outside every sequence's range are not written.
  * scale must be finite and > 0 (else PKV_ERR_INVALID).
  * Implemented for f16 / bf16 pools with q of the same type, head_size 64 or
- * 128, num_q_heads / num_kv_heads in {1, 2, 4, 8}; others return
- * PKV_ERR_UNSUPPORTED.  Inconsistent query_start / seq_lens (n_s < 0,
+ * 128, num_q_heads / num_kv_heads in {1, 2, 4, 8}, and at most 2^31 - 1 CTAs
+ * (ceil(max_query_len * G / 256) * num_kv_heads * num_seqs, G = num_q_heads /
+ * num_kv_heads); others return PKV_ERR_UNSUPPORTED.
+ * work_units, num_work_units: the order in which the CTAs start.  A CTA
+ * covers unit u = s * nq + qt (sequence s, its query rows [qt * r, (qt + 1) *
+ * r) with r = 256 / G tokens, nq = ceil(max_query_len / r)) for one KV head.
+ * Null (num_work_units 0): every unit, each (sequence, KV head) from its last
+ * rows down.  Otherwise a device int32 array of num_work_units units, each
+ * run for every KV head in that order, and only those; pkv_prefill_plan
+ * writes the batch's units longest causal key range first.  A unit outside
+ * [0, num_seqs * nq) sets PKV_DEVERR_SEQ_LEN and is skipped.
+ * Inconsistent query_start / seq_lens (n_s < 0,
  * n_s > seq_lens[s], past num_tokens or the block table) set
  * PKV_DEVERR_SEQ_LEN and the sequence is skipped; a block id outside the pool
  * sets PKV_DEVERR_BLOCK_ID.  Needs no workspace.
@@ -345,7 +355,28 @@ pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype, int32_t n
                                        int32_t num_seqs, const int32_t* query_start, int32_t max_query_len,
                                        const void* k_cache, const void* v_cache, const pkv_cache_desc* desc,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                       const int32_t* seq_lens, float scale, void* out, void* stream);
+                                       const int32_t* seq_lens, const int32_t* work_units,
+                                       int32_t num_work_units, float scale, void* out, void* stream);
+
+/*
+ * Host work plan for pkv_paged_attention_prefill (plain C++, no GPU):
+ * writes to units[0 .. *num_units) every non-empty unit s * nq + qt of the
+ * batch (see work_units above), sorted by the causal key range of the
+ * unit's last query row, longest first (ties: sequence, then query tile,
+ * ascending), so that the last CTAs to start are the shortest.  The batch
+ * may mix chunks over contexts of any length; scheduling long units first
+ * keeps the last wave short.
+ * query_start [num_seqs + 1], seq_lens [num_seqs]: HOST copies of the
+ *   prefill call's arrays.  max_query_len, num_q_heads, num_kv_heads: as
+ *   passed to the prefill call.
+ * *num_units always receives the count; PKV_ERR_WORKSPACE if it exceeds
+ * units_cap (nothing written).  Inconsistent sequences (n_s < 0, n_s >
+ * max_query_len, n_s > seq_lens[s], query_start[s] < 0) return
+ * PKV_ERR_INVALID; a head ratio outside {1, 2, 4, 8} PKV_ERR_UNSUPPORTED.
+ */
+pkv_status pkv_prefill_plan(const int32_t* query_start, const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads, int32_t max_query_len, int32_t* units,
+                            int32_t units_cap, int32_t* num_units);
 
 /*
  * Partition size the automatic choice (partition_tokens = 0) would use for

@@ -82,6 +82,8 @@ struct PrefillParams {
     int32_t G, TT;               // heads per KV head, tokens per CTA (128 / G)
     int32_t num_qtiles;          // CTAs per (sequence, KV head) along the queries
     int32_t max_query_len;       // the caller's bound on every chunk
+    const int32_t* work;         // [num_work] units s * num_qtiles + qt in start order, or null
+    int32_t num_work;
     float qk_scale;              // scale * log2(e)
     unsigned int* err;
     // cascade prefix pass only
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
+    int h;
     const int G = p.G;
     const int RQ = kTileM / G;  // tokens (prefill) or members (prefix) per Q tile
     // ---- this CTA's rows and keys (uniform across the CTA).  Keys are
@@ -198,17 +200,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prefix pass
     int m0 = 0, members = 0, mrow0 = 0, seq0 = 0, pp = 0;
     if constexpr (!kPrefix) {
-        const int s = blockIdx.z;
-        const int qt = p.num_qtiles - 1 - static_cast<int>(blockIdx.x);  // longest key ranges first
+        // One CTA per (sequence s, query tile pair qt, KV head h).  CTAs start
+        // in linear order.  With a work list (the host plan of
+        // pkv_prefill_plan, longest causal key range first over the whole
+        // batch) CTA i takes unit work[i / Hkv] and head i % Hkv; without one,
+        // each (s, h) runs its query tiles from the last down.
+        const int64_t lin = blockIdx.x;
+        int s, qt;
+        if (p.work) {
+            const int u = __ldg(p.work + lin / p.Hkv);
+            h = static_cast<int>(lin % p.Hkv);
+            if (u < 0 || u >= p.S * p.num_qtiles) {
+                if (threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+                return;
+            }
+            s = u / p.num_qtiles;
+            qt = u % p.num_qtiles;
+        } else {
+            qt = p.num_qtiles - 1 - static_cast<int>(lin % p.num_qtiles);
+            h = static_cast<int>((lin / p.num_qtiles) % p.Hkv);
+            s = static_cast<int>(lin / (static_cast<int64_t>(p.num_qtiles) * p.Hkv));
+        }
         q0 = __ldg(p.query_start + s);
         const int q1 = __ldg(p.query_start + s + 1);
         n = q1 - q0;
         const int L = __ldg(p.seq_lens + s);
         if (q0 < 0 || n < 0 || q1 > p.T || L < n || L > p.MB * kBlockSize) {
-            if (threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+            if (threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
             return;
         }
-        if (n > p.max_query_len && threadIdx.x == 0 && blockIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+        if (n > p.max_query_len && threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
         t0 = qt * 2 * RQ;
         if (t0 >= n) return;
         ctx = L - n;  // tokens before this chunk
@@ -219,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
     } else {
         pp = blockIdx.x;
+        h = blockIdx.y;
         const int grp = blockIdx.z / p.row_chunks, chunk = blockIdx.z % p.row_chunks;
         m0 = __ldg(p.group_offsets + grp);
         members = __ldg(p.group_offsets + grp + 1) - m0;
@@ -705,7 +727,8 @@ cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq
 template <typename T>
 cudaError_t launch_prefill(const PrefillParams& p, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t st) {
-    const dim3 grid(p.num_qtiles, p.Hkv, p.S);
+    const int64_t units = p.work ? p.num_work : static_cast<int64_t>(p.num_qtiles) * p.S;
+    const dim3 grid(static_cast<unsigned>(units * p.Hkv));
     return D == 64 ? launch_tile<T, 64, false>(p, grid, tq, tk, tv, st)
                    : launch_tile<T, 128, false>(p, grid, tq, tk, tv, st);
 }
@@ -751,9 +774,11 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
                                                   int32_t num_q_heads, int32_t num_seqs, const int32_t* query_start,
                                                   int32_t max_query_len, const void* k_cache, const void* v_cache,
                                                   const pkv_cache_desc* desc, const int32_t* block_tables,
-                                                  int32_t max_blocks_per_seq, const int32_t* seq_lens, float scale,
+                                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                                  const int32_t* work_units, int32_t num_work_units, float scale,
                                                   void* out, void* stream) {
     if (!desc || num_tokens < 0 || num_seqs < 0 || max_query_len < 0 || num_q_heads <= 0) return PKV_ERR_INVALID;
+    if (num_work_units < 0 || (!work_units && num_work_units > 0)) return PKV_ERR_INVALID;
     if (desc->block_size != kBlockSize || desc->num_kv_heads <= 0 || desc->num_blocks <= 0) return PKV_ERR_INVALID;
     if (num_q_heads % desc->num_kv_heads) return PKV_ERR_INVALID;
     const int G = num_q_heads / desc->num_kv_heads;
@@ -762,7 +787,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
     if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID;  // finite, > 0 (max on raw scores)
-    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0 || (work_units && num_work_units == 0)) return PKV_OK;
     if (!q || !out || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start) return PKV_ERR_INVALID;
     if (max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return PKV_ERR_INVALID;
@@ -785,6 +810,10 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     p.G = G;
     p.TT = kTileM / G;
     p.num_qtiles = (max_query_len + 2 * p.TT - 1) / (2 * p.TT);  // CTAs of two Q tiles
+    if (static_cast<int64_t>(p.num_qtiles) * p.Hkv * p.S > INT32_MAX) return PKV_ERR_UNSUPPORTED;  // one grid axis
+    p.work = work_units;
+    p.num_work = num_work_units;
+    if (static_cast<int64_t>(num_work_units) * p.Hkv > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     p.max_query_len = max_query_len;
     p.qk_scale = scale * 1.4426950408889634f;
     p.err = err;

@@ -36,6 +36,7 @@ EXPORTED = [
     "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
     "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
+    "pkv_prefill_plan",
 ]
 
 
@@ -130,8 +131,9 @@ def lib():
         "pkv_alloc_num_cached": (i32, [P]),
         "pkv_alloc_block_hash_of": (i64, [P, i32, P]),
         "pkv_alloc_reset_prefix_cache": (None, [P]),
-        "pkv_paged_attention_prefill": (i32, [P, i32, i32, i32, i32, P, i32, P, P, D, P, i32, P, ctypes.c_float,
-                                              P, P]),
+        "pkv_paged_attention_prefill": (i32, [P, i32, i32, i32, i32, P, i32, P, P, D, P, i32, P, P, i32,
+                                              ctypes.c_float, P, P]),
+        "pkv_prefill_plan": (i32, [P, P, i32, i32, i32, i32, P, i32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -347,19 +349,43 @@ def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_t
 
 
 def paged_attention_prefill(q, k_cache, v_cache, desc: CacheDesc, query_start, max_query_len: int, block_tables,
-                            seq_lens, scale: float, out, q_dtype: str | None = None, stream=None) -> None:
+                            seq_lens, scale: float, out, q_dtype: str | None = None, stream=None,
+                            work_units=None) -> None:
     """Causal paged prefill: q, out [T, Hq, D]; query_start int32 [S + 1],
-    block_tables int32 [S, MB], seq_lens int32 [S] (device tensors)."""
+    block_tables int32 [S, MB], seq_lens int32 [S] (device tensors);
+    work_units: optional device int32 CTA order from prefill_plan."""
     T, Hq = int(q.shape[0]), int(q.shape[1])
     S = int(seq_lens.shape[0])
     if int(query_start.shape[0]) != S + 1:
         raise ValueError("query_start must have num_seqs + 1 entries")
+    nw = 0 if work_units is None else int(work_units.numel())
+    wp = _dev_ptr(work_units, "work_units") if nw else None
     st = lib().pkv_paged_attention_prefill(
         _dev_ptr(q, "q"), _dtype_code(q, q_dtype), T, Hq, S, _dev_ptr(query_start, "query_start"), int(max_query_len),
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
         _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
-        float(scale), _dev_ptr(out, "out"), _stream(stream))
+        wp, nw, float(scale), _dev_ptr(out, "out"), _stream(stream))
     _check(st, "paged_attention_prefill")
+
+
+def prefill_plan(query_start, seq_lens, num_q_heads: int, num_kv_heads: int, max_query_len: int) -> np.ndarray:
+    """Host work plan for paged_attention_prefill (host arrays in, int32
+    units out, longest causal key range first)."""
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    S = int(sl.size)
+    if qs.size != S + 1:
+        raise ValueError("query_start must have num_seqs + 1 entries")
+    n = ctypes.c_int32(0)
+    st = lib().pkv_prefill_plan(_np_ptr(qs), _np_ptr(sl) if S else None, S, int(num_q_heads), int(num_kv_heads),
+                                int(max_query_len), None, 0, ctypes.byref(n))
+    if st not in (0, 5):  # OK or WORKSPACE (count only)
+        _check(st, "prefill_plan")
+    out = np.zeros(max(int(n.value), 1), dtype=np.int32)
+    st = lib().pkv_prefill_plan(_np_ptr(qs), _np_ptr(sl) if S else None, S, int(num_q_heads), int(num_kv_heads),
+                                int(max_query_len), _np_ptr(out), int(out.size), ctypes.byref(n))
+    _check(st, "prefill_plan")
+    return out[: int(n.value)]
 
 
 def block_hash(parent: int, tokens, extras=()) -> int:

@@ -168,9 +168,11 @@ class PrefillStep:
 
     Host: the allocator holds every sequence's earlier context, then reserves
     one slot per new token (``append_tokens``).  Device, in stream order: ``paged_kv_append`` of the new
-    tokens' K/V -> ``paged_attention_prefill`` for their query rows."""
+    tokens' K/V -> ``paged_attention_prefill`` for their query rows, its CTAs
+    in the order of the host plan (``prefill_plan``: longest causal key range
+    first) unless ``plan`` is False."""
 
-    def __init__(self, wl, device="cuda", alloc: pk.Allocator | None = None):
+    def __init__(self, wl, device="cuda", alloc: pk.Allocator | None = None, plan: bool = True):
         self.wl = wl
         self.device = torch.device(device)
         self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.dtype,
@@ -194,6 +196,10 @@ class PrefillStep:
         self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
         self.d_query_start = torch.from_numpy(self.query_start).to(dev)
         self.out = torch.empty((wl.T, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
+        self.work = None
+        if plan:
+            self.work_host = pk.prefill_plan(self.query_start, self.seq_lens, wl.Hq, wl.Hkv, wl.max_query_len)
+            self.work = torch.from_numpy(self.work_host).to(dev)
 
     def kernel_launches(self) -> int:
         return 2  # append + prefill attention
@@ -206,7 +212,7 @@ class PrefillStep:
         pk.paged_attention_prefill(self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
                                    self.d_query_start, self.wl.max_query_len, self.d_tables, self.d_lens,
                                    self.wl.scale, self.out if out is None else out, q_dtype=self.wl.dtype,
-                                   stream=stream)
+                                   stream=stream, work_units=self.work)
 
     def run(self, stream=None):
         self.append(stream)

@@ -22,9 +22,9 @@ def lib():
     return pagedkv
 
 
-def run(wl):
+def run(wl, plan=True):
     from paged_kv_cache_10_gb300.step import PrefillStep
-    st = PrefillStep(wl, device="cuda")
+    st = PrefillStep(wl, device="cuda", plan=plan)
     st.run()
     torch.cuda.synchronize()
     return st
@@ -82,12 +82,14 @@ CASES = [
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("case", [0, 1])
 @pytest.mark.parametrize("D", [128, 64])
-def test_prefill_matches_oracle_every_element(lib, dtype, G, case, D):
+@pytest.mark.parametrize("plan", [True, False])
+def test_prefill_matches_oracle_every_element(lib, dtype, G, case, D, plan):
+    """plan: CTAs in the host plan's longest-first order, or in grid order."""
     from paged_kv_cache_10_gb300 import workloads
     ctx, qlens = CASES[case]
     Hkv = 2
     wl = workloads.prefill("prefill_small", 2000 + 10 * G + case + D, ctx, qlens, Hkv * G, Hkv, D=D, dtype=dtype)
-    st = run(wl)
+    st = run(wl, plan)
     assert lib.get_device_error() == 0
     err, mx = check_full(st)
     assert err <= TOL[dtype], (err, mx)
@@ -139,6 +141,45 @@ def test_prefill_ignores_nan_bytes_past_the_sequence_end(lib):
     assert lib.get_device_error() == 0
     err, mx = check_full(st)
     assert err <= TOL["bf16"], (err, mx)
+
+
+def test_prefill_work_list_runs_exactly_its_units(lib):
+    """A work list runs only the units it names, in any order; a unit id
+    outside the batch is flagged and skipped."""
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.prefill("prefill_units", 2103, [40, 0, 300], [70, 129, 33], 8, 2, dtype="bf16")
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["bf16"], (err, mx)
+    full = host_bits(st.out).copy()
+    plan = st.work_host
+    assert len(plan) == len(set(plan.tolist()))
+    # run only the second half of the plan, reversed, into a cleared output
+    part = plan[len(plan) // 2:][::-1].copy()
+    st.out.zero_()
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16",
+                                work_units=torch.from_numpy(part).cuda())
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    got = host_bits(st.out)
+    rows_per_unit = 2 * (128 // (wl.Hq // wl.Hkv))
+    nq = -(-wl.max_query_len // rows_per_unit)
+    done = np.zeros(wl.T, bool)
+    for u in part.tolist():
+        s, qt = divmod(u, nq)
+        a = st.query_start[s] + qt * rows_per_unit
+        done[a:min(a + rows_per_unit, st.query_start[s + 1])] = True
+    assert np.array_equal(got[done], full[done])
+    assert np.all(got[~done] == 0)
+    # an out-of-range unit: flagged, the valid ones still run
+    bad = np.concatenate([plan[:1], np.array([wl.S * nq + 3], np.int32)])
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16",
+                                work_units=torch.from_numpy(bad).cuda())
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_SEQ_LEN
 
 
 def test_prefill_rejects_bad_arguments(lib):
