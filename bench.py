@@ -335,8 +335,6 @@ def run_ours(args, rank, world, local_rank):
     }
     if len(step.pairs):  # the step's copy-on-write: per-row sources (fused) or the pair list
         h["cow"] = (step.d_cow_src if step.fused else step.d_pairs).cpu().pin_memory()
-    if step.work is not None:  # the host plan, rebuilt from the host arrays every step
-        h["work"] = torch.from_numpy(step.work_host.copy()).pin_memory()
     d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
     out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
