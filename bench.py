@@ -193,6 +193,77 @@ def aggregate(value_bytes: float, seconds: float, group=None):
     return float(b.item()), float(s.item())
 
 
+E2E_COPIES = ("every step: its inputs host->device in one upload from a pinned staging buffer on an upload "
+              "stream, its result device->host into pinned memory on a download stream; two device buffer sets, "
+              "so the copies of one step overlap the kernels of its neighbours")
+
+
+def e2e_pipelined(h, launch, out, steps, stream, flush_buf=None):
+    """Times `steps` steps end to end as a serving loop runs them: every step
+    copies its inputs `h` (host tensors, staged in one pinned buffer) to the
+    device in one upload, launches its
+    kernels (`launch(device_inputs, device_out)`) and copies the result back
+    into pinned host memory.  Two device buffer sets let step i + 1's
+    host->device copies (on an upload stream) overlap step i's kernels, and
+    step i's device->host copy (on a download stream) overlap step i + 1.
+    Returns the elapsed ms on `stream` from before the first copy to after
+    the last result has landed, minus the L2 flushes (`flush_buf` written
+    before each step's kernels, each timed by its own events), and the bytes
+    one upload moves."""
+    dev = out.device
+    # the step's inputs staged in one pinned buffer (256-byte aligned fields),
+    # so a step is one upload; the device copies are views of one buffer
+    offs, n = {}, 0
+    for k, t in h.items():
+        offs[k] = n
+        n += -(-(t.numel() * t.element_size()) // 256) * 256
+    staged = torch.empty(n, dtype=torch.uint8).pin_memory()
+    for k, t in h.items():
+        nb = t.numel() * t.element_size()
+        staged[offs[k]:offs[k] + nb].copy_(t.reshape(-1).view(torch.uint8))
+    packed = [torch.empty(n, dtype=torch.uint8, device=dev) for _ in range(2)]
+    ds = [{k: packed[i][offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+           for k, t in h.items()} for i in range(2)]
+    outs = [out, torch.empty_like(out)]
+    out_hs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]   # inputs of the buffer's step on the device
+    done = [torch.cuda.Event() for _ in range(2)]    # its kernels finished (inputs free, output written)
+    landed = [torch.cuda.Event() for _ in range(2)]  # its output copied to the host
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps if flush_buf is not None else 0)]
+    torch.cuda.synchronize()
+    e0.record(stream)
+    up.wait_stream(stream)
+    down.wait_stream(stream)
+    for i in range(steps):
+        b = i & 1
+        if i >= 2:
+            up.wait_event(done[b])
+        with torch.cuda.stream(up):
+            packed[b].copy_(staged, non_blocking=True)
+        ready[b].record(up)
+        if flush_buf is not None:
+            fl[i][0].record(stream)
+            flush_buf.zero_()
+            fl[i][1].record(stream)
+        stream.wait_event(ready[b])
+        if i >= 2:
+            stream.wait_event(landed[b])
+        launch(ds[b], outs[b])
+        done[b].record(stream)
+        down.wait_event(done[b])
+        with torch.cuda.stream(down):
+            out_hs[b].copy_(outs[b], non_blocking=True)
+        landed[b].record(down)
+    stream.wait_stream(up)
+    stream.wait_stream(down)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) - sum(a.elapsed_time(b) for a, b in fl), n
+
+
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -335,39 +406,22 @@ def run_ours(args, rank, world, local_rank):
     }
     if len(step.pairs):  # the step's copy-on-write: per-row sources (fused) or the pair list
         h["cow"] = (step.d_cow_src if step.fused else step.d_pairs).cpu().pin_memory()
-    d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = step.out.numel() * step.out.element_size()
     Ke = 0 if args.profile else max(1, min(K, 200))
     barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        if flush:
-            flush_buf.zero_()
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
+
+    def launch_decode(dd, o):
         if len(step.pairs) and not step.fused:
             from paged_kv_cache_10_gb300 import pagedkv as pk
-            pk.copy_blocks(step.k_cache, step.v_cache, step.desc, d["cow"])
-        step.append(k=d["k"], v=d["v"], slots=d["slots"])
-        step.decode(q=d["q"], tables=d["tables"], lens=d["lens"], k=d["k"], v=d["v"], slots=d["slots"],
-                    cow_src=d["cow"] if (len(step.pairs) and step.fused) else None)
-        out_h.copy_(step.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if flush:
-        # the flushes are not part of the step: subtract their measured cost
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(Ke):
-            flush_buf.zero_()
-        f1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms -= f0.elapsed_time(f1)
+            pk.copy_blocks(step.k_cache, step.v_cache, step.desc, dd["cow"])
+        step.append(k=dd["k"], v=dd["v"], slots=dd["slots"])
+        step.decode(q=dd["q"], tables=dd["tables"], lens=dd["lens"], k=dd["k"], v=dd["v"], slots=dd["slots"],
+                    cow_src=dd["cow"] if (len(step.pairs) and step.fused) else None, out=o)
+
+    # the flushes are not part of the step: e2e_pipelined subtracts each one's time
+    e2e_ms, h2d = (e2e_pipelined(h, launch_decode, step.out, Ke, stream, flush_buf if flush else None) if Ke
+                   else (0.0, h2d))
     e2e_bytes, e2e_s = aggregate(nbytes["total"] * Ke, max(e2e_ms, 1e-6) / 1e3)
 
     from paged_kv_cache_10_gb300 import pagedkv as pk
@@ -423,7 +477,7 @@ def run_ours(args, rank, world, local_rank):
                       + ("; append fused into the decode kernel" if step.fused else ""),
         },
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
+                "d2h_bytes_per_step": d2h, "steps": Ke, "copies": E2E_COPIES},
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
@@ -560,40 +614,23 @@ def run_prefill(args, rank, world, local_rank):
          "lens": step.d_lens.cpu().pin_memory(), "qs": step.d_query_start.cpu().pin_memory()}
     if step.work is not None:  # the host plan, rebuilt from the host arrays every step
         h["work"] = torch.from_numpy(step.work_host.copy()).pin_memory()
-    d = {k: torch.empty_like(t, device=dev) for k, t in h.items()}
-    out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = out_h.numel() * out_h.element_size()
+    d2h = step.out.numel() * step.out.element_size()
     Ke = 0 if args.profile else max(1, min(K, 100))
     barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        if flush:
-            flush_buf.zero_()
-        if "work" in h:  # planning is host work of the step; the batch (so the plan) never changes here
+
+    def launch_prefill(dd, o):
+        if "work" in dd:  # planning is host work of the step; the batch (so the plan) never changes here
             wk = pk.prefill_plan(step.query_start, step.seq_lens, wl.Hq, wl.Hkv, wl.max_query_len)
             if not np.array_equal(wk, step.work_host):
                 raise RuntimeError("prefill plan changed between steps")
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
-        pk.paged_kv_append(d["k"], d["v"], d["slots"], step.k_cache, step.v_cache, step.desc, in_dtype=wl.dtype)
-        pk.paged_attention_prefill(d["q"], step.k_cache, step.v_cache, step.desc, d["qs"], wl.max_query_len,
-                                   d["tables"], d["lens"], wl.scale, step.out, q_dtype=wl.dtype,
-                                   work_units=d.get("work"))
-        out_h.copy_(step.out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if flush and Ke:
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(Ke):
-            flush_buf.zero_()
-        f1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms -= f0.elapsed_time(f1)
+        pk.paged_kv_append(dd["k"], dd["v"], dd["slots"], step.k_cache, step.v_cache, step.desc, in_dtype=wl.dtype)
+        pk.paged_attention_prefill(dd["q"], step.k_cache, step.v_cache, step.desc, dd["qs"], wl.max_query_len,
+                                   dd["tables"], dd["lens"], wl.scale, o, q_dtype=wl.dtype,
+                                   work_units=dd.get("work"))
+
+    e2e_ms, h2d = (e2e_pipelined(h, launch_prefill, step.out, Ke, stream, flush_buf if flush else None) if Ke
+                   else (0.0, h2d))
     e2e_flops, e2e_s = aggregate(flops * Ke, max(e2e_ms, 1e-6) / 1e3)
     assert pk.get_device_error() == 0, "device error word set during the benchmark"
     if rank != 0:
@@ -617,7 +654,7 @@ def run_prefill(args, rank, world, local_rank):
                                  else "grid order"),
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
+                "d2h_bytes_per_step": d2h, "steps": Ke, "copies": E2E_COPIES},
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, "prefill"),
