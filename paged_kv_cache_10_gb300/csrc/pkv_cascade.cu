@@ -19,6 +19,7 @@
 //
 // The result is the same function as pkv_paged_attention_decode.
 #include <cstdint>
+#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -27,6 +28,35 @@ namespace pkv {
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The prefix pass and the own-token decode read the pool and write disjoint
+// partials, so they may run at the same time: the prefix pass goes to a
+// library-owned stream forked from the caller's (an event), and the caller's
+// stream waits for it (a second event) before the merge.  The call stays
+// ordered on the caller's stream and can be captured into a CUDA graph.
+// One side stream and event pair per device; the mutex keeps the record /
+// wait pairs of concurrent callers from interleaving.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex side_mu;
+
+cudaError_t side_stream(SideStream** out) {
+    static SideStream per_dev[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream& ss = per_dev[dev];
+    if (!ss.stream) {
+        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &ss;
+    return cudaSuccess;
+}
 }  // namespace
 
 }  // namespace pkv
@@ -116,18 +146,31 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
         return PKV_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    // 1. shared prefixes
-    if (npp > 0 && row_chunks > 0) {
+    const bool prefix = npp > 0 && row_chunks > 0;
+    std::unique_lock<std::mutex> lock(side_mu, std::defer_lock);
+    SideStream* ss = nullptr;
+    // 1. shared prefixes, on the side stream, after everything before this call
+    if (prefix) {
+        lock.lock();
+        if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
+        if (cudaEventRecord(ss->fork, st) != cudaSuccess || cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
+            return PKV_ERR_CUDA;
         CascadeParams cp{p, group_offsets, group_members, G, static_cast<int32_t>(row_chunks), npp};
-        e = launch_cascade_prefix_tc(cp, num_groups, d->kv_dtype, tq, tk, tv, st);
-        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        e = launch_cascade_prefix_tc(cp, num_groups, d->kv_dtype, tq, tk, tv, ss->stream);
+        if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->stream);
+        if (e != cudaSuccess) {
+            (void)cudaStreamWaitEvent(st, ss->join, 0);  // keep the caller's stream behind what was enqueued
+            return PKV_ERR_CUDA;
+        }
     }
-    // 2. each sequence's own tokens
+    // 2. each sequence's own tokens, meanwhile on the caller's stream
     if (G >= 2) {
         e = d->kv_dtype == PKV_BF16 ? launch_decode_mma_bf16(p, G, tk, tv, st) : launch_decode_mma_f16(p, G, tk, tv, st);
     } else {
         e = d->kv_dtype == PKV_BF16 ? launch_decode_bf16(p, G, st) : launch_decode_f16(p, G, st);
     }
+    // join before the merge reads the prefix partials
+    if (prefix && cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess) return PKV_ERR_CUDA;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
     // 3. merge every row
     e = launch_merge(p, q_dtype, st);
