@@ -454,6 +454,7 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "median_us_per_step": round(1e3 * statistics.median(a.elapsed_time(c) for a, _, c in ev), 2),
         "tokens_per_s": round(world * wl.S / (tot_s / K), 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_8tbs": round(100 * value / world / 8000.0, 2),
@@ -487,6 +488,7 @@ def run_ours(args, rank, world, local_rank):
                                + (", with the step's append fused in" if step.fused else ""),
                      "kernel_sources_hash": kernel_hash(kind),
                      "mean_launch_us": round(dec_ms * 1e3, 2),
+                     "median_launch_us": round(statistics.median(decode_ms) * 1e3, 2),
                      "algorithmic_bytes_per_launch": roof_bytes,
                      "bytes_basis": ("distinct KV bytes (blocks shared between sequences counted once)" if shared
                                      else "KV bytes gathered through the block tables"),
@@ -644,6 +646,7 @@ def run_prefill(args, rank, world, local_rank):
     line = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "us_per_step": round(1e3 * total_ms / K, 2),
+        "median_us_per_step": round(1e3 * statistics.median(a.elapsed_time(c) for a, _, c in ev), 2),
         "tokens_per_s": round(world * wl.T / (tot_s / K), 1), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype + ", fp32 accumulate", "data": "synthetic",
         "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D,
@@ -660,6 +663,7 @@ def run_prefill(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, "prefill"),
                      "peak_kind": peak_kind, "kernel": "prefill_tc_kernel",
                      "kernel_sources_hash": kernel_hash("prefill"), "mean_launch_us": round(a_ms * 1e3, 2),
+                     "median_launch_us": round(statistics.median(attn_ms) * 1e3, 2),
                      "algorithmic_flops_per_launch": flops,
                      "hbm_gbs_at_min_bytes": round(nbytes / (a_ms / 1e3) / 1e9, 1)},
         "clocks": clocks,
