@@ -81,3 +81,31 @@ def test_cascade_rejects_fp8(lib):
     with pytest.raises(lib.PagedKVError) as e:
         run(wl, cascade=True)
     assert e.value.status == lib.ERR_UNSUPPORTED
+
+
+def test_cascade_graph_replay_and_stream_order(lib):
+    """The prefix pass runs on the library's own stream, forked from the
+    caller's and joined before the merge: captured into a CUDA graph the step
+    replays to the same bits as eager, and on a non-default caller stream the
+    eager result is the same too."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.fork_groups("cgraph", 74, [(320, 5), (96, 3)], 2, 32, 8)
+    st = DecodeStep(wl, device="cuda", cascade=True, cascade_min_blocks=1)
+    assert st.groups.num_groups >= 1
+    g = st.capture()  # runs one eager step first, then captures
+    eager = host_bits(st.out).copy()
+    err, mx = check_step(st)
+    assert err <= TOL["bf16"], (err, mx)
+    for _ in range(2):
+        st.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(st.out), eager)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        st.out.zero_()
+        st.decode(stream=side)
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    assert np.array_equal(host_bits(st.out), eager)
