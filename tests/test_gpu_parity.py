@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL, check_step, host_bits
+from parity_util import TOL, check_step, host_bits, max_error
 
 pytestmark = pytest.mark.gpu
 
@@ -206,6 +206,23 @@ def test_device_errors_are_reported_not_trapped(lib):
     assert err <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (32, 8)])
+def test_many_sequences_and_a_full_block_table(lib, Hq, Hkv):
+    """3000 short sequences (a large grid and 3000 x Hq merge rows) around
+    one 2048-token sequence whose block table is exactly full, split into
+    256-token partitions; every row against the oracle, pools bit-exact."""
+    from paged_kv_cache_10_gb300 import workloads
+    rng = np.random.default_rng(97)
+    lens = rng.integers(0, 40, 3000).tolist()
+    lens[1234] = 2048  # 128 blocks: the widest table, every entry used
+    wl = workloads.custom("many", 98 + Hq, lens, Hq, Hkv, 128, kv_dtype="bf16", partition_tokens=256)
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    assert st.tables.shape[1] == 128 and np.all(st.tables[1234] >= 0)
+    err, mx = check_step(st)
+    assert err <= TOL["bf16"], (err, mx)
+
+
 def test_library_is_loaded_from_the_tree(lib):
     import os
     maps = open("/proc/self/maps").read()
@@ -288,7 +305,7 @@ def test_swap_round_trip_preserves_sequences(lib):
     ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), "bf16", keep_k, keep_v, "bf16", tables, lens,
                               wl.scale)
     got = oracle.dequantize(host_bits(out), "bf16")
-    assert np.max(np.abs(got - ref)) <= TOL["bf16"]
+    assert max_error(got, ref, "bf16", TOL["bf16"]) <= TOL["bf16"]
     # and it is the attention of the original data (old tables, original pools)
     ref0 = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), "bf16", orig_k, orig_v, "bf16",
                                st.tables[rows], st.seq_lens[rows], wl.scale)

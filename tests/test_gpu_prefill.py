@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from oracle.allocator_model import AllocatorModel
-from parity_util import TOL, host_bits
+from parity_util import TOL, host_bits, max_error
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +68,7 @@ def check_full(st):
     ref = oracle.paged_prefill(wl.q, wl.dtype, st.query_start, kp, vp, wl.dtype, tables, lens, wl.scale)
     got = oracle.dequantize(host_bits(st.out), wl.dtype)
     assert np.all(np.isfinite(got))
-    return float(np.max(np.abs(got - ref))), float(np.max(np.abs(ref)))
+    return max_error(got, ref, wl.dtype, TOL[wl.dtype]), float(np.max(np.abs(ref)))
 
 
 CASES = [
@@ -120,7 +120,7 @@ def test_prefill_full_size_sampled_rows(lib, name):
                               np.ascontiguousarray(tables[seqs]), np.array(pos, np.int32) + 1, wl.scale)
     got = oracle.dequantize(host_bits(st.out)[rows], wl.dtype)
     assert np.all(np.isfinite(got))
-    err = float(np.max(np.abs(got - ref)))
+    err = max_error(got, ref, wl.dtype, TOL[wl.dtype])
     assert err <= TOL[wl.dtype], err
     # every row was written (finite) and the appended pool bytes match
     assert np.all(np.isfinite(oracle.dequantize(host_bits(st.out), wl.dtype)))
