@@ -20,6 +20,19 @@ def output_ulp(ref: np.ndarray, out_dtype: str) -> np.ndarray:
     return np.exp2(np.floor(np.log2(a)) - _MANT[out_dtype])
 
 
+# unit roundoff of the probabilities' 16-bit type in the tensor-core products
+P_ROUNDOFF = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+
+
+def p_rounding_allowance(p_dtype: str, vmax: float) -> float:
+    """Error a kernel that rounds the softmax probabilities to a 16-bit MMA
+    operand may add when few keys dominate a row: each weight moves by at
+    most the unit roundoff u, so the output by at most u * max|V|.  (Rows
+    spread over many keys, as with the configs' N(0,1) queries, average it
+    out.)"""
+    return P_ROUNDOFF[p_dtype] * float(vmax)
+
+
 def max_error(got: np.ndarray, ref: np.ndarray, out_dtype: str, tol: float) -> float:
     """Max-abs error against the float64 oracle, with the allowance of an
     output whose format cannot meet the absolute bound: where one unit in

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from oracle.allocator_model import AllocatorModel
-from parity_util import TOL, host_bits, max_error
+from parity_util import TOL, host_bits, max_error, p_rounding_allowance
 
 pytestmark = pytest.mark.gpu
 
@@ -223,3 +223,24 @@ def test_prefill_rejects_bad_arguments(lib):
     assert lib.get_device_error() == 0
     err, mx = check_full(st)
     assert err <= TOL["bf16"], (err, mx)
+
+
+@pytest.mark.parametrize("dtype,G", [("bf16", 4), ("f16", 1)])
+def test_prefill_sharp_softmax(lib, dtype, G):
+    """q scaled by 30: the row maximum jumps by far more than the lazy
+    rebase threshold (2^8) between key tiles, in prompts and in chunks over
+    earlier context.  Few keys dominate each row, so the bound adds the
+    rounding of the probabilities to the operand type of P V."""
+    import oracle as orc
+    from paged_kv_cache_10_gb300 import workloads
+    Hkv = 2
+    wl = workloads.prefill("prefill_sharp", 2200 + G, [0, 300, 0], [257, 130, 40], Hkv * G, Hkv, dtype=dtype)
+    x = orc.dequantize(wl.q, dtype) * 30.0
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    wl.q = t.view(torch.int16).numpy().view(np.uint16).copy()
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    vmax = float(np.max(np.abs(orc.dequantize(np.concatenate([wl.v_pool.ravel(), wl.v_new.ravel()]), dtype))))
+    extra = p_rounding_allowance(dtype, vmax)
+    assert err <= TOL[dtype] + extra, (err, mx, extra)
