@@ -94,3 +94,23 @@ def test_validation_rejects_before_any_launch(pk):
     # empty work is a no-op that needs no device
     assert L.pkv_copy_blocks(fake, fake, ctypes.byref(d), None, 0, None) == pk.OK
     assert L.pkv_paged_kv_append(None, None, 1, 0, None, None, None, ctypes.byref(d), None) == pk.OK
+
+
+def test_prefill_validation_rejects_before_any_launch(pk):
+    L = pk.lib()
+    d = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="bf16").c()
+    d96 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=96, kv_dtype="bf16").c()
+    fake = 1 << 20  # never dereferenced
+
+    def call(desc=d, q_dtype=1, work=None, nwork=0, scale=0.1, Hq=8):
+        return L.pkv_paged_attention_prefill(fake, q_dtype, 64, Hq, 2, fake, 32, fake, fake, ctypes.byref(desc), fake,
+                                             4, fake, work, nwork, scale, fake, None)
+
+    assert call(nwork=-1) == pk.ERR_INVALID            # negative work-list length
+    assert call(work=None, nwork=3) == pk.ERR_INVALID  # a length without a list
+    assert call(work=fake, nwork=0) == pk.OK           # an empty list: nothing to run
+    assert call(desc=d96) == pk.ERR_UNSUPPORTED        # head_size 96
+    assert call(q_dtype=0) == pk.ERR_UNSUPPORTED       # f16 q over a bf16 pool
+    assert call(scale=0.0) == pk.ERR_INVALID           # the row maximum needs scale > 0
+    assert call(Hq=6) == pk.ERR_UNSUPPORTED            # 3 query heads per KV head
+    assert call(Hq=5) == pk.ERR_INVALID                # heads not a multiple
