@@ -9,7 +9,7 @@
 // its own part, which are combined exactly by the log-sum-exp merge:
 //
 //   1. the prefix pass (the tcgen05 attention tile of pkv_prefill.cu): for
-//      each group, KV head and 512-token prefix partition, the query heads of
+//      each group, KV head and 1024-token prefix partition, the query heads of
 //      the group's members (128 / G members x G heads per CTA, on the MMA's
 //      M dimension) attend to the shared blocks, read once per CTA; partials
 //      go to partition indices [0, NPP);

@@ -93,8 +93,11 @@ cudaError_t launch_decode_mma_fp8_f16q(const DecodeParams& p, int G, const CUten
                                        cudaStream_t st);
 
 // Shared-prefix (cascade) decode: the prefix pass over each group's shared
-// leading blocks, kPrefixPartitionBlocks blocks per prefix partition.
-constexpr int kPrefixPartitionBlocks = 32;  // 512 tokens
+// leading blocks, kPrefixPartitionBlocks blocks per prefix partition.  Wide
+// partitions leave SMs to the own-token decode running beside the prefix
+// pass (1024 tokens: graph step 48.8 -> 43.4 us against 512 on the
+// 128-sequence, 2048-token-prefix batch; 256 tokens: 59.0 us).
+constexpr int kPrefixPartitionBlocks = 64;  // 1024 tokens
 int prefix_partitions(int blocks);
 struct CascadeParams {
     DecodeParams base;
