@@ -329,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     wl = workloads.NAMED[args.workload]()
     step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=args.cascade,
-                      fused=not args.unfused)
+                      fused=not args.unfused, plan={"auto": "auto", "on": True, "off": False}[args.decode_plan])
     nbytes = step_bytes(step)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -413,18 +413,24 @@ def run_ours(args, rank, world, local_rank):
     }
     if len(step.pairs):  # the step's copy-on-write: per-row sources (fused) or the pair list
         h["cow"] = (step.d_cow_src if step.fused else step.d_pairs).cpu().pin_memory()
+    if step.work is not None:  # the host plan, rebuilt from the host arrays every step
+        h["work"] = torch.from_numpy(step.work_host.copy())
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = step.out.numel() * step.out.element_size()
     Ke = 0 if args.profile else max(1, min(K, 200))
     barrier()
 
     def launch_decode(dd, o):
+        from paged_kv_cache_10_gb300 import pagedkv as pk
         if len(step.pairs) and not step.fused:
-            from paged_kv_cache_10_gb300 import pagedkv as pk
             pk.copy_blocks(step.k_cache, step.v_cache, step.desc, dd["cow"])
         step.append(k=dd["k"], v=dd["v"], slots=dd["slots"])
+        if "work" in dd:  # planning is host work of the step; the batch (so the plan) never changes here
+            wk = pk.decode_plan(step.seq_lens, wl.Hkv, step.max_seq_len, step.partition_tokens)
+            if not np.array_equal(wk, step.work_host):
+                raise RuntimeError("decode plan changed between steps")
         step.decode(q=dd["q"], tables=dd["tables"], lens=dd["lens"], k=dd["k"], v=dd["v"], slots=dd["slots"],
-                    cow_src=dd["cow"] if (len(step.pairs) and step.fused) else None, out=o)
+                    cow_src=dd["cow"] if (len(step.pairs) and step.fused) else None, out=o, work=dd.get("work"))
 
     # the flushes are not part of the step: e2e_pipelined subtracts each one's time
     e2e_ms, h2d = (e2e_pipelined(h, launch_decode, step.out, Ke, stream, flush_buf if flush else None) if Ke
@@ -483,6 +489,7 @@ def run_ours(args, rank, world, local_rank):
             "parallelism": f"replicas x{world}",
             "launch": ("CUDA graph replay per step" if args.graph else "eager launches")
                       + ("; append fused into the decode kernel" if step.fused else ""),
+            "cta_order": ("host plan, longest unit first" if step.work is not None else "grid order"),
         },
         "e2e": {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke, "copies": E2E_COPIES},
@@ -879,6 +886,9 @@ def main(argv=None):
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-plan", choices=["auto", "on", "off"], default="auto",
+                    help="decode: CTAs in the host plan's longest-first order (auto: when unit lengths differ "
+                         "and no blocks are shared)")
     ap.add_argument("--no-plan", action="store_true",
                     help="prefill: CTAs in grid order instead of the host plan's longest-first order")
     ap.add_argument("--profile", action="store_true",

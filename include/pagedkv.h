@@ -258,6 +258,14 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
  *   copy-on-write pairs (not into an appending row's last block) must be
  *   copied with pkv_copy_blocks first.  Other arguments, errors and
  *   workspace as for pkv_paged_attention_decode.
+ * work_units, num_work_units (device int32, may be NULL / 0): the order in
+ *   which the CTAs start.  A CTA covers unit u = s * NP + partition (NP =
+ *   ceil(max_seq_len / P), P the partition size this call uses) for one KV
+ *   head; the list's units run in order, each for every KV head.  NULL: the
+ *   grid order (partition, KV head, sequence).  pkv_decode_plan writes every
+ *   unit of a batch longest first.  A list must hold every unit of the batch
+ *   (a row whose units are missing is left undefined, and so is its append);
+ *   a unit outside [0, num_seqs * NP) sets PKV_DEVERR_SEQ_LEN and is skipped.
  */
 pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
                                              const int64_t* slot_mapping, const int32_t* cow_src,
@@ -266,7 +274,24 @@ pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_ne
                                              const pkv_cache_desc* desc, const int32_t* block_tables,
                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                              int32_t max_seq_len, float scale, void* out, void* workspace,
-                                             size_t workspace_bytes, int32_t partition_tokens, void* stream);
+                                             size_t workspace_bytes, int32_t partition_tokens,
+                                             const int32_t* work_units, int32_t num_work_units, void* stream);
+
+/*
+ * Host work plan for pkv_paged_attention_decode_append (plain C++, no GPU
+ * work; with partition_tokens 0 it asks the device for its SM count, as the
+ * decode's automatic choice does).  Writes to units[0 .. *num_units) every
+ * unit s * NP + partition of the batch (every partition of every row, one
+ * for a zero-length row), sorted by its tokens, longest first (ties: unit
+ * order), so that the last CTAs to start are the shortest
+ * (longest-processing-time-first list scheduling).  seq_lens: HOST copy of
+ * the decode call's array; num_kv_heads, max_seq_len, partition_tokens: as
+ * passed to it.  *num_units always receives the count; PKV_ERR_WORKSPACE if
+ * it exceeds units_cap (nothing written).  A length outside [0,
+ * max_seq_len] returns PKV_ERR_INVALID.
+ */
+pkv_status pkv_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_kv_heads, int32_t max_seq_len,
+                           int32_t partition_tokens, int32_t* units, int32_t units_cap, int32_t* num_units);
 
 /*
  * Shared-prefix ("cascade") decode attention: the same function as

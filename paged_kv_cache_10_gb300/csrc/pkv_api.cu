@@ -1,9 +1,11 @@
 // pkv_api.cu -- C ABI entry points for decode attention, the device error
 // word, status strings.  Argument meaning, layout, ownership and error
 // behaviour are specified in include/pagedkv.h.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -225,8 +227,10 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
                          const void* k_cache, const void* v_cache, const pkv_cache_desc* d,
                          const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                          int32_t max_seq_len, float scale, void* out, void* workspace, size_t ws_bytes,
-                         int32_t partition_tokens, void* stream, const FusedAppend* app) {
+                         int32_t partition_tokens, void* stream, const FusedAppend* app,
+                         const int32_t* work = nullptr, int32_t num_work = 0) {
     // ---- validation (host, before any launch)
+    if (num_work < 0 || (!work && num_work > 0)) return PKV_ERR_INVALID;
     if (!d || num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
         partition_tokens < 0)
         return PKV_ERR_INVALID;
@@ -245,8 +249,9 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
     const int G = num_q_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || d->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PKV_OK;
+    if (num_seqs == 0 || (work && num_work == 0)) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PKV_ERR_INVALID;
+    if (static_cast<int64_t>(num_work) * d->num_kv_heads > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return PKV_ERR_INVALID;
@@ -288,6 +293,8 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
     p.qk_scale = scale * log2e * (d->kv_dtype == PKV_FP8_E4M3 ? d->k_scale : 1.f);
     p.v_scale = d->kv_dtype == PKV_FP8_E4M3 ? d->v_scale : 1.f;
     p.err = err;
+    p.work = work;
+    p.num_work = num_work;
     if (need > 0) partials_layout(p, workspace);
     if (app) {
         p.k_new = app->k;
@@ -359,11 +366,46 @@ extern "C" pkv_status pkv_paged_attention_decode_append(const void* k_new, const
                                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
                                                         const int32_t* seq_lens, int32_t max_seq_len, float scale,
                                                         void* out, void* workspace, size_t ws_bytes,
-                                                        int32_t partition_tokens, void* stream) {
+                                                        int32_t partition_tokens, const int32_t* work_units,
+                                                        int32_t num_work_units, void* stream) {
     const FusedAppend app{k_new, v_new, in_dtype, slot_mapping, cow_src};
     return decode_common(q, q_dtype, num_seqs, num_q_heads, k_cache, v_cache, d, block_tables, max_blocks_per_seq,
                          seq_lens, max_seq_len, scale, out, workspace, ws_bytes, partition_tokens, stream,
-                         num_seqs > 0 ? &app : nullptr);
+                         num_seqs > 0 ? &app : nullptr, work_units, num_work_units);
+}
+
+// Host work plan for the decode: the batch's (sequence, partition) units,
+// longest first.  See pagedkv.h.
+extern "C" pkv_status pkv_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t num_kv_heads,
+                                      int32_t max_seq_len, int32_t partition_tokens, int32_t* units,
+                                      int32_t units_cap, int32_t* num_units) {
+    if (!num_units) return PKV_ERR_INVALID;
+    *num_units = 0;
+    if (num_seqs < 0 || num_kv_heads <= 0 || max_seq_len < 0 || partition_tokens < 0 || units_cap < 0 ||
+        partition_tokens % kBlockSize)
+        return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!seq_lens) return PKV_ERR_INVALID;
+    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, num_kv_heads, max_seq_len);
+    const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
+    if (NP * num_seqs > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    std::vector<std::pair<int64_t, int32_t>> list;  // (tokens, unit)
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t L = seq_lens[s];
+        if (L < 0 || L > max_seq_len) return PKV_ERR_INVALID;
+        const int64_t n = L > 0 ? ceil_div(L, P) : 1;  // a zero-length row still has a unit (it writes zeros)
+        for (int64_t part = 0; part < n; ++part)
+            list.emplace_back(std::min<int64_t>(P, L - part * P), static_cast<int32_t>(s * NP + part));
+    }
+    std::stable_sort(list.begin(), list.end(),
+                     [](const std::pair<int64_t, int32_t>& a, const std::pair<int64_t, int32_t>& b) {
+                         return a.first > b.first;
+                     });
+    *num_units = static_cast<int32_t>(list.size());
+    if (static_cast<int64_t>(list.size()) > units_cap) return PKV_ERR_WORKSPACE;
+    if (!units) return PKV_ERR_INVALID;
+    for (size_t i = 0; i < list.size(); ++i) units[i] = list[i].second;
+    return PKV_OK;
 }
 
 extern "C" pkv_status pkv_get_device_error(uint32_t* flags, void* stream) {

@@ -80,6 +80,29 @@ struct DecodeSmem {
     }
 };
 
+// This CTA's (partition, KV head, sequence): from the grid, or from the
+// host's work list (unit = s * (NP - part_base) + partition, KV head
+// fastest).  A unit outside the batch sets PKV_DEVERR_SEQ_LEN; false: skip.
+__device__ __forceinline__ bool decode_unit(const DecodeParams& p, int& part, int& h, int& s) {
+    if (!p.work) {
+        part = blockIdx.x;
+        h = blockIdx.y;
+        s = blockIdx.z;
+        return true;
+    }
+    const int64_t lin = blockIdx.x;
+    const int u = __ldg(p.work + lin / p.Hkv);
+    const int npl = p.NP - p.part_base;
+    h = static_cast<int>(lin % p.Hkv);
+    if (u < 0 || static_cast<int64_t>(u) >= static_cast<int64_t>(p.S) * npl) {
+        if (threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
+        return false;
+    }
+    s = u / npl;
+    part = u % npl;
+    return true;
+}
+
 template <int D, int G, typename KT, typename QT, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     constexpr int VEC = D / 16;               // elements of a row per lane
@@ -96,7 +119,8 @@ __global__ void __launch_bounds__(NW * 32) decode_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     allow_dependent_launch();  // the merge may stage its CTAs behind this grid's last wave
     const int hf = lane >> 4, li = lane & 15;
-    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    int part, h, s;
+    if (!decode_unit(p, part, h, s)) return;
 
     // Sequence length, clamped to the block table's reach and to the
     // partitions this launch covers; the sequence's own range starts after
@@ -395,7 +419,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
+    const dim3 grid = p.work ? dim3(static_cast<unsigned>(static_cast<int64_t>(p.num_work) * p.Hkv))
+                             : dim3(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
     kern<<<grid, NW * 32, SMEM, st>>>(p);
     return cudaGetLastError();
 }

@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     allow_dependent_launch();  // the merge may stage its CTAs behind this grid's last wave
     const int g8 = lane >> 2, qd = lane & 3;  // fragment row group / quad member
-    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    int part, h, s;
+    if (!decode_unit(p, part, h, s)) return;
 
     // Sequence length, clamped to the block table's reach and to the
     // partitions this launch covers; the sequence's own range starts after
@@ -520,7 +521,8 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, const CUtensorMap& tk, co
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    dim3 grid(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
+    const dim3 grid = p.work ? dim3(static_cast<unsigned>(static_cast<int64_t>(p.num_work) * p.Hkv))
+                             : dim3(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
     kern<<<grid, NW * 32, SMEM, st>>>(p, tk, tv);
     return cudaGetLastError();
 }

@@ -52,6 +52,11 @@ struct DecodeParams {
     int32_t in_dtype = 0;
     float k_enc_scale = 1.f;  // fp8 caches: code = e4m3(x / scale)
     float v_enc_scale = 1.f;
+    // Optional CTA order (host plan): CTA i takes unit work[i / Hkv] =
+    // s * (NP - part_base) + partition and KV head i % Hkv; null: the grid
+    // (partition, KV head, sequence).
+    const int32_t* work = nullptr;
+    int32_t num_work = 0;
 };
 
 // First token of a sequence's own (non-shared) attention range, clamped

@@ -36,7 +36,7 @@ EXPORTED = [
     "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
     "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
-    "pkv_prefill_plan",
+    "pkv_prefill_plan", "pkv_decode_plan",
 ]
 
 
@@ -122,7 +122,8 @@ def lib():
         "pkv_alloc_swap_in": (i32, [P, P, i64, P, i32, P]),
         "pkv_alloc_append_tokens": (i32, [P, P, P, i32, P, i64, P, i32, P]),
         "pkv_paged_attention_decode_append": (i32, [P, P, i32, P, P, P, i32, i32, i32, P, P, D, P, i32, P, i32,
-                                                    ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
+                                                    ctypes.c_float, P, P, ctypes.c_size_t, i32, P, i32, P]),
+        "pkv_decode_plan": (i32, [P, i32, i32, i32, i32, P, i32, P]),
         "pkv_block_hash": (ctypes.c_uint64, [ctypes.c_uint64, P, i32, P, i32]),
         "pkv_prefix_block_hashes": (i32, [P, i64, i32, P, i32, P, P, i64, P]),
         "pkv_alloc_lookup": (i32, [P, P, i32]),
@@ -308,7 +309,7 @@ class PrefixGroups:
 def paged_attention_decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cache, desc: CacheDesc, block_tables,
                                   seq_lens, max_seq_len: int, scale: float, out, workspace=None,
                                   partition_tokens: int = 0, q_dtype: str | None = None, in_dtype: str | None = None,
-                                  cow_src=None, stream=None) -> None:
+                                  cow_src=None, stream=None, work_units=None) -> None:
     """Copy-on-write copies into the appending rows' last blocks (cow_src
     int32 [S], -1 for none), append (one token per batch row, slot_mapping
     int64 [S]) and decode, in one launch."""
@@ -325,8 +326,27 @@ def paged_attention_decode_append(k_new, v_new, slot_mapping, q, k_cache, v_cach
         _dev_ptr(q, "q"), _dtype_code(q, q_dtype), S, Hq,
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
         _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
-        int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes, int(partition_tokens), _stream(stream))
+        int(max_seq_len), float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes, int(partition_tokens),
+        _dev_ptr(work_units, "work_units") if work_units is not None and work_units.numel() else None,
+        int(work_units.numel()) if work_units is not None else 0, _stream(stream))
     _check(st, "paged_attention_decode_append")
+
+
+def decode_plan(seq_lens, num_kv_heads: int, max_seq_len: int, partition_tokens: int = 0) -> np.ndarray:
+    """Host work plan for paged_attention_decode_append: every (sequence,
+    partition) unit, longest first (int32)."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    S = int(sl.size)
+    n = ctypes.c_int32(0)
+    st = lib().pkv_decode_plan(_np_ptr(sl) if S else None, S, int(num_kv_heads), int(max_seq_len),
+                               int(partition_tokens), None, 0, ctypes.byref(n))
+    if st not in (0, 5):
+        _check(st, "decode_plan")
+    out = np.zeros(max(int(n.value), 1), dtype=np.int32)
+    st = lib().pkv_decode_plan(_np_ptr(sl) if S else None, S, int(num_kv_heads), int(max_seq_len),
+                               int(partition_tokens), _np_ptr(out), int(out.size), ctypes.byref(n))
+    _check(st, "decode_plan")
+    return out[: int(n.value)]
 
 
 def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_tables, seq_lens, max_seq_len: int,

@@ -33,7 +33,7 @@ class DecodeStep:
     """Device state and launch sequence of one workload's decode step."""
 
     def __init__(self, wl, device="cuda", partition_tokens=None, alloc: pk.Allocator | None = None,
-                 cascade: bool = False, cascade_min_blocks: int = 16, fused: bool = True):
+                 cascade: bool = False, cascade_min_blocks: int = 16, fused: bool = True, plan="auto"):
         self.wl = wl
         self.device = torch.device(device)
         self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.kv_dtype,
@@ -87,6 +87,28 @@ class DecodeStep:
             ws = pk.decode_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
         self.launches = 0
+        # the fused decode's CTAs in the host plan's order (longest unit
+        # first).  "auto": where that order can pay, i.e. the units' lengths
+        # differ (by a block or more) and no two rows share a block (CTAs of
+        # rows sharing blocks are better co-scheduled in grid order, for L2).
+        self.work = None
+        if plan == "auto":
+            plan = self._plan_pays()
+        if plan and self.fused and wl.S:
+            self.work_host = pk.decode_plan(self.seq_lens, wl.Hkv, self.max_seq_len, self.partition_tokens)
+            self.work = torch.from_numpy(self.work_host).to(dev)
+
+    def _plan_pays(self) -> bool:
+        if not self.fused or self.wl.S == 0:
+            return False
+        used = self.tables[self.tables >= 0]
+        if len(self.pairs) or np.unique(used).size != used.size:
+            return False  # blocks shared between rows
+        P = self.effective_partition()
+        lens = self.seq_lens.astype(np.int64)
+        full = lens // P  # full partitions, plus one partial of lens % P tokens
+        units = np.concatenate([np.full(int(full.sum()), P), (lens % P)[lens % P > 0]])
+        return units.size > 0 and int(units.max() - units.min()) >= self.wl.b
 
     def effective_partition(self) -> int:
         if self.partition_tokens:
@@ -119,7 +141,7 @@ class DecodeStep:
                            in_dtype=self.wl.in_dtype, stream=stream)
 
     def decode(self, stream=None, q=None, tables=None, lens=None, out=None, k=None, v=None, slots=None,
-               cow_src=None):
+               cow_src=None, work=None):
         if self.fused:
             pk.paged_attention_decode_append(
                 self.k_new if k is None else k, self.v_new if v is None else v, self.d_slots if slots is None else slots,
@@ -127,7 +149,8 @@ class DecodeStep:
                 self.d_tables if tables is None else tables, self.d_lens if lens is None else lens, self.max_seq_len,
                 self.wl.scale, self.out if out is None else out, workspace=self.workspace,
                 partition_tokens=self.partition_tokens, q_dtype=self.wl.q_dtype, in_dtype=self.wl.in_dtype,
-                cow_src=(self.d_cow_src if cow_src is None else cow_src) if len(self.pairs) else None, stream=stream)
+                cow_src=(self.d_cow_src if cow_src is None else cow_src) if len(self.pairs) else None, stream=stream,
+                work_units=self.work if work is None else work)
             return
         if self.cascade:
             g = self.groups

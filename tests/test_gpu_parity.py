@@ -414,3 +414,27 @@ def test_sharp_softmax_matches_oracle(lib, kv, G, partition):
                float(np.max(np.abs(oracle.dequantize(wl.v_new, wl.in_dtype)))))
     extra = 0.0 if G == 1 else p_rounding_allowance("bf16" if kv == "bf16" else "f16", vmax)
     assert err <= TOL[kv] + extra, (err, mx, extra)
+
+
+@pytest.mark.parametrize("kv,G,partition", [("bf16", 1, 64), ("bf16", 4, 0), ("e4m3", 8, 256), ("f16", 2, 16)])
+def test_decode_in_plan_order_matches_oracle(lib, kv, G, partition):
+    """The fused decode with its CTAs in the host plan's longest-first order:
+    same rows, pools and appends as the grid order, every element against
+    the oracle; a unit outside the batch is flagged."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    Hkv = 2
+    wl = workloads.custom(f"plan_{kv}", 131 + G, EDGE_LENS + [0, 2050], Hkv * G, Hkv, 128, kv_dtype=kv,
+                          partition_tokens=partition)
+    st = DecodeStep(wl, device="cuda", plan=True)
+    assert st.work is not None and len(set(st.work_host.tolist())) == len(st.work_host)
+    st.run()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    err, mx = check_step(st)
+    assert err <= TOL[kv], (err, mx)
+    bad = torch.from_numpy(np.concatenate([st.work_host, np.array([10 ** 6], np.int32)])).cuda()
+    st.work = bad
+    st.decode()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_SEQ_LEN

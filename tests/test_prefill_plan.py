@@ -81,3 +81,28 @@ def test_plan_errors(pk):
         pk.prefill_plan(qs, lens, 12, 8, 20)
     # nothing to do
     assert pk.prefill_plan(np.array([0], np.int32), np.zeros(0, np.int32), 8, 8, 20).size == 0
+
+
+def test_decode_plan_lists_every_unit_longest_first(pk):
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 5000, 300).astype(np.int32)
+    lens[7] = 0
+    P = 512
+    got = pk.decode_plan(lens, 8, int(lens.max()), P)
+    NP = -(-int(lens.max()) // P)
+    want = []
+    for s, L in enumerate(lens.tolist()):
+        n = -(-L // P) if L > 0 else 1
+        for p in range(n):
+            want.append((-min(P, L - p * P), s * NP + p))
+    want.sort()
+    assert got.tolist() == [u for _, u in want]
+    # lengths beyond the bound: invalid; more units than the cap: the count comes back
+    with pytest.raises(pk.PagedKVError):
+        pk.decode_plan(np.array([10, 600], np.int32), 8, 500, 512)
+    import ctypes
+    n = ctypes.c_int32(-1)
+    out = np.zeros(1, np.int32)
+    st = pk.lib().pkv_decode_plan(pk._np_ptr(lens), lens.size, 8, int(lens.max()), P, pk._np_ptr(out), 1,
+                                  ctypes.byref(n))
+    assert st == 5 and n.value == len(want)
