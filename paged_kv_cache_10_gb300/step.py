@@ -88,9 +88,10 @@ class DecodeStep:
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
         self.launches = 0
         # the fused decode's CTAs in the host plan's order (longest unit
-        # first).  "auto": where that order can pay, i.e. the units' lengths
-        # differ (by a block or more) and no two rows share a block (CTAs of
-        # rows sharing blocks are better co-scheduled in grid order, for L2).
+        # first).  "auto": where that order can pay, i.e. there is more than
+        # a wave of CTAs, the units' lengths differ (by a block or more) and
+        # no two rows share a block (CTAs of rows sharing blocks are better
+        # co-scheduled in grid order, for L2).
         self.work = None
         if plan == "auto":
             plan = self._plan_pays()
@@ -108,7 +109,10 @@ class DecodeStep:
         lens = self.seq_lens.astype(np.int64)
         full = lens // P  # full partitions, plus one partial of lens % P tokens
         units = np.concatenate([np.full(int(full.sum()), P), (lens % P)[lens % P > 0]])
-        return units.size > 0 and int(units.max() - units.min()) >= self.wl.b
+        sms = torch.cuda.get_device_properties(self.device).multi_processor_count if self.device.type == "cuda" else 1
+        if units.size * self.wl.Hkv <= 2 * sms:
+            return False  # one wave: the order does not matter
+        return int(units.max() - units.min()) >= self.wl.b
 
     def effective_partition(self) -> int:
         if self.partition_tokens:
