@@ -266,6 +266,9 @@ pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t q_dtype, in
  *   unit of a batch longest first.  A list must hold every unit of the batch
  *   (a row whose units are missing is left undefined, and so is its append);
  *   a unit outside [0, num_seqs * NP) sets PKV_DEVERR_SEQ_LEN and is skipped.
+ *   With a list and partition_tokens 0 the automatic partition size has no
+ *   2048-token cap (long CTAs start first, so it only adds merge work);
+ *   pkv_decode_plan with partition_tokens 0 uses that same size.
  */
 pkv_status pkv_paged_attention_decode_append(const void* k_new, const void* v_new, int32_t in_dtype,
                                              const int64_t* slot_mapping, const int32_t* cow_src,
@@ -411,9 +414,12 @@ pkv_status pkv_prefill_plan(const int32_t* query_start, const int32_t* seq_lens,
 /*
  * Partition size the automatic choice (partition_tokens = 0) would use for
  * these sizes on the current device, or a negative pkv_status on error.
+ * planned != 0: the size for a launch with a work list (no 2048-token cap,
+ * see pkv_paged_attention_decode_append); 0: grid order (every other decode
+ * entry point).
  */
 int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                  int32_t head_size, int32_t max_seq_len);
+                                  int32_t head_size, int32_t max_seq_len, int32_t planned);
 
 /*
  * Decode kernel selection for subsequent pkv_paged_attention_decode calls

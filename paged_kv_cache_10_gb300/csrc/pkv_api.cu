@@ -145,19 +145,22 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Tokens per split-K partition when the caller passes 0.  Enough CTAs for a
 // few waves of resident CTAs keep the SMs evenly loaded when sequence
 // lengths differ; beyond that, splitting only adds partial-result traffic.
-// A CTA never takes more than kAutoMaxPartition tokens, so a few long
-// sequences cannot leave the last wave running alone (measured on GB300:
-// 64 x U[512, 4096] MHA decodes 2.4 % faster with 2048-token partitions;
-// sequences of <= 2048 tokens are not split by this cap).
+// In grid order a CTA never takes more than kAutoMaxPartition tokens, so a
+// few long sequences cannot leave the last wave running alone (measured on
+// GB300: 64 x U[512, 4096] MHA decodes 2.4 % faster with 2048-token
+// partitions; sequences of <= 2048 tokens are not split by this cap).  A
+// launch in a host plan's longest-first order (planned) starts the long
+// CTAs first, so there the cap only adds merge work and is dropped (the same
+// batch: 341.4 against 346.2 us).
 constexpr int kAutoMaxPartition = 2048;
 
-int auto_partition(int S, int Hkv, int max_seq_len) {
+int auto_partition(int S, int Hkv, int max_seq_len, bool planned) {
     const int64_t units = static_cast<int64_t>(S) * Hkv;
     const int64_t want = static_cast<int64_t>(num_sms()) * 2 * 4;
     int64_t parts = ceil_div(want, units > 0 ? units : 1);
     if (parts < 1) parts = 1;
     int64_t P = ceil_div(ceil_div(max_seq_len > 0 ? max_seq_len : 1, parts), kBlockSize) * kBlockSize;
-    if (P > kAutoMaxPartition) P = kAutoMaxPartition;
+    if (!planned && P > kAutoMaxPartition) P = kAutoMaxPartition;
     if (P < kAutoMinPartition) P = kAutoMinPartition;
     return static_cast<int>(P);
 }
@@ -207,10 +210,10 @@ extern "C" size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
 }
 
 extern "C" int32_t pkv_decode_auto_partition(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                             int32_t head_size, int32_t max_seq_len) {
+                                             int32_t head_size, int32_t max_seq_len, int32_t planned) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_size <= 0 || max_seq_len < 0)
         return -static_cast<int32_t>(PKV_ERR_INVALID);
-    return auto_partition(num_seqs, num_kv_heads, max_seq_len);
+    return auto_partition(num_seqs, num_kv_heads, max_seq_len, planned != 0);
 }
 
 namespace {
@@ -265,7 +268,8 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
         if (!same16 && !to_fp8) return PKV_ERR_UNSUPPORTED;
     }
 
-    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len);
+    const int P =
+        partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len, work != nullptr);
     const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
     if (NP > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     const size_t need = workspace_bytes(num_seqs, num_q_heads, d->head_size, max_seq_len, P);
@@ -386,7 +390,7 @@ extern "C" pkv_status pkv_decode_plan(const int32_t* seq_lens, int32_t num_seqs,
         return PKV_ERR_INVALID;
     if (num_seqs == 0) return PKV_OK;
     if (!seq_lens) return PKV_ERR_INVALID;
-    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, num_kv_heads, max_seq_len);
+    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, num_kv_heads, max_seq_len, true);
     const int64_t NP = max_seq_len > 0 ? ceil_div(max_seq_len, P) : 1;
     if (NP * num_seqs > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
     std::vector<std::pair<int64_t, int32_t>> list;  // (tokens, unit)

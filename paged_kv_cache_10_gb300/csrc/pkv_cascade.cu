@@ -104,7 +104,7 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     const int64_t pool_rows = static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * kBlockSize;
     if (pool_rows > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
 
-    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len);
+    const int P = partition_tokens > 0 ? partition_tokens : auto_partition(num_seqs, d->num_kv_heads, max_seq_len, false);
     const int npp = num_groups > 0 ? prefix_partitions(max_group_blocks) : 0;
     const int64_t nps = max_seq_len > 0 ? cdiv(max_seq_len, P) : 1;
     const int64_t NP = npp + nps;

@@ -120,7 +120,7 @@ cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, in
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);
 
 // Host helpers shared by the entry points (pkv_api.cu).
-int auto_partition(int S, int Hkv, int max_seq_len);
+int auto_partition(int S, int Hkv, int max_seq_len, bool planned);
 bool encode_pool_map(CUtensorMap* map, const void* base, int elem_bytes, int64_t rows, int D);
 // 3-D view of a 16-bit [T][H][D] tensor with a box of 64 elements x box_h x
 // box_t and the 128-byte swizzle (a box lands as box_t * box_h rows of 128

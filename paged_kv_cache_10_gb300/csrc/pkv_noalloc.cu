@@ -66,7 +66,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(const void* q, int32_t 
     // Resolve the partition size first so the scratch need is exact.
     int32_t P = partition_tokens;
     if (P == 0) {
-        P = pkv_decode_auto_partition(num_seqs, num_q_heads, desc->num_kv_heads, desc->head_size, max_seq_len);
+        P = pkv_decode_auto_partition(num_seqs, num_q_heads, desc->num_kv_heads, desc->head_size, max_seq_len, 0);
         if (P < 0) return static_cast<pkv_status>(-P);
     }
     const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, desc->head_size, max_seq_len, P);

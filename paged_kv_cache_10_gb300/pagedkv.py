@@ -92,7 +92,7 @@ def lib():
                                              P, P, ctypes.c_size_t, i32, P]),
         "pkv_paged_attention_decode_noalloc": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, ctypes.c_float,
                                                      P, i32, P]),
-        "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32]),
+        "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32, i32]),
         "pkv_get_device_error": (i32, [u32p, P]),
         "pkv_set_decode_path": (i32, [i32]),
         "pkv_get_decode_path": (i32, []),
@@ -214,8 +214,9 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: int, max_
     return int(lib().pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len, partition_tokens))
 
 
-def decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len) -> int:
-    r = int(lib().pkv_decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len))
+def decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len, planned: bool = False) -> int:
+    r = int(lib().pkv_decode_auto_partition(num_seqs, num_q_heads, num_kv_heads, head_size, max_seq_len,
+                                            1 if planned else 0))
     if r < 0:
         _check(-r, "decode_auto_partition")
     return r

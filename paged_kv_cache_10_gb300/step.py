@@ -105,7 +105,7 @@ class DecodeStep:
         used = self.tables[self.tables >= 0]
         if len(self.pairs) or np.unique(used).size != used.size:
             return False  # blocks shared between rows
-        P = self.effective_partition()
+        P = self.effective_partition(planned=True)
         lens = self.seq_lens.astype(np.int64)
         full = lens // P  # full partitions, plus one partial of lens % P tokens
         units = np.concatenate([np.full(int(full.sum()), P), (lens % P)[lens % P > 0]])
@@ -114,10 +114,14 @@ class DecodeStep:
             return False  # one wave: the order does not matter
         return int(units.max() - units.min()) >= self.wl.b
 
-    def effective_partition(self) -> int:
+    def effective_partition(self, planned=None) -> int:
+        """Tokens per split-K partition of this step's decode (a planned
+        launch's automatic size has no cap)."""
         if self.partition_tokens:
             return self.partition_tokens
-        return pk.decode_auto_partition(self.wl.S, self.wl.Hq, self.wl.Hkv, self.wl.D, self.max_seq_len)
+        if planned is None:
+            planned = getattr(self, "work", None) is not None
+        return pk.decode_auto_partition(self.wl.S, self.wl.Hq, self.wl.Hkv, self.wl.D, self.max_seq_len, planned)
 
     def kernel_launches(self) -> int:
         """Number of kernels one ``run`` enqueues."""

@@ -114,3 +114,20 @@ def test_prefill_validation_rejects_before_any_launch(pk):
     assert call(scale=0.0) == pk.ERR_INVALID           # the row maximum needs scale > 0
     assert call(Hq=6) == pk.ERR_UNSUPPORTED            # 3 query heads per KV head
     assert call(Hq=5) == pk.ERR_INVALID                # heads not a multiple
+
+
+def test_header_declares_every_exported_function_in_c(pk, tmp_path):
+    """include/pagedkv.h compiles as C99 and C++17 without warnings and
+    declares every function the binding loads (a stray comment would hide
+    a declaration from C callers while the library still builds)."""
+    import shutil
+    import subprocess
+    if not shutil.which("gcc") or not shutil.which("g++"):
+        pytest.skip("no host compiler")
+    refs = "\n".join(f"    (void)&{s};" for s in sorted(pk.EXPORTED))
+    src = tmp_path / "use_header.c"
+    src.write_text(f'#include "pagedkv.h"\nint main(void) {{\n{refs}\n    return 0;\n}}\n')
+    inc = os.path.dirname(HEADER)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, "-fsyntax-only", str(src)], check=True)
+    subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", "-I", inc, "-fsyntax-only", "-x", "c++", str(src)],
+                   check=True)
