@@ -532,9 +532,11 @@ def prefill_flops(wl) -> float:
 
 def prefill_bytes(wl) -> int:
     """Least bytes the step must move: q and out, every key / value of each
-    sequence once per KV head, the appended k / v (read and written)."""
-    kv = sum(wl.seq_lens) * 2 * wl.Hkv * wl.D * 2
-    return 2 * wl.T * wl.Hq * wl.D * 2 + kv + wl.T * 2 * wl.Hkv * wl.D * 2 * 2
+    sequence once per KV head, the appended k / v (read in q's type, written
+    in the pool's)."""
+    e = 1 if wl.kv_dtype == "e4m3" else 2
+    kv = sum(wl.seq_lens) * 2 * wl.Hkv * wl.D * e
+    return 2 * wl.T * wl.Hq * wl.D * 2 + kv + wl.T * 2 * wl.Hkv * wl.D * (2 + e)
 
 
 def measured_tensor_peak():
@@ -555,7 +557,7 @@ def prefill_cpu_baseline(wl, budget_s=10.0):
     slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
     tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
-    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
     qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
     m, flops, dt, reps = 8, 0.0, 0.0, 0
     while dt < budget_s and reps < 10000:
@@ -567,8 +569,8 @@ def prefill_cpu_baseline(wl, budget_s=10.0):
         ctx = int(lens[s]) - wl.qlens[s]
         q = np.ascontiguousarray(wl.q[qs[s]:qs[s] + n])
         t = time.perf_counter()
-        oracle.paged_prefill(q, wl.dtype, np.array([0, n], np.int32), kp, vp, wl.dtype, tables[s:s + 1],
-                             np.array([ctx + n], np.int32), wl.scale)
+        oracle.paged_prefill(q, wl.dtype, np.array([0, n], np.int32), kp, vp, wl.kv_dtype, tables[s:s + 1],
+                             np.array([ctx + n], np.int32), wl.scale, wl.k_scale, wl.v_scale)
         dt += time.perf_counter() - t
         flops += 4.0 * wl.D * wl.Hq * (n * ctx + n * (n + 1) // 2)
         if reps == 0 and dt < budget_s / 50:
@@ -645,7 +647,7 @@ def run_prefill(args, rank, world, local_rank):
         pk.paged_kv_append(dd["k"], dd["v"], dd["slots"], step.k_cache, step.v_cache, step.desc, in_dtype=wl.dtype)
         pk.paged_attention_prefill(dd["q"], step.k_cache, step.v_cache, step.desc, dd["qs"], wl.max_query_len,
                                    dd["tables"], dd["lens"], wl.scale, o, q_dtype=wl.dtype,
-                                   work_units=dd.get("work"))
+                                   work_units=dd.get("work"), workspace=step.workspace)
 
     e2e_ms, h2d = (e2e_pipelined(h, launch_prefill, step.out, Ke, stream, flush_buf if flush else None) if Ke
                    else (0.0, h2d))
@@ -664,9 +666,11 @@ def run_prefill(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "us_per_step": round(1e3 * total_ms / K, 2),
         "median_us_per_step": round(1e3 * statistics.median(a.elapsed_time(c) for a, _, c in ev), 2),
         "tokens_per_s": round(world * wl.T / (tot_s / K), 1), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype + ", fp32 accumulate", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": (f"e4m3 KV, {wl.dtype} q" if wl.kv_dtype == "e4m3" else wl.dtype) + ", fp32 accumulate",
+        "data": "synthetic",
         "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D,
-                   "new_tokens": wl.T, "chunk_tokens": wl.qlens, "context_tokens": wl.ctx, "num_blocks": wl.NB,
+                   "kv_dtype": wl.kv_dtype, "new_tokens": wl.T, "chunk_tokens": wl.qlens, "context_tokens": wl.ctx, "num_blocks": wl.NB,
                    "flops_per_step": flops, "min_bytes_per_step": nbytes,
                    "l2": ("flushed between steps (2x L2 write)" if flush else "inputs larger than L2, no flush"),
                    "cta_order": ("host plan, longest causal key range first" if step.work is not None
@@ -677,7 +681,9 @@ def run_prefill(args, rank, world, local_rank):
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name, "prefill"),
-                     "peak_kind": peak_kind, "kernel": "prefill_tc_kernel",
+                     "peak_kind": peak_kind,
+                     "kernel": ("stage_fp8_kernel + prefill_tc_kernel (timed together)" if step.workspace is not None
+                                else "prefill_tc_kernel"),
                      "kernel_sources_hash": kernel_hash("prefill"), "mean_launch_us": round(a_ms * 1e3, 2),
                      "median_launch_us": round(statistics.median(attn_ms) * 1e3, 2),
                      "algorithmic_flops_per_launch": flops,
@@ -785,7 +791,7 @@ def run_reference_prefill(args, wl):
     slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
     tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
-    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
     qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
     m = 4
 
@@ -794,7 +800,8 @@ def run_reference_prefill(args, wl):
         n = min(m, wl.qlens[s])
         ctx = int(lens[s]) - wl.qlens[s]
         oracle.paged_prefill(np.ascontiguousarray(wl.q[qs[s]:qs[s] + n]), wl.dtype, np.array([0, n], np.int32), kp, vp,
-                             wl.dtype, tables[s:s + 1], np.array([ctx + n], np.int32), wl.scale)
+                             wl.kv_dtype, tables[s:s + 1], np.array([ctx + n], np.int32), wl.scale,
+                             wl.k_scale, wl.v_scale)
         return 4.0 * wl.D * wl.Hq * (n * ctx + n * (n + 1) // 2)
 
     K, W = args.steps, args.warmup
@@ -810,7 +817,8 @@ def run_reference_prefill(args, wl):
         "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": K, "warmup": W, "ms_per_step": round(1e3 * t / K, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D},
+        "config": {"workload": wl.name, "num_seqs": wl.S, "q_heads": wl.Hq, "kv_heads": wl.Hkv, "head_size": wl.D,
+                   "kv_dtype": wl.kv_dtype},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"the first {m} tokens of one chunk of {wl.name} per step (all heads), rotating: "
                                    f"float64 causal attention"},

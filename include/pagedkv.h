@@ -367,10 +367,24 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  *   PKV_DEVERR_SEQ_LEN and its rows past the bound may be left unwritten.
  * Rows of out outside every sequence's range are not written.
  * scale must be finite and > 0 (else PKV_ERR_INVALID).
- * Implemented for f16 / bf16 pools with q of the same type, head_size 64 or
- * 128, num_q_heads / num_kv_heads in {1, 2, 4, 8}, and at most 2^31 - 1 CTAs
- * (ceil(max_query_len * G / 256) * num_kv_heads * num_seqs, G = num_q_heads /
- * num_kv_heads); others return PKV_ERR_UNSUPPORTED.
+ * Implemented for f16 / bf16 pools with q of the same type, fp8 E4M3 pools
+ * with f16 or bf16 q, head_size 64 or 128, num_q_heads / num_kv_heads in
+ * {1, 2, 4, 8}, and at most 2^31 - 1 CTAs (ceil(max_query_len * G / 256) *
+ * num_kv_heads * num_seqs, G = num_q_heads / num_kv_heads); others return
+ * PKV_ERR_UNSUPPORTED.  out has q's type.
+ * fp8 pools: the keys and values are desc->k_scale * code and
+ * desc->v_scale * code (both finite and > 0, else PKV_ERR_INVALID).  A first
+ * kernel, on the same stream, copies the blocks the batch reaches (the first
+ * ceil(seq_lens[s] / 16) entries of each block-table row) into 16-bit
+ * blocks of q's type in the workspace -- exact, since every E4M3 value is an
+ * f16 and a bf16 value -- and the attention pass reads that copy.
+ * workspace, workspace_bytes: device memory of at least
+ * pkv_prefill_workspace_bytes(desc->kv_dtype, num_seqs, num_kv_heads,
+ * head_size, max_blocks_per_seq) bytes, 16-byte aligned, owned by the
+ * caller and not read or written by any other work until this call's
+ * kernels finish in stream order (else PKV_ERR_WORKSPACE).  16-bit pools
+ * need none (NULL, 0).  num_seqs * max_blocks_per_seq * num_kv_heads * 16
+ * must stay below 2^31 for an fp8 pool (else PKV_ERR_UNSUPPORTED).
  * work_units, num_work_units: the order in which the CTAs start.  A CTA
  * covers unit u = s * nq + qt (sequence s, its query rows [qt * r, (qt + 1) *
  * r) with r = 256 / G tokens, nq = ceil(max_query_len / r)) for one KV head.
@@ -382,14 +396,25 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * Inconsistent query_start / seq_lens (n_s < 0,
  * n_s > seq_lens[s], past num_tokens or the block table) set
  * PKV_DEVERR_SEQ_LEN and the sequence is skipped; a block id outside the pool
- * sets PKV_DEVERR_BLOCK_ID.  Needs no workspace.
+ * sets PKV_DEVERR_BLOCK_ID (for an fp8 pool the block reads as zeros).
  */
 pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype, int32_t num_tokens, int32_t num_q_heads,
                                        int32_t num_seqs, const int32_t* query_start, int32_t max_query_len,
                                        const void* k_cache, const void* v_cache, const pkv_cache_desc* desc,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* seq_lens, const int32_t* work_units,
-                                       int32_t num_work_units, float scale, void* out, void* stream);
+                                       int32_t num_work_units, float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes pkv_paged_attention_prefill needs: 0 for an f16 / bf16
+ * pool; for an fp8 E4M3 pool 2 * 2 * num_seqs * max_blocks_per_seq *
+ * num_kv_heads * 16 * head_size bytes of 16-bit block copies plus a 4-byte
+ * block-table entry per (sequence, block), each part rounded up to 256 bytes.
+ * Returns 0 for a negative count or a non-positive num_kv_heads / head_size.
+ */
+size_t pkv_prefill_workspace_bytes(int32_t kv_dtype, int32_t num_seqs, int32_t num_kv_heads, int32_t head_size,
+                                   int32_t max_blocks_per_seq);
 
 /*
  * Host work plan for pkv_paged_attention_prefill (plain C++, no GPU):

@@ -84,7 +84,8 @@ struct PrefillParams {
     int32_t max_query_len;       // the caller's bound on every chunk
     const int32_t* work;         // [num_work] units s * num_qtiles + qt in start order, or null
     int32_t num_work;
-    float qk_scale;              // scale * log2(e)
+    float qk_scale;              // scale * log2(e) (* k_scale for a staged fp8 pool)
+    float o_scale = 1.f;         // factor on O / l: v_scale for a staged fp8 pool
     unsigned int* err;
     // cascade prefix pass only
     const int32_t* group_offsets;  // [groups + 1]
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (live) ok = warp_all(tc::wait_spin(o_done + X, (ntx - 1) & 1));
         if (live && ok) {
             tc::fence_after();
-            const float inv = 1.f / l;
+            const float inv = p.o_scale / l;
             if constexpr (!kPrefix) {
                 typename T::storage* orow =
                     reinterpret_cast<typename T::storage*>(p.out) +
@@ -735,6 +736,90 @@ cudaError_t launch_prefill(const PrefillParams& p, int D, const CUtensorMap& tq,
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// ------------------------------------------------------- fp8 pools: staging
+// The tensor-core kind::f16 MMA takes 16-bit operands on both sides, so
+// before the attention pass the blocks the batch reaches are copied out of
+// an E4M3 pool into a 16-bit copy in q's type.  The copy is exact (every
+// E4M3 value is also an f16 and a bf16 value); k_scale joins the score
+// scale and v_scale the final 1 / l, so the scales cost no rounding of the
+// cached codes.  Copy block s * MB + j holds sequence s's logical block j,
+// and the copy's block table says so.
+//
+// Workspace: the copy's block table int32 [S][MB], then the K copy and the
+// V copy, each [S * MB][Hkv][16][D] 16-bit, all on 256-byte boundaries.
+struct StageLayout {
+    int64_t table_off, k_off, v_off, bytes;
+};
+
+StageLayout stage_layout(int64_t S, int64_t MB, int64_t Hkv, int64_t D) {
+    const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+    StageLayout l{};
+    const int64_t copy = S * MB * Hkv * kBlockSize * D * 2;
+    l.table_off = 0;
+    l.k_off = up(S * MB * 4);
+    l.v_off = l.k_off + up(copy);
+    l.bytes = l.v_off + up(copy);
+    return l;
+}
+
+// One CTA per (logical block j, sequence s, pool z: 0 keys, 1 values):
+// converts the block's codes of every KV head.  A thread takes 8 codes (8 bytes in, one 16-byte
+// vector out), so each warp reads 256 and writes 512 contiguous bytes, and it
+// issues kStageUnroll loads before it converts.  Blocks at or past the
+// sequence's length are skipped; a block id outside the pool is reported and
+// its copy zeroed (the attention pass then reads zeros, not stale bytes).
+constexpr int kStageUnroll = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) stage_fp8_kernel(const uint8_t* __restrict__ k_cache,
+                                                        const uint8_t* __restrict__ v_cache,
+                                                        const int32_t* __restrict__ block_tables,
+                                                        const int32_t* __restrict__ seq_lens, int MB, int NB,
+                                                        int block_vecs, uint4* __restrict__ k_copy,
+                                                        uint4* __restrict__ v_copy, int32_t* __restrict__ table_copy,
+                                                        unsigned int* err) {
+    constexpr bool kBF = std::is_same<T, BF16>::value;
+    const int j = blockIdx.x, s = blockIdx.y, z = blockIdx.z;
+    const int L = __ldg(seq_lens + s);  // the attention pass reports a bad length
+    const int nblk = L <= 0 ? 0 : min((L + kBlockSize - 1) / kBlockSize, MB);
+    if (j >= nblk) return;
+    const int64_t dst = static_cast<int64_t>(s) * MB + j;
+    const int id = __ldg(block_tables + dst);
+    const bool bad = id < 0 || id >= NB;
+    if (threadIdx.x == 0 && z == 0) {
+        table_copy[dst] = static_cast<int32_t>(dst);
+        if (bad) report(err, PKV_DEVERR_BLOCK_ID);
+    }
+    // block_vecs: 16-byte output vectors per block and pool (Hkv * 16 * D / 8)
+    const int64_t src = static_cast<int64_t>(bad ? 0 : id) * block_vecs;
+    const uint2* sp = reinterpret_cast<const uint2*>(z ? v_cache : k_cache) + src;
+    uint4* dp = (z ? v_copy : k_copy) + dst * block_vecs;
+    const int total = block_vecs;
+    for (int base = 0; base < total; base += kStageUnroll * blockDim.x) {
+        uint2 w[kStageUnroll];
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            w[u] = make_uint2(0u, 0u);
+            if (i < total && !bad) w[u] = __ldcs(sp + i);  // read once
+        }
+#pragma unroll
+        for (int u = 0; u < kStageUnroll; ++u) {
+            const int i = base + u * blockDim.x + threadIdx.x;
+            if (i >= total) continue;
+            const uint32_t words[2] = {w[u].x, w[u].y};
+            float f[8];
+            Unpack<E4M3, 8>::run(words, f);
+            uint4 o;
+            o.x = pack2<kBF>(f[0], f[1]);
+            o.y = pack2<kBF>(f[2], f[3]);
+            o.z = pack2<kBF>(f[4], f[5]);
+            o.w = pack2<kBF>(f[6], f[7]);
+            dp[i] = o;
+        }
+    }
+}
+
 }  // namespace
 
 int prefix_partitions(int blocks) { return (blocks + kPrefixPartitionBlocks - 1) / kPrefixPartitionBlocks; }
@@ -776,7 +861,8 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
                                                   const pkv_cache_desc* desc, const int32_t* block_tables,
                                                   int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                                   const int32_t* work_units, int32_t num_work_units, float scale,
-                                                  void* out, void* stream) {
+                                                  void* out, void* workspace, size_t workspace_bytes,
+                                                  void* stream) {
     if (!desc || num_tokens < 0 || num_seqs < 0 || max_query_len < 0 || num_q_heads <= 0) return PKV_ERR_INVALID;
     if (num_work_units < 0 || (!work_units && num_work_units > 0)) return PKV_ERR_INVALID;
     if (desc->block_size != kBlockSize || desc->num_kv_heads <= 0 || desc->num_blocks <= 0) return PKV_ERR_INVALID;
@@ -784,17 +870,55 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     const int G = num_q_heads / desc->num_kv_heads;
     const int D = desc->head_size;
     if ((D != 64 && D != 128) || (G != 1 && G != 2 && G != 4 && G != 8)) return PKV_ERR_UNSUPPORTED;
-    if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-    if (q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
+    const bool fp8 = desc->kv_dtype == PKV_FP8_E4M3;
+    if (desc->kv_dtype != PKV_F16 && desc->kv_dtype != PKV_BF16 && !fp8) return PKV_ERR_UNSUPPORTED;
+    if (fp8 ? (q_dtype != PKV_F16 && q_dtype != PKV_BF16) : q_dtype != desc->kv_dtype) return PKV_ERR_UNSUPPORTED;
     if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID;  // finite, > 0 (max on raw scores)
+    if (fp8 && !(desc->k_scale > 0.f && desc->k_scale < 3.0e38f && desc->v_scale > 0.f && desc->v_scale < 3.0e38f))
+        return PKV_ERR_INVALID;
+    if (fp8 && !(scale * desc->k_scale < 3.0e38f)) return PKV_ERR_INVALID;
     if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0 || (work_units && num_work_units == 0)) return PKV_OK;
     if (!q || !out || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start) return PKV_ERR_INVALID;
     if (max_blocks_per_seq <= 0 || !aligned16(q) || !aligned16(out) || !aligned16(k_cache) || !aligned16(v_cache))
         return PKV_ERR_INVALID;
     if (num_seqs > 65535 || desc->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    StageLayout lay{};
+    if (fp8) {
+        // the copy is a pool of num_seqs * max_blocks_per_seq blocks
+        if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * desc->num_kv_heads * kBlockSize > INT32_MAX)
+            return PKV_ERR_UNSUPPORTED;
+        lay = stage_layout(num_seqs, max_blocks_per_seq, desc->num_kv_heads, D);
+        if (!workspace || static_cast<int64_t>(workspace_bytes) < lay.bytes) return PKV_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return PKV_ERR_INVALID;
+    }
     unsigned int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void* k_pool = k_cache;
+    const void* v_pool = v_cache;
+    int32_t pool_blocks = desc->num_blocks;
+    if (fp8) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        int32_t* table_copy = reinterpret_cast<int32_t*>(ws + lay.table_off);
+        uint4* k_copy = reinterpret_cast<uint4*>(ws + lay.k_off);
+        uint4* v_copy = reinterpret_cast<uint4*>(ws + lay.v_off);
+        const int block_vecs = desc->num_kv_heads * kBlockSize * D / 8;  // 8 codes -> one 16-byte vector
+        const dim3 grid(static_cast<unsigned>(max_blocks_per_seq), static_cast<unsigned>(num_seqs), 2);
+        const auto* kc = static_cast<const uint8_t*>(k_cache);
+        const auto* vc = static_cast<const uint8_t*>(v_cache);
+        if (q_dtype == PKV_BF16)
+            stage_fp8_kernel<BF16><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
+                                                         desc->num_blocks, block_vecs, k_copy, v_copy, table_copy, err);
+        else
+            stage_fp8_kernel<F16><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
+                                                        desc->num_blocks, block_vecs, k_copy, v_copy, table_copy, err);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        block_tables = table_copy;
+        k_pool = k_copy;
+        v_pool = v_copy;
+        pool_blocks = num_seqs * max_blocks_per_seq;
+    }
 
     PrefillParams p{};
     p.query_start = query_start;
@@ -806,7 +930,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     p.Hq = num_q_heads;
     p.Hkv = desc->num_kv_heads;
     p.MB = max_blocks_per_seq;
-    p.NB = desc->num_blocks;
+    p.NB = pool_blocks;
     p.G = G;
     p.TT = kTileM / G;
     p.num_qtiles = (max_query_len + 2 * p.TT - 1) / (2 * p.TT);  // CTAs of two Q tiles
@@ -815,16 +939,23 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     p.num_work = num_work_units;
     if (static_cast<int64_t>(num_work_units) * p.Hkv > INT32_MAX) return PKV_ERR_UNSUPPORTED;
     p.max_query_len = max_query_len;
-    p.qk_scale = scale * 1.4426950408889634f;
+    p.qk_scale = scale * (fp8 ? desc->k_scale : 1.f) * 1.4426950408889634f;
+    p.o_scale = fp8 ? desc->v_scale : 1.f;
     p.err = err;
 
     CUtensorMap tq, tk, tv;
-    const int64_t pool_rows = static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * kBlockSize;
+    const int64_t pool_rows = static_cast<int64_t>(pool_blocks) * desc->num_kv_heads * kBlockSize;
     if (!encode_token_head_map(&tq, q, D, num_q_heads, num_tokens, G, kTileM / G) ||
-        !encode_pool_map(&tk, k_cache, 2, pool_rows, D) || !encode_pool_map(&tv, v_cache, 2, pool_rows, D))
+        !encode_pool_map(&tk, k_pool, 2, pool_rows, D) || !encode_pool_map(&tv, v_pool, 2, pool_rows, D))
         return PKV_ERR_CUDA;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = desc->kv_dtype == PKV_BF16 ? launch_prefill<BF16>(p, D, tq, tk, tv, st)
-                                                      : launch_prefill<F16>(p, D, tq, tk, tv, st);
+    const cudaError_t e = q_dtype == PKV_BF16 ? launch_prefill<BF16>(p, D, tq, tk, tv, st)
+                                              : launch_prefill<F16>(p, D, tq, tk, tv, st);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" size_t pkv_prefill_workspace_bytes(int32_t kv_dtype, int32_t num_seqs, int32_t num_kv_heads,
+                                              int32_t head_size, int32_t max_blocks_per_seq) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_size <= 0 || max_blocks_per_seq < 0) return 0;
+    if (kv_dtype != PKV_FP8_E4M3) return 0;  // 16-bit pools are read in place
+    return static_cast<size_t>(stage_layout(num_seqs, max_blocks_per_seq, num_kv_heads, head_size).bytes);
 }

@@ -36,7 +36,7 @@ EXPORTED = [
     "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
     "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
-    "pkv_prefill_plan", "pkv_decode_plan",
+    "pkv_prefill_plan", "pkv_decode_plan", "pkv_prefill_workspace_bytes",
 ]
 
 
@@ -133,7 +133,8 @@ def lib():
         "pkv_alloc_block_hash_of": (i64, [P, i32, P]),
         "pkv_alloc_reset_prefix_cache": (None, [P]),
         "pkv_paged_attention_prefill": (i32, [P, i32, i32, i32, i32, P, i32, P, P, D, P, i32, P, P, i32,
-                                              ctypes.c_float, P, P]),
+                                              ctypes.c_float, P, P, ctypes.c_size_t, P]),
+        "pkv_prefill_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32]),
         "pkv_prefill_plan": (i32, [P, P, i32, i32, i32, i32, P, i32, P]),
     }
     for name, (res, args) in sig.items():
@@ -371,22 +372,32 @@ def paged_attention_decode_cascade(q, k_cache, v_cache, desc: CacheDesc, block_t
 
 def paged_attention_prefill(q, k_cache, v_cache, desc: CacheDesc, query_start, max_query_len: int, block_tables,
                             seq_lens, scale: float, out, q_dtype: str | None = None, stream=None,
-                            work_units=None) -> None:
+                            work_units=None, workspace=None) -> None:
     """Causal paged prefill: q, out [T, Hq, D]; query_start int32 [S + 1],
     block_tables int32 [S, MB], seq_lens int32 [S] (device tensors);
-    work_units: optional device int32 CTA order from prefill_plan."""
+    work_units: optional device int32 CTA order from prefill_plan;
+    workspace: device buffer of prefill_workspace_bytes(...) bytes (fp8 pools)."""
     T, Hq = int(q.shape[0]), int(q.shape[1])
     S = int(seq_lens.shape[0])
     if int(query_start.shape[0]) != S + 1:
         raise ValueError("query_start must have num_seqs + 1 entries")
     nw = 0 if work_units is None else int(work_units.numel())
     wp = _dev_ptr(work_units, "work_units") if nw else None
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
     st = lib().pkv_paged_attention_prefill(
         _dev_ptr(q, "q"), _dtype_code(q, q_dtype), T, Hq, S, _dev_ptr(query_start, "query_start"), int(max_query_len),
         _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"), ctypes.byref(desc.c()),
         _dev_ptr(block_tables, "block_tables"), int(block_tables.shape[1]), _dev_ptr(seq_lens, "seq_lens"),
-        wp, nw, float(scale), _dev_ptr(out, "out"), _stream(stream))
+        wp, nw, float(scale), _dev_ptr(out, "out"), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "paged_attention_prefill")
+
+
+def prefill_workspace_bytes(kv_dtype: str, num_seqs: int, num_kv_heads: int, head_size: int,
+                            max_blocks_per_seq: int) -> int:
+    return int(lib().pkv_prefill_workspace_bytes(DTYPE_CODE[kv_dtype], num_seqs, num_kv_heads, head_size,
+                                                 max_blocks_per_seq))
 
 
 def prefill_plan(query_start, seq_lens, num_q_heads: int, num_kv_heads: int, max_query_len: int) -> np.ndarray:

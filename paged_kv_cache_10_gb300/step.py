@@ -201,13 +201,14 @@ class PrefillStep:
     one slot per new token (``append_tokens``).  Device, in stream order: ``paged_kv_append`` of the new
     tokens' K/V -> ``paged_attention_prefill`` for their query rows, its CTAs
     in the order of the host plan (``prefill_plan``: longest causal key range
-    first) unless ``plan`` is False."""
+    first) unless ``plan`` is False.  Over an fp8 pool the attention call
+    first copies the blocks it reaches into 16-bit blocks in ``workspace``."""
 
     def __init__(self, wl, device="cuda", alloc: pk.Allocator | None = None, plan: bool = True):
         self.wl = wl
         self.device = torch.device(device)
-        self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.dtype,
-                                 block_size=wl.b)
+        self.desc = pk.CacheDesc(num_blocks=wl.NB, num_kv_heads=wl.Hkv, head_size=wl.D, kv_dtype=wl.kv_dtype,
+                                 k_scale=wl.k_scale, v_scale=wl.v_scale, block_size=wl.b)
         self.alloc = alloc or pk.Allocator(wl.NB, wl.b, wl.free_order)
         for s, c in enumerate(wl.ctx):
             self.alloc.seq_new(s, int(c))
@@ -227,13 +228,16 @@ class PrefillStep:
         self.d_lens = torch.from_numpy(self.seq_lens).to(dev)
         self.d_query_start = torch.from_numpy(self.query_start).to(dev)
         self.out = torch.empty((wl.T, wl.Hq, wl.D), dtype=torch.uint16, device=dev)
+        ws = pk.prefill_workspace_bytes(wl.kv_dtype, wl.S, wl.Hkv, wl.D, wl.max_blocks)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev) if ws else None
         self.work = None
         if plan:
             self.work_host = pk.prefill_plan(self.query_start, self.seq_lens, wl.Hq, wl.Hkv, wl.max_query_len)
             self.work = torch.from_numpy(self.work_host).to(dev)
 
     def kernel_launches(self) -> int:
-        return 2  # append + prefill attention
+        # append + prefill attention (+ the 16-bit staging of an fp8 pool)
+        return 3 if self.workspace is not None else 2
 
     def append(self, stream=None):
         pk.paged_kv_append(self.k_new, self.v_new, self.d_slots, self.k_cache, self.v_cache, self.desc,
@@ -243,7 +247,7 @@ class PrefillStep:
         pk.paged_attention_prefill(self.q if q is None else q, self.k_cache, self.v_cache, self.desc,
                                    self.d_query_start, self.wl.max_query_len, self.d_tables, self.d_lens,
                                    self.wl.scale, self.out if out is None else out, q_dtype=self.wl.dtype,
-                                   stream=stream, work_units=self.work)
+                                   stream=stream, work_units=self.work, workspace=self.workspace)
 
     def run(self, stream=None):
         self.append(stream)

@@ -38,6 +38,8 @@ run causal attention for them:
                        context each (a 4096-token batch), 32/8 heads, bf16
   prefill_prompt_gqa   4 whole prompts of 4096 tokens, 32/8 heads, bf16
   prefill_prompt_mha   4 whole prompts of 2048 tokens, 32/32 heads, bf16
+  prefill_chunked_gqa_fp8  prefill_chunked_gqa over an fp8 E4M3 cache with
+                       per-tensor scales (bf16 queries and output)
 """
 from __future__ import annotations
 
@@ -294,7 +296,7 @@ class PrefillWorkload:
     Hkv: int
     D: int
     NB: int
-    dtype: str            # "f16" | "bf16" (q, pool, appended k/v, output)
+    dtype: str            # "f16" | "bf16" (q, appended k/v, output; the pool too unless kv_dtype says)
     scale: float
     ctx: list
     qlens: list
@@ -305,6 +307,12 @@ class PrefillWorkload:
     v_new: np.ndarray
     free_order: np.ndarray
     b: int = BLOCK_SIZE
+    kv_dtype: str = ""     # pool element type; "" = dtype; "e4m3" with the per-tensor scales below
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    def __post_init__(self):
+        self.kv_dtype = self.kv_dtype or self.dtype
 
     @property
     def T(self) -> int:
@@ -323,23 +331,27 @@ class PrefillWorkload:
         return max(self.qlens) if self.qlens else 0
 
 
-def prefill(name, seed, ctx, qlens, Hq, Hkv, D=128, dtype="bf16", NB=None) -> PrefillWorkload:
+def prefill(name, seed, ctx, qlens, Hq, Hkv, D=128, dtype="bf16", NB=None, kv_dtype=None) -> PrefillWorkload:
+    """kv_dtype: the pool's element type (default dtype); for "e4m3" each pool
+    draws its per-tensor scale from its values (max |x| / 448) and the new
+    tokens, drawn in dtype, are encoded with it by the append."""
     ss = np.random.SeedSequence(seed)
     s_q, s_k, s_v, s_kn, s_vn, s_free = ss.spawn(6)
     ctx = [int(c) for c in ctx]
     qlens = [int(n) for n in qlens]
     T = sum(qlens)
+    kv_dtype = kv_dtype or dtype
     need = sum(_blocks(c + n) for c, n in zip(ctx, qlens))
     NB = NB or max(4, need + math.ceil(0.10 * need))
-    k_pool, _ = _values(s_k, (NB, Hkv, BLOCK_SIZE, D), dtype)
-    v_pool, _ = _values(s_v, (NB, Hkv, BLOCK_SIZE, D), dtype)
+    k_pool, k_scale = _values(s_k, (NB, Hkv, BLOCK_SIZE, D), kv_dtype)
+    v_pool, v_scale = _values(s_v, (NB, Hkv, BLOCK_SIZE, D), kv_dtype)
     q, _ = _values(s_q, (T, Hq, D), dtype)
     k_new, _ = _values(s_kn, (T, Hkv, D), dtype)
     v_new, _ = _values(s_vn, (T, Hkv, D), dtype)
     free_order = np.random.Generator(np.random.PCG64(s_free)).permutation(NB).astype(np.int32)
     return PrefillWorkload(name=name, S=len(ctx), Hq=Hq, Hkv=Hkv, D=D, NB=NB, dtype=dtype, scale=1.0 / math.sqrt(D),
                            ctx=ctx, qlens=qlens, q=q, k_pool=k_pool, v_pool=v_pool, k_new=k_new, v_new=v_new,
-                           free_order=free_order)
+                           free_order=free_order, kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale)
 
 
 def prefill_chunked_gqa(seed=1010) -> PrefillWorkload:
@@ -362,8 +374,17 @@ def prefill_prompt_mha(seed=1012) -> PrefillWorkload:
     return prefill("prefill_prompt_mha", seed, [0] * 4, [2048] * 4, 32, 32)
 
 
+def prefill_chunked_gqa_fp8(seed=1010) -> PrefillWorkload:
+    """prefill_chunked_gqa (same seed, context lengths and queries) over an fp8 E4M3 cache
+    (per-tensor scales), bf16 queries and output."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(7)[6]))
+    ctx = rng.integers(0, 3584, size=8, endpoint=True)
+    return prefill("prefill_chunked_gqa_fp8", seed, ctx, [512] * 8, 32, 8, kv_dtype="e4m3")
+
+
 PREFILL = {
     "prefill_chunked_gqa": prefill_chunked_gqa,
+    "prefill_chunked_gqa_fp8": prefill_chunked_gqa_fp8,
     "prefill_prompt_gqa": prefill_prompt_gqa,
     "prefill_prompt_mha": prefill_prompt_mha,
 }

@@ -102,9 +102,9 @@ def test_prefill_validation_rejects_before_any_launch(pk):
     d96 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=96, kv_dtype="bf16").c()
     fake = 1 << 20  # never dereferenced
 
-    def call(desc=d, q_dtype=1, work=None, nwork=0, scale=0.1, Hq=8):
+    def call(desc=d, q_dtype=1, work=None, nwork=0, scale=0.1, Hq=8, ws=None, ws_bytes=0):
         return L.pkv_paged_attention_prefill(fake, q_dtype, 64, Hq, 2, fake, 32, fake, fake, ctypes.byref(desc), fake,
-                                             4, fake, work, nwork, scale, fake, None)
+                                             4, fake, work, nwork, scale, fake, ws, ws_bytes, None)
 
     assert call(nwork=-1) == pk.ERR_INVALID            # negative work-list length
     assert call(work=None, nwork=3) == pk.ERR_INVALID  # a length without a list
@@ -114,6 +114,32 @@ def test_prefill_validation_rejects_before_any_launch(pk):
     assert call(scale=0.0) == pk.ERR_INVALID           # the row maximum needs scale > 0
     assert call(Hq=6) == pk.ERR_UNSUPPORTED            # 3 query heads per KV head
     assert call(Hq=5) == pk.ERR_INVALID                # heads not a multiple
+    # fp8 pools: a 16-bit q, positive finite scales, a large enough aligned workspace
+    d8 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="e4m3", k_scale=0.5, v_scale=0.25).c()
+    need = L.pkv_prefill_workspace_bytes(pk.FP8_E4M3, 2, 2, 128, 4)
+    assert need > 0
+    assert call(desc=d8) == pk.ERR_WORKSPACE                           # no workspace
+    assert call(desc=d8, ws=fake, ws_bytes=need - 1) == pk.ERR_WORKSPACE
+    assert call(desc=d8, ws=fake + 4, ws_bytes=need + 4) == pk.ERR_INVALID  # not 16-byte aligned
+    assert call(desc=d8, q_dtype=2, ws=fake, ws_bytes=need) == pk.ERR_UNSUPPORTED  # fp8 q
+    for ks, vs in [(0.0, 1.0), (1.0, -1.0), (float("inf"), 1.0), (float("nan"), 1.0)]:
+        bad = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="e4m3", k_scale=ks, v_scale=vs).c()
+        assert call(desc=bad, ws=fake, ws_bytes=need) == pk.ERR_INVALID
+
+
+def test_prefill_workspace_bytes(pk):
+    """0 for 16-bit pools (read in place); for fp8 pools a 4-byte table entry
+    per (sequence, block) and two 16-bit copies of S * MB blocks, each part
+    rounded up to 256 bytes."""
+    L = pk.lib()
+    for code in (pk.F16, pk.BF16):
+        assert L.pkv_prefill_workspace_bytes(code, 8, 8, 128, 256) == 0
+    up = lambda x: -(-x // 256) * 256
+    for S, Hkv, D, MB in [(2, 2, 128, 4), (8, 8, 128, 256), (3, 1, 64, 7), (0, 4, 128, 10)]:
+        copy = S * MB * Hkv * 16 * D * 2
+        assert L.pkv_prefill_workspace_bytes(pk.FP8_E4M3, S, Hkv, D, MB) == up(S * MB * 4) + 2 * up(copy)
+    assert L.pkv_prefill_workspace_bytes(pk.FP8_E4M3, -1, 2, 128, 4) == 0
+    assert L.pkv_prefill_workspace_bytes(pk.FP8_E4M3, 2, 0, 128, 4) == 0
 
 
 def test_header_declares_every_exported_function_in_c(pk, tmp_path):

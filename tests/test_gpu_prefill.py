@@ -1,6 +1,7 @@
 """Paged (chunked) prefill attention on the GPU against the float64 oracle:
 every output element on small mixed batches (several query and key tiles,
-ragged tails, empty chunks, all group sizes, both 16-bit types), sampled rows
+ragged tails, empty chunks, all group sizes, both 16-bit types, fp8 E4M3
+pools with per-tensor scales), sampled rows
 of the full-size workloads (each sampled token is one decode row of the
 oracle at its own position), the appended pool bytes, and the error paths."""
 import numpy as np
@@ -52,7 +53,7 @@ def model(wl):
 
 def oracle_pools(wl, slots):
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
-    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.dtype)
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
     return kp, vp
 
 
@@ -65,10 +66,11 @@ def check_full(st):
     kp, vp = oracle_pools(wl, slots)
     assert np.array_equal(host_bits(st.k_cache), kp)
     assert np.array_equal(host_bits(st.v_cache), vp)
-    ref = oracle.paged_prefill(wl.q, wl.dtype, st.query_start, kp, vp, wl.dtype, tables, lens, wl.scale)
+    ref = oracle.paged_prefill(wl.q, wl.dtype, st.query_start, kp, vp, wl.kv_dtype, tables, lens, wl.scale,
+                               wl.k_scale, wl.v_scale)
     got = oracle.dequantize(host_bits(st.out), wl.dtype)
     assert np.all(np.isfinite(got))
-    return max_error(got, ref, wl.dtype, TOL[wl.dtype]), float(np.max(np.abs(ref)))
+    return max_error(got, ref, wl.dtype, TOL[wl.kv_dtype]), float(np.max(np.abs(ref)))
 
 
 CASES = [
@@ -95,7 +97,71 @@ def test_prefill_matches_oracle_every_element(lib, dtype, G, case, D, plan):
     assert err <= TOL[dtype], (err, mx)
 
 
-@pytest.mark.parametrize("name", ["prefill_chunked_gqa", "prefill_prompt_gqa", "prefill_prompt_mha"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_fp8_cache_matches_oracle_every_element(lib, dtype, G, case, D):
+    """fp8 E4M3 pools with per-tensor scales: the new tokens are encoded by
+    the append, the attention pass reads 16-bit copies of the reached blocks;
+    every output element against the oracle over the same codes."""
+    from paged_kv_cache_10_gb300 import workloads
+    ctx, qlens = CASES[case]
+    Hkv = 2
+    wl = workloads.prefill("prefill_fp8", 2300 + 10 * G + case + D, ctx, qlens, Hkv * G, Hkv, D=D, dtype=dtype,
+                           kv_dtype="e4m3")
+    assert wl.k_scale != wl.v_scale  # a swapped scale would show
+    st = run(wl)
+    assert st.workspace is not None
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["e4m3"], (err, mx)
+
+
+def test_prefill_fp8_cache_ignores_nan_codes_past_the_sequence_end(lib):
+    """E4M3 NaN codes (0x7f, 0xff) in the slots no sequence has written reach
+    the 16-bit copy as NaN and must still get probability 0."""
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.prefill("prefill_fp8_nan", 2398, [0, 0, 0], [10, 7, 150], 8, 2, dtype="bf16", kv_dtype="e4m3")
+    wl.k_pool[:] = 0x7f
+    wl.v_pool[:] = 0xff
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["e4m3"], (err, mx)
+
+
+def test_prefill_fp8_cache_errors(lib):
+    """A block id outside the pool is flagged (its copy reads as zeros), a
+    short workspace is refused before any launch, and the next correct call
+    still matches."""
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.prefill("prefill_fp8_err", 2399, [40, 0], [9, 30], 8, 2, dtype="bf16", kv_dtype="e4m3")
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    bad_tables = st.d_tables.clone()
+    bad_tables[0, 0] = wl.NB + 5
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                bad_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16", workspace=st.workspace)
+    torch.cuda.synchronize()
+    assert lib.get_device_error() & lib.DEVERR_BLOCK_ID
+    with pytest.raises(lib.PagedKVError):
+        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                    st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16",
+                                    workspace=st.workspace[:-1])
+    with pytest.raises(lib.PagedKVError):
+        lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                    st.d_tables, st.d_lens, wl.scale, st.out, q_dtype="bf16")
+    st.out.zero_()
+    st.attend()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["e4m3"], (err, mx)
+
+
+@pytest.mark.parametrize("name", ["prefill_chunked_gqa", "prefill_prompt_gqa", "prefill_prompt_mha",
+                                  "prefill_chunked_gqa_fp8"])
 def test_prefill_full_size_sampled_rows(lib, name):
     from paged_kv_cache_10_gb300 import workloads
     wl = workloads.PREFILL[name]()
@@ -116,12 +182,13 @@ def test_prefill_full_size_sampled_rows(lib, name):
     rows = np.array(rows)
     # one decode row of the oracle per sampled token: its own position is the
     # last key it may see
-    ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.dtype, kp, vp, wl.dtype,
-                              np.ascontiguousarray(tables[seqs]), np.array(pos, np.int32) + 1, wl.scale)
+    ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.dtype, kp, vp, wl.kv_dtype,
+                              np.ascontiguousarray(tables[seqs]), np.array(pos, np.int32) + 1, wl.scale,
+                              wl.k_scale, wl.v_scale)
     got = oracle.dequantize(host_bits(st.out)[rows], wl.dtype)
     assert np.all(np.isfinite(got))
-    err = max_error(got, ref, wl.dtype, TOL[wl.dtype])
-    assert err <= TOL[wl.dtype], err
+    err = max_error(got, ref, wl.dtype, TOL[wl.kv_dtype])
+    assert err <= TOL[wl.kv_dtype], err
     # every row was written (finite) and the appended pool bytes match
     assert np.all(np.isfinite(oracle.dequantize(host_bits(st.out), wl.dtype)))
     assert np.array_equal(host_bits(st.k_cache), kp)
