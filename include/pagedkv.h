@@ -385,14 +385,20 @@ size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
  * kernels finish in stream order (else PKV_ERR_WORKSPACE).  16-bit pools
  * need none (NULL, 0).  num_seqs * max_blocks_per_seq * num_kv_heads * 16
  * must stay below 2^31 for an fp8 pool (else PKV_ERR_UNSUPPORTED).
- * work_units, num_work_units: the order in which the CTAs start.  A CTA
- * covers unit u = s * nq + qt (sequence s, its query rows [qt * r, (qt + 1) *
- * r) with r = 256 / G tokens, nq = ceil(max_query_len / r)) for one KV head.
+ * work_units, num_work_units: the order in which units are taken.  A unit
+ * u = s * nq + qt (sequence s, its query rows [qt * r, (qt + 1) * r) with
+ * r = 256 / G tokens, nq = ceil(max_query_len / r)) runs for one KV head.
  * Null (num_work_units 0): every unit, each (sequence, KV head) from its last
  * rows down.  Otherwise a device int32 array of num_work_units units, each
  * run for every KV head in that order, and only those; pkv_prefill_plan
  * writes the batch's units longest causal key range first.  A unit outside
  * [0, num_seqs * nq) sets PKV_DEVERR_SEQ_LEN and is skipped.
+ * The attention kernel is persistent: one CTA per SM takes (unit, KV head)
+ * pairs in list order from a device counter as it finishes the one before.
+ * The library owns 1024 such counters and hands one to each call in turn;
+ * the kernel returns its counter to zero when it ends.  Calls that run at
+ * the same time (other streams, or two different captured graphs) must
+ * not hold the same counter, i.e. must be fewer than 1024 calls apart.
  * Inconsistent query_start / seq_lens (n_s < 0,
  * n_s > seq_lens[s], past num_tokens or the block table) set
  * PKV_DEVERR_SEQ_LEN and the sequence is skipped; a block id outside the pool

@@ -26,6 +26,8 @@
 // rebased only when it grows by more than 2^8, which keeps every
 // probability <= 256 and skips most O corrections; the final O / l is the
 // same softmax.
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 #include <type_traits>
@@ -53,9 +55,15 @@ static_assert(128 * kLoadRegs + 256 * kSoftmaxRegs <= kThreads * (65536 / kThrea
 constexpr int kSoftmaxWarps = 4;  // per Q tile
 constexpr float kRebase = 8.0f;   // log2 units
 
-// q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], v_zero, s_full[2 tiles], p_full[2 tiles],
-// o_done[2 tiles], drain
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 1 + 2 + 2 + 2 + 1;
+// Persistent prefill: each CTA claims units from a counter and publishes
+// them to its warps through a ring of kUnitSlots slots; 11 warps read each
+// slot (the K, V and MMA warps and the 8 softmax warps).
+constexpr int kUnitSlots = 4;
+constexpr int kUnitReaders = 11;
+
+// q_full, q_empty, k_full[3], k_empty[3], v_full[2], v_empty[2], v_zero[2], s_full[2 tiles],
+// p_full[2 tiles], o_done[2 tiles], drain, u_full[4], u_empty[4]
+constexpr int kNumBars = 2 + 2 * kKStages + 3 * kVStages + 2 + 2 + 2 + 1 + 2 * kUnitSlots;
 
 // Shared-memory layout for head_size D (64 or 128): operands are 128 rows x
 // D 16-bit elements in D / 64 column blocks of 128-byte rows.
@@ -69,7 +77,9 @@ struct Tile {
     static constexpr int kOffV = kOffK + kKStages * kOp;
     static constexpr int kOffBar = kOffV + kVStages * kOp;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    static constexpr int kUnitBytes = 48;  // one published unit (sizeof(Unit) rounded up)
+    static constexpr int kSmemBytes = kOffMisc + 8 + kUnitSlots * kUnitBytes + 1024;  // tmem slot, abort flag,
+                                                                                       // unit ring; alignment slack
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -95,7 +105,17 @@ struct PrefillParams {
     float* part_l;
     float* part_o;
     int32_t NP, row_chunks;
+    // prefill: the launch's scheduling counters (g_prefill_sched slot)
+    int32_t sched_slot;
 };
+
+// Unit-claim counters of the persistent prefill, one pair (next unit, CTAs
+// finished) per launch slot.  Zero at load; the last CTA of a launch puts its
+// pair back to zero, so a launch (or a graph replay) always starts from 0.
+// The host hands out slots round-robin: launches that run at the same time
+// take different slots unless kSchedSlots of them overlap.
+constexpr int kSchedSlots = 1024;
+__device__ unsigned int g_prefill_sched[2 * kSchedSlots];
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
@@ -158,12 +178,84 @@ __device__ __forceinline__ void setmaxnreg_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
 }
 
-// kPrefix = false: causal prefill; Q tile X (X = 0, 1) holds 128 / G tokens x
+// One unit of work: the rows of a Q tile pair and the keys they need.
+struct Unit {
+    const int32_t* bt;  // block table, from the unit's first key block
+    int kv_end[2];      // keys Q tile X needs (0: the tile has no rows)
+    int h;              // KV head
+    int q0, n, ctx, t0;  // prefill: the sequence's first row in q / out, its new tokens, the
+                         // tokens before them, the first token of Q tile A
+};
+
+// Prefill unit number lin: unit work[lin / Hkv] of the host plan (or of the
+// default order: each (sequence, KV head) from its last query tiles down)
+// for KV head lin % Hkv.  False when the unit has no rows or its sequence's
+// bounds are inconsistent (reported when rep).
+__device__ bool prefill_unit(const PrefillParams& p, int64_t lin, int RQ, bool rep, Unit& u) {
+    int s, qt;
+    if (p.work) {
+        const int w = __ldg(p.work + lin / p.Hkv);
+        u.h = static_cast<int>(lin % p.Hkv);
+        if (w < 0 || w >= p.S * p.num_qtiles) {
+            if (rep) report(p.err, PKV_DEVERR_SEQ_LEN);
+            return false;
+        }
+        s = w / p.num_qtiles;
+        qt = w % p.num_qtiles;
+    } else {
+        qt = p.num_qtiles - 1 - static_cast<int>(lin % p.num_qtiles);
+        u.h = static_cast<int>((lin / p.num_qtiles) % p.Hkv);
+        s = static_cast<int>(lin / (static_cast<int64_t>(p.num_qtiles) * p.Hkv));
+    }
+    u.q0 = __ldg(p.query_start + s);
+    const int q1 = __ldg(p.query_start + s + 1);
+    u.n = q1 - u.q0;
+    const int L = __ldg(p.seq_lens + s);
+    if (u.q0 < 0 || u.n < 0 || q1 > p.T || L < u.n || L > p.MB * kBlockSize) {
+        if (rep) report(p.err, PKV_DEVERR_SEQ_LEN);
+        return false;
+    }
+    if (u.n > p.max_query_len && rep) report(p.err, PKV_DEVERR_SEQ_LEN);
+    u.t0 = qt * 2 * RQ;
+    if (u.t0 >= u.n) return false;
+    u.ctx = L - u.n;  // tokens before this chunk
+    for (int X = 0; X < 2; ++X) {
+        const int tx = u.t0 + X * RQ;
+        u.kv_end[X] = tx < u.n ? u.ctx + tx + min(RQ, u.n - tx) : 0;
+    }
+    u.bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
+    return true;
+}
+
+// Waits for unit k in the ring slot k % kUnitSlots, copies it and hands the
+// slot back; false on timeout.  A unit with h < 0 ends the list.  Called by
+// one thread (warp 1) or by a whole warp (every lane waits; lane 0 hands
+// back).
+__device__ __forceinline__ bool take_unit(uint64_t* u_full, uint64_t* u_empty, const Unit* ring, int k,
+                                          bool whole_warp, Unit& u) {
+    const int slot = k % kUnitSlots;
+    bool ok = mbar_wait(u_full + slot, (k / kUnitSlots) & 1);
+    if (whole_warp) ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    u = ring[slot];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || (threadIdx.x & 31) == 0) tc::arrive(u_empty + slot);
+    return true;
+}
+
+// kPrefix = false: causal prefill, persistent.  The grid has one CTA per SM
+// (or per unit, when there are fewer); each CTA claims units in list order
+// from a counter, so the longest units of the host plan start first and an
+// SM that finishes early takes the next one.  Warp 3 claims unit k + 1 and
+// loads its Q tiles while the other warps still work on unit k, and the K / V
+// rings run across unit boundaries, so the next unit's loads overlap this
+// unit's last tiles and epilogue.  Q tile X (X = 0, 1) holds 128 / G tokens x
 // the G heads of one (sequence, KV head), tokens [t0 + X * TT, ...); keys 0 ..
 // each row's position; normalised output.
-// kPrefix = true: the cascade decode's shared-prefix pass; Q tile X holds
-// 128 / G members x G heads of one (group, KV head); keys = one 512-token
-// partition of the group's shared blocks (no causal mask); split-K partials.
+// kPrefix = true: the cascade decode's shared-prefix pass, one unit per CTA;
+// Q tile X holds 128 / G members x G heads of one (group, KV head); keys =
+// one partition of the group's shared blocks (no causal mask); split-K
+// partials.
 template <typename T, int D, bool kPrefix>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
@@ -175,73 +267,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* q_full = reinterpret_cast<uint64_t*>(sm + TL::kOffBar);
-    uint64_t* k_full = q_full + 1;           // [kKStages]
+    uint64_t* q_empty = q_full + 1;
+    uint64_t* k_full = q_empty + 1;          // [kKStages]
     uint64_t* k_empty = k_full + kKStages;   // [kKStages]
     uint64_t* v_full = k_empty + kKStages;   // [kVStages]
     uint64_t* v_empty = v_full + kVStages;   // [kVStages]
-    uint64_t* v_zero = v_empty + kVStages;
-    uint64_t* s_full = v_zero + 1;   // [Q tile]
-    uint64_t* p_full = s_full + 2;   // [Q tile]
-    uint64_t* o_done = p_full + 2;   // [Q tile]
+    uint64_t* v_zero = v_empty + kVStages;   // [kVStages]
+    uint64_t* s_full = v_zero + kVStages;    // [Q tile]
+    uint64_t* p_full = s_full + 2;           // [Q tile]
+    uint64_t* o_done = p_full + 2;           // [Q tile]
     uint64_t* drain = o_done + 2;
+    uint64_t* u_full = drain + 1;            // [kUnitSlots]
+    uint64_t* u_empty = u_full + kUnitSlots; // [kUnitSlots]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
+    Unit* unit_ring = reinterpret_cast<Unit*>(sm + kOffMisc + 8);  // [kUnitSlots]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int h;
     const int G = p.G;
     const int RQ = kTileM / G;  // tokens (prefill) or members (prefix) per Q tile
-    // ---- this CTA's rows and keys (uniform across the CTA).  Keys are
-    // counted from the block `bt` points at.  kv_end[X]: keys Q tile X needs
-    // (0 when the tile is empty); the CTA loads max(kv_end) keys.
-    const int32_t* bt;
-    int kv_end[2];
-    // prefill
-    int q0 = 0, n = 0, ctx = 0, t0 = 0;
-    // prefix pass
+    // prefix pass: this CTA's one unit, fixed by its grid position
+    Unit pre{};
     int m0 = 0, members = 0, mrow0 = 0, seq0 = 0, pp = 0;
-    if constexpr (!kPrefix) {
-        // One CTA per (sequence s, query tile pair qt, KV head h).  CTAs start
-        // in linear order.  With a work list (the host plan of
-        // pkv_prefill_plan, longest causal key range first over the whole
-        // batch) CTA i takes unit work[i / Hkv] and head i % Hkv; without one,
-        // each (s, h) runs its query tiles from the last down.
-        const int64_t lin = blockIdx.x;
-        int s, qt;
-        if (p.work) {
-            const int u = __ldg(p.work + lin / p.Hkv);
-            h = static_cast<int>(lin % p.Hkv);
-            if (u < 0 || u >= p.S * p.num_qtiles) {
-                if (threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-                return;
-            }
-            s = u / p.num_qtiles;
-            qt = u % p.num_qtiles;
-        } else {
-            qt = p.num_qtiles - 1 - static_cast<int>(lin % p.num_qtiles);
-            h = static_cast<int>((lin / p.num_qtiles) % p.Hkv);
-            s = static_cast<int>(lin / (static_cast<int64_t>(p.num_qtiles) * p.Hkv));
-        }
-        q0 = __ldg(p.query_start + s);
-        const int q1 = __ldg(p.query_start + s + 1);
-        n = q1 - q0;
-        const int L = __ldg(p.seq_lens + s);
-        if (q0 < 0 || n < 0 || q1 > p.T || L < n || L > p.MB * kBlockSize) {
-            if (threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-            return;
-        }
-        if (n > p.max_query_len && threadIdx.x == 0) report(p.err, PKV_DEVERR_SEQ_LEN);
-        t0 = qt * 2 * RQ;
-        if (t0 >= n) return;
-        ctx = L - n;  // tokens before this chunk
-        for (int X = 0; X < 2; ++X) {
-            const int tx = t0 + X * RQ;
-            kv_end[X] = tx < n ? ctx + tx + min(RQ, n - tx) : 0;
-        }
-        bt = p.block_tables + static_cast<int64_t>(s) * p.MB;
-    } else {
+    if constexpr (kPrefix) {
         pp = blockIdx.x;
-        h = blockIdx.y;
+        pre.h = blockIdx.y;
+        const int h = pre.h;
         const int grp = blockIdx.z / p.row_chunks, chunk = blockIdx.z % p.row_chunks;
         m0 = __ldg(p.group_offsets + grp);
         members = __ldg(p.group_offsets + grp + 1) - m0;
@@ -276,18 +327,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             return;
         }
         const int keys = (min(nb, b0 + kPrefixPartitionBlocks) - b0) * kBlockSize;
-        kv_end[0] = keys;
-        kv_end[1] = 0;
-        bt = p.block_tables + static_cast<int64_t>(seq0) * p.MB + b0;
+        pre.kv_end[0] = keys;
+        pre.kv_end[1] = 0;
+        pre.bt = p.block_tables + static_cast<int64_t>(seq0) * p.MB + b0;
     }
-    const bool has_b = kv_end[1] > 0;
-    const int kv_max = max(kv_end[0], kv_end[1]);
-    const int nkt = (kv_max + kTileN - 1) / kTileN;      // key tiles loaded
-    const int nblk = (kv_max + kBlockSize - 1) / kBlockSize;
-    const int nt[2] = {(kv_end[0] + kTileN - 1) / kTileN, (kv_end[1] + kTileN - 1) / kTileN};  // per Q tile
+    unsigned int* sched = g_prefill_sched + 2 * p.sched_slot;
+    const int64_t total = kPrefix ? 1
+                          : (p.work ? static_cast<int64_t>(p.num_work) * p.Hkv
+                                    : static_cast<int64_t>(p.num_qtiles) * p.Hkv * p.S);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(k_full + i, 1);
             mbar_init(k_empty + i, 1);
@@ -295,14 +346,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kVStages; ++i) {
             mbar_init(v_full + i, 1);
             mbar_init(v_empty + i, 1);
+            mbar_init(v_zero + i, 1);
         }
-        mbar_init(v_zero, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
             mbar_init(p_full + i, kSoftmaxWarps);  // one arrival per softmax warp
             mbar_init(o_done + i, 1);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < kUnitSlots; ++i) {
+            mbar_init(u_full + i, 1);
+            mbar_init(u_empty + i, kUnitReaders);
+        }
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -319,36 +374,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile X at 256 + X * 128
     if (warp < 4) {
       setmaxnreg_dec();
-      if (warp == 0 || warp == 2) {
-        // --------------------------------------------- TMA producers (K, V)
-        // Warp 0 streams Q and the key tiles, warp 2 the value tiles, each
-        // through its own ring, so a key load never waits for a P V to free
-        // a value stage.
-        const bool is_k = warp == 0;
-        const int nst = is_k ? kKStages : kVStages;
-        const uint64_t pol_kv = policy_evict_last();  // re-read by other CTAs of the sequence / group
-        uint64_t* full = is_k ? k_full : v_full;
-        uint64_t* empty = is_k ? k_empty : v_empty;
-        const CUtensorMap* map = is_k ? &tmk : &tmv;
-        unsigned char* ring = sm + (is_k ? kOffK : kOffV);
-        // block ids 32 at a time (4 tiles), read 4 tiles before their use:
-        // lane l holds the id of block 32 * batch + l
-        auto load_ids = [&](int batch) {
-            const int idx = batch * 32 + lane;
-            return idx < nblk ? __ldg(bt + idx) : 0;
-        };
-        int ids_cur = load_ids(0);
-        int ids_nxt = load_ids(1);
-        if (is_k) {
-            const uint64_t pol_q = policy_evict_first();
-            const int ntiles = has_b ? 2 : 1;
+      if (warp == 3) {
+        // ------------------------------- unit claims and Q loads (warp 3)
+        // Claims the next unit with a row, publishes it to the other warps
+        // and loads its Q tiles (the S MMAs of the unit before, which read
+        // the Q buffers, are complete by then).  A claim past the list
+        // publishes -1 (done).
+        const uint64_t pol_q = policy_evict_first();
+        int k = 0, qloads = 0;
+        bool done = false;
+        for (;; ++k) {
+            // unit k is claimed once the S MMAs of unit k - 1 are issued (that
+            // unit is in its last key tile), so a CTA holds at most one unit
+            // ahead and the list stays longest first across the SMs
+            if (k > 0 && !done && !__all_sync(0xffffffffu, mbar_wait(q_empty, (k - 1) & 1))) {
+                if (lane == 0) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                done = true;  // publishes -1
+            }
+            Unit u{};
+            u.h = -1;  // the end of the list unless a claim finds a unit
+            if (!done && *abort_flag == 0) {
+                if constexpr (kPrefix) {
+                    if (k == 0) u = pre;
+                } else {
+                    bool found = false;
+                    for (;;) {
+                        unsigned int c = 0;
+                        if (lane == 0) c = atomicAdd(sched, 1u);
+                        c = __shfl_sync(0xffffffffu, c, 0);
+                        if (c >= total) break;
+                        if (prefill_unit(p, c, RQ, lane == 0, u)) {
+                            found = true;
+                            break;
+                        }
+                    }
+                    if (!found) u.h = -1;
+                }
+            }
+            const int slot = k % kUnitSlots;
+            if (k >= kUnitSlots && !__all_sync(0xffffffffu, mbar_wait(u_empty + slot, ((k / kUnitSlots) + 1) & 1))) {
+                if (lane == 0) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            if (lane == 0) {
+                unit_ring[slot] = u;
+                tc::arrive(u_full + slot);
+            }
+            __syncwarp();
+            if (u.h < 0) break;
+            const int ntiles = u.kv_end[1] > 0 ? 2 : 1;
             if constexpr (!kPrefix) {
                 if (lane == 0) {
                     mbar_arrive_expect_tx(q_full, ntiles * kOpBytes);
                     for (int X = 0; X < ntiles; ++X)
                         for (int dh = 0; dh < kDB; ++dh)
-                            tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kColBlock, &tmq, dh * 64, h * G,
-                                            q0 + t0 + X * RQ, q_full, pol_q);
+                            tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kColBlock, &tmq, dh * 64, u.h * G,
+                                            u.q0 + u.t0 + X * RQ, q_full, pol_q);
                 }
             } else {
                 // G query rows of each member (its batch row in q); rows of
@@ -357,18 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kMaxPerLane = 2 * kTileM / 32;  // G = 1: 8 members per lane
                 int bs[kMaxPerLane];
 #pragma unroll
-                for (int k = 0; k < kMaxPerLane; ++k) {
-                    const int mi = lane + 32 * k;
-                    bs[k] = seq0;
-                    if (mi < ntiles * RQ && mrow0 + mi < members) bs[k] = __ldg(p.group_members + m0 + mrow0 + mi);
+                for (int i = 0; i < kMaxPerLane; ++i) {
+                    const int mi = lane + 32 * i;
+                    bs[i] = seq0;
+                    if (mi < ntiles * RQ && mrow0 + mi < members) bs[i] = __ldg(p.group_members + m0 + mrow0 + mi);
                 }
                 if (lane == 0) mbar_arrive_expect_tx(q_full, ntiles * kOpBytes);
                 __syncwarp();
 #pragma unroll
-                for (int k = 0; k < kMaxPerLane; ++k) {
-                    const int mi = lane + 32 * k;
+                for (int i = 0; i < kMaxPerLane; ++i) {
+                    const int mi = lane + 32 * i;
                     if (mi >= ntiles * RQ) break;
-                    int b = bs[k];
+                    int b = bs[i];
                     if (b < 0 || b >= p.S) {
                         report(p.err, PKV_DEVERR_SEQ_LEN);
                         b = seq0;
@@ -376,87 +463,136 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int X = mi / RQ, mx = mi - X * RQ;
                     for (int dh = 0; dh < kDB; ++dh)
                         tc::tma_load_3d(sm + kOffQ + X * kOpBytes + dh * kColBlock + mx * G * 128, &tmq, dh * 64,
-                                        h * G, b, q_full, pol_q);
+                                        u.h * G, b, q_full, pol_q);
                 }
             }
+            ++qloads;
+            __syncwarp();
         }
-        int issued = 0;
-        for (int j = 0; j < nkt; ++j) {
-            const int st = j % nst;
-            const int nb_tile = min(8, nblk - j * 8);
-            if (j > 0 && (j & 3) == 0) {
-                ids_cur = ids_nxt;
-                ids_nxt = load_ids((j >> 2) + 1);
-            }
-            int phys = __shfl_sync(0xffffffffu, ids_cur, ((j & 3) << 3) + (lane & 7));
-            if (lane < nb_tile && (phys < 0 || phys >= p.NB)) {
-                report(p.err, PKV_DEVERR_BLOCK_ID);
-                phys = 0;
-            }
-            const int row = (phys * p.Hkv + h) * kBlockSize;
-            // the stage is free once the MMAs that read it (Q K^T or P V of
-            // tile j - nst) have completed
-            const bool waited = j < nst || mbar_wait(empty + st, ((j / nst) + 1) & 1);
-            if (!warp_all(waited)) {
+        // the last Q copy has landed before the CTA can exit
+        if (qloads > 0 && !mbar_wait(q_full, (qloads - 1) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+      } else if (warp == 0 || warp == 2) {
+        // --------------------------------------------- TMA producers (K, V)
+        // Warp 0 streams the key tiles, warp 2 the value tiles, each through
+        // its own ring, so a key load never waits for a P V to free a value
+        // stage.  Tile g of the CTA (counted across its units) uses stage
+        // g % stages.
+        const bool is_k = warp == 0;
+        const int nst = is_k ? kKStages : kVStages;
+        const uint64_t pol_kv = policy_evict_last();  // re-read by other CTAs of the sequence / group
+        uint64_t* full = is_k ? k_full : v_full;
+        uint64_t* empty = is_k ? k_empty : v_empty;
+        const CUtensorMap* map = is_k ? &tmk : &tmv;
+        unsigned char* ring = sm + (is_k ? kOffK : kOffV);
+        int gt = 0;  // tiles issued by this warp
+        bool run = true;
+        for (int k = 0; run; ++k) {
+            Unit u;
+            if (!take_unit(u_full, u_empty, unit_ring, k, true, u)) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
                 break;
             }
-            if (!warp_all(*abort_flag == 0)) break;  // uniform across the warp
-            if (lane == 0) mbar_arrive_expect_tx(full + st, nb_tile * kDB * kBlockTileBytes);
-            __syncwarp();
-            if (lane < nb_tile) {
-                unsigned char* d = ring + st * kOpBytes + lane * kBlockTileBytes;
-                for (int dh = 0; dh < kDB; ++dh) tc::tma_load_2d(d + dh * kColBlock, map, dh * 64, row, full + st, pol_kv);
-            }
-            issued = j + 1;
-            if (!is_k && j == nkt - 1) {
-                // Value rows at or past the last key get probability 0, but
-                // the pool slots past a sequence's end (and never-loaded
-                // rows) may hold any bits, NaN included, and 0 * NaN = NaN in
-                // the MMA: clear them once the tile has landed.
-                const int r0 = kv_max - j * kTileN;
-                bool okv = true;
-                if (r0 < kTileN) {
-                    okv = warp_all(mbar_wait(v_full + st, (j / nst) & 1));
-                    if (okv) {
-                        unsigned char* vb = sm + kOffV + st * kOpBytes;
-                        constexpr int kRowChunks = D / 8;  // 16-byte chunks of a row
-                        for (int idx = lane; idx < (kTileN - r0) * kRowChunks; idx += 32) {
-                            const int r = r0 + idx / kRowChunks, c = idx % kRowChunks;
-                            *reinterpret_cast<uint4*>(vb + (c >> 3) * kColBlock + swz128(r, c & 7)) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                    }
+            if (u.h < 0) break;
+            const int kv_max = max(u.kv_end[0], u.kv_end[1]);
+            const int nkt = (kv_max + kTileN - 1) / kTileN;
+            const int nblk = (kv_max + kBlockSize - 1) / kBlockSize;
+            // block ids 32 at a time (4 tiles), read 4 tiles before their
+            // use: lane l holds the id of block 32 * batch + l
+            auto load_ids = [&](int batch) {
+                const int idx = batch * 32 + lane;
+                return idx < nblk ? __ldg(u.bt + idx) : 0;
+            };
+            int ids_cur = load_ids(0);
+            int ids_nxt = load_ids(1);
+            for (int j = 0; j < nkt; ++j) {
+                const int g = gt;  // this tile's number in the CTA's stream
+                const int st = g % nst;
+                const int nb_tile = min(8, nblk - j * 8);
+                if (j > 0 && (j & 3) == 0) {
+                    ids_cur = ids_nxt;
+                    ids_nxt = load_ids((j >> 2) + 1);
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    if (!okv) {
+                int phys = __shfl_sync(0xffffffffu, ids_cur, ((j & 3) << 3) + (lane & 7));
+                if (lane < nb_tile && (phys < 0 || phys >= p.NB)) {
+                    report(p.err, PKV_DEVERR_BLOCK_ID);
+                    phys = 0;
+                }
+                const int row = (phys * p.Hkv + u.h) * kBlockSize;
+                // the stage is free once the MMAs that read it (Q K^T or P V
+                // of tile g - nst) have completed
+                const bool waited = g < nst || mbar_wait(empty + st, ((g / nst) + 1) & 1);
+                if (!warp_all(waited)) {
+                    if (lane == 0) {
                         report(p.err, PKV_DEVERR_TIMEOUT);
                         *abort_flag = 1;
                     }
-                    tc::arrive(v_zero);
+                    run = false;
+                    break;
                 }
+                if (!warp_all(*abort_flag == 0)) {  // uniform across the warp
+                    run = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(full + st, nb_tile * kDB * kBlockTileBytes);
+                __syncwarp();
+                if (lane < nb_tile) {
+                    unsigned char* d = ring + st * kOpBytes + lane * kBlockTileBytes;
+                    for (int dh = 0; dh < kDB; ++dh)
+                        tc::tma_load_2d(d + dh * kColBlock, map, dh * 64, row, full + st, pol_kv);
+                }
+                if (!is_k) {
+                    // Value rows at or past the unit's last key get
+                    // probability 0, but the pool slots past a sequence's end
+                    // (and never-loaded rows) may hold any bits, NaN included,
+                    // and 0 * NaN = NaN in the MMA: in the unit's last tile
+                    // they are cleared once it has landed.  Every value tile
+                    // then completes v_zero of its stage.
+                    const int r0 = kv_max - j * kTileN;
+                    bool okv = true;
+                    if (j == nkt - 1 && r0 < kTileN) {
+                        okv = warp_all(mbar_wait(v_full + st, (g / nst) & 1));
+                        if (okv) {
+                            unsigned char* vb = sm + kOffV + st * kOpBytes;
+                            constexpr int kRowChunks = D / 8;  // 16-byte chunks of a row
+                            for (int idx = lane; idx < (kTileN - r0) * kRowChunks; idx += 32) {
+                                const int r = r0 + idx / kRowChunks, c = idx % kRowChunks;
+                                *reinterpret_cast<uint4*>(vb + (c >> 3) * kColBlock + swz128(r, c & 7)) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (!okv) {
+                            report(p.err, PKV_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        tc::arrive(v_zero + st);
+                    }
+                }
+                gt = g + 1;
             }
         }
         // every copy this warp started has landed before the CTA can exit
-        for (int j = max(0, issued - nst); j < issued; ++j)
-            if (!mbar_wait(full + j % nst, (j / nst) & 1) && lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
-        if (is_k && lane == 0 && !mbar_wait(q_full, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
-      } else if (warp == 1) {
+        for (int g = gt > nst ? gt - nst : 0; g < gt; ++g)
+            if (!mbar_wait(full + g % nst, (g / nst) & 1) && lane == 0)
+                report(p.err, PKV_DEVERR_TIMEOUT);
+      } else {
         // ------------------------------------------------------- MMA issuer
-        // Order S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
+        // Per unit: S_A(0), S_B(0), then per key tile j: P V_A(j), S_A(j+1),
         // P V_B(j), S_B(j+1).  tcgen05.mma from one thread run in order, so
         // S_X(j+1) overwrites Q tile X's S / P columns only after P V_X(j)
         // has read P_X(j), and the softmax of one Q tile overlaps the MMAs
-        // of the other.
+        // of the other.  The first P V_X of a unit overwrites O_X: it waits
+        // for P_X of that unit, which its softmax warps write only after
+        // they have read O_X out for the unit before.
         if (lane == 0) {
             const uint32_t idS = tc::idesc_f16(kBF, kTileM, kTileN, false);
             const uint32_t idO = tc::idesc_f16(kBF, kTileM, D, true);
-            bool ok = tc::wait_spin(q_full, 0);
             // Descriptors: bases per Q tile and ring stage, computed once; the
             // k-th 16-element step adds a constant (the start address field
             // is the low 14 bits, >> 4, and every operand sits below 256 KB).
@@ -469,8 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dK2 = tc::sdesc_sw128(smem_addr(sm + kOffK + 2 * kOpBytes), 16, 1024);
             const uint64_t dV0 = tc::sdesc_sw128(smem_addr(sm + kOffV), kColBlock, 1024);
             const uint64_t dV1 = tc::sdesc_sw128(smem_addr(sm + kOffV + kOpBytes), kColBlock, 1024);
-            auto issue_s = [&](int X, int j) {
-                const int st = j % kKStages;
+            bool any_mma = false;
+            auto issue_s = [&](int X, int g) {
+                any_mma = true;
+                const int st = g % kKStages;
                 const uint64_t q = X ? dQ1 : dQ0;
                 const uint64_t k = st == 0 ? dK0 : (st == 1 ? dK1 : dK2);
                 const uint32_t d = tmem + X * kTileN;
@@ -481,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc::commit(s_full + X);
             };
-            auto issue_pv = [&](int X, int j) {
-                const uint64_t v = (j % kVStages) ? dV1 : dV0;
+            auto issue_pv = [&](int X, int j, int g) {
+                const uint64_t v = (g % kVStages) ? dV1 : dV0;
                 const uint32_t d = tmem + 256 + X * kTileN, pa = tmem + X * kTileN;
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk)
@@ -490,48 +628,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    j > 0 || kk > 0);
                 tc::commit(o_done + X);
             };
-            // tile 0's keys, then S of both Q tiles
-            if (ok) ok = tc::wait_spin(k_full, 0);
-            if (ok) {
+            bool ok = true;
+            int gt = 0;            // key / value tiles of the finished units
+            int tp0 = 0, tp1 = 0;  // tiles of Q tiles A and B in the finished units
+            for (int k = 0;; ++k) {
+                Unit u;
+                ok = take_unit(u_full, u_empty, unit_ring, k, false, u);
+                if (!ok || u.h < 0) break;
+                const int nt0 = (u.kv_end[0] + kTileN - 1) / kTileN;
+                const int nt1 = (u.kv_end[1] + kTileN - 1) / kTileN;
+                const int nkt = max(nt0, nt1);
+                // this unit's Q tiles and its first keys, then S of both Q tiles
+                ok = tc::wait_spin(q_full, k & 1);
+                if (ok) ok = tc::wait_spin(k_full + gt % kKStages, (gt / kKStages) & 1);
+                if (!ok) break;
                 tc::fence_after();
-                for (int X = 0; X < 2; ++X)
-                    if (nt[X] > 0) issue_s(X, 0);
-                tc::commit(k_empty);
-            }
-            for (int j = 0; ok && j < nkt; ++j) {
-                if (*abort_flag) break;
-                // values of tile j (and, for the last tile, its cleared rows)
-                ok = tc::wait_spin(v_full + j % kVStages, (j / kVStages) & 1);
-                if (ok && j == nkt - 1) ok = tc::wait_spin(v_zero, 0);
-                bool kn = false;  // keys of tile j + 1 waited for
-                for (int X = 0; ok && X < 2; ++X) {
-                    if (j < nt[X]) {
-                        ok = tc::wait_spin(p_full + X, j & 1);
-                        if (!ok) break;
-                        tc::fence_after();
-                        issue_pv(X, j);
+                if (nt0 > 0) issue_s(0, gt);
+                if (nt1 > 0) issue_s(1, gt);
+                tc::commit(k_empty + gt % kKStages);
+                if (nkt == 1) tc::commit(q_empty);  // the unit's last S MMAs are issued
+                for (int j = 0; j < nkt; ++j) {
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
                     }
-                    if (j + 1 < nt[X]) {
-                        if (!kn) {
-                            ok = tc::wait_spin(k_full + (j + 1) % kKStages, ((j + 1) / kKStages) & 1);
-                            if (!ok) break;
-                            tc::fence_after();
-                            kn = true;
+                    const int g = gt + j;
+                    // values of tile j; in the unit's last tile, with the rows
+                    // past its keys cleared.  v_zero of a stage completes once
+                    // per value tile, and the producer cannot be a stage round
+                    // ahead here (it waits for v_empty of this tile), so the
+                    // last tile's phase is the one this parity names.
+                    ok = tc::wait_spin(v_full + g % kVStages, (g / kVStages) & 1);
+                    if (ok && j == nkt - 1) ok = tc::wait_spin(v_zero + g % kVStages, (g / kVStages) & 1);
+                    if (!ok) break;
+                    bool kn = false;  // keys of tile j + 1 waited for
+                    // Q tile A, then B: P V_X(j), then S_X(j + 1)
+#pragma unroll
+                    for (int X = 0; X < 2; ++X) {
+                        const int ntx = X ? nt1 : nt0;
+                        const int tpx = X ? tp1 : tp0;
+                        if (ok && j < ntx) {
+                            ok = tc::wait_spin(p_full + X, (tpx + j) & 1);
+                            if (ok) {
+                                tc::fence_after();
+                                issue_pv(X, j, g);
+                            }
                         }
-                        issue_s(X, j + 1);
+                        if (ok && j + 1 < ntx) {
+                            if (!kn) {
+                                ok = tc::wait_spin(k_full + (g + 1) % kKStages, ((g + 1) / kKStages) & 1);
+                                if (ok) tc::fence_after();
+                                kn = true;
+                            }
+                            if (ok) issue_s(X, g + 1);
+                        }
                     }
+                    if (!ok) break;
+                    tc::commit(v_empty + g % kVStages);
+                    if (j + 1 < nkt) tc::commit(k_empty + (g + 1) % kKStages);
+                    if (j + 2 == nkt) tc::commit(q_empty);  // the unit's last S MMAs are issued
                 }
                 if (!ok) break;
-                tc::commit(v_empty + j % kVStages);
-                if (j + 1 < nkt) tc::commit(k_empty + (j + 1) % kKStages);
+                gt += nkt;
+                tp0 += nt0;
+                tp1 += nt1;
             }
             if (!ok) {
                 report(p.err, PKV_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
             // the tensor core is idle before the memory it uses is released
-            tc::commit(drain);
-            if (!tc::wait_spin(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+            // (a CTA whose claims all came too late issued none)
+            if (any_mma) {
+                tc::commit(drain);
+                if (!tc::wait_spin(drain, 0)) report(p.err, PKV_DEVERR_TIMEOUT);
+            }
         }
         __syncwarp();
       }
@@ -546,156 +717,166 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wq = warp & 3;           // tensor-memory lane quarter
         const int row = wq * 32 + lane;
         const int rq = row / G, g = row - rq * G;
-        const int ntx = nt[X];
-        bool row_valid;
-        int pos;  // last key this row attends to
-        if constexpr (!kPrefix) {
-            const int tx = t0 + X * RQ;
-            row_valid = tx + rq < n;
-            pos = ctx + tx + min(rq, max(n - 1 - tx, 0));  // padding rows reuse the last position
-        } else {
-            row_valid = mrow0 + X * RQ + rq < members;
-            pos = kv_end[0] - 1;
-        }
-        // prefix pass: this row's batch row, read now so the epilogue does
-        // not wait for it
-        const int member_row = kPrefix && row_valid ? __ldg(p.group_members + m0 + mrow0 + X * RQ + rq) : -1;
         const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + X * kTileN + lane_base;
         const uint32_t tO = tmem + 256 + X * kTileN + lane_base;
         const float c = p.qk_scale;
         const float2 c2 = make_float2(c, c);
-        float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntx; ++j) {
-            ok = warp_all(tc::wait_spin(s_full + X, j & 1));
-            if (!ok || !warp_all(*abort_flag == 0)) break;
-            tc::fence_after();
-            // P V_X(j - 1) is complete (it precedes S_X(j)): take its phase
-            if (j > 0) ok = warp_all(tc::wait_spin(o_done + X, (j - 1) & 1));
-            if (!ok) break;
-            uint32_t x[4][32];
+        int tp = 0;  // tiles of this Q tile in the finished units
+        for (int k = 0;; ++k) {
+            Unit u;
+            ok = take_unit(u_full, u_empty, unit_ring, k, true, u);
+            if (!ok || u.h < 0) break;
+            const int h = u.h;
+            const int ntx = ((X ? u.kv_end[1] : u.kv_end[0]) + kTileN - 1) / kTileN;
+            bool row_valid;
+            int pos;  // last key this row attends to
+            if constexpr (!kPrefix) {
+                const int tx = u.t0 + X * RQ;
+                row_valid = tx + rq < u.n;
+                pos = u.ctx + tx + min(rq, max(u.n - 1 - tx, 0));  // padding rows reuse the last position
+            } else {
+                row_valid = mrow0 + X * RQ + rq < members;
+                pos = u.kv_end[0] - 1;
+            }
+            // prefix pass: this row's batch row, read now so the epilogue
+            // does not wait for it
+            const int member_row =
+                kPrefix && row_valid ? __ldg(p.group_members + m0 + mrow0 + X * RQ + rq) : -1;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < ntx; ++j) {
+                ok = warp_all(tc::wait_spin(s_full + X, (tp + j) & 1));
+                if (!ok || !warp_all(*abort_flag == 0)) break;
+                tc::fence_after();
+                // P V_X(j - 1) is complete (it precedes S_X(j)): take its phase
+                if (j > 0) ok = warp_all(tc::wait_spin(o_done + X, (tp + j - 1) & 1));
+                if (!ok) break;
+                uint32_t x[4][32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tc::ld32(tS + q * 32, x[q]);
-            tc::wait_ld();
+                for (int q = 0; q < 4; ++q) tc::ld32(tS + q * 32, x[q]);
+                tc::wait_ld();
 
-            // masked keys -inf; row maximum of the raw scores (scale > 0
-            // keeps the order)
-            const int key0 = j * kTileN;
-            if (key0 + kTileN - 1 > pos) {
+                // masked keys -inf; row maximum of the raw scores (scale > 0
+                // keeps the order)
+                const int key0 = j * kTileN;
+                if (key0 + kTileN - 1 > pos) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (key0 + q * 32 + i > pos) x[q][i] = __float_as_uint(-INFINITY);
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (key0 + q * 32 + i > pos) x[q][i] = __float_as_uint(-INFINITY);
-            }
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int i = 0; i < 32; i += 2)
-                    mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(x[q][i]), __uint_as_float(x[q][i + 1]));
-            const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY) * c;
-            const float m_new = fmaxf(m_ref, mt);
-            const bool rebase = m_new > m_ref + kRebase;
-            float alpha = 1.f;
-            if (rebase) {
-                alpha = ex2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
-                m_ref = m_new;
-            }
-            const float2 nm2 = make_float2(-m_ref, -m_ref);
-            float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t pk[64];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float2 a = ffma2(make_float2(__uint_as_float(x[q][2 * i]), __uint_as_float(x[q][2 * i + 1])), c2, nm2);
-                    a.x = ex2(a.x);
-                    a.y = ex2(a.y);
-                    ls[i & 3] = fadd2(ls[i & 3], a);
-                    pk[q * 16 + i] = pack2<kBF>(a.x, a.y);
+                    for (int i = 0; i < 32; i += 2)
+                        mx[(i >> 1) & 3] = fmax3(mx[(i >> 1) & 3], __uint_as_float(x[q][i]), __uint_as_float(x[q][i + 1]));
+                const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], -INFINITY) * c;
+                const float m_new = fmaxf(m_ref, mt);
+                const bool rebase = m_new > m_ref + kRebase;
+                float alpha = 1.f;
+                if (rebase) {
+                    alpha = ex2(m_ref - m_new);  // 0 on the first tile (m_ref = -inf)
+                    m_ref = m_new;
                 }
-            const float2 lt = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
-            l = l * alpha + (lt.x + lt.y);
-            tc::st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-            tc::st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-            if (j > 0 && __any_sync(0xffffffffu, rebase)) {
-                const float2 a2 = make_float2(alpha, alpha);
+                const float2 nm2 = make_float2(-m_ref, -m_ref);
+                float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                uint32_t pk[64];
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    tc::ld32(tO + q * 32, o);
-                    tc::wait_ld();
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float2 v = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
-                        o[2 * i] = __float_as_uint(v.x);
-                        o[2 * i + 1] = __float_as_uint(v.y);
+                        float2 a = ffma2(make_float2(__uint_as_float(x[q][2 * i]), __uint_as_float(x[q][2 * i + 1])), c2, nm2);
+                        a.x = ex2(a.x);
+                        a.y = ex2(a.y);
+                        ls[i & 3] = fadd2(ls[i & 3], a);
+                        pk[q * 16 + i] = pack2<kBF>(a.x, a.y);
                     }
-                    tc::st32(tO + q * 32, o);
+                const float2 lt = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+                l = l * alpha + (lt.x + lt.y);
+                tc::st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+                tc::st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+                if (j > 0 && __any_sync(0xffffffffu, rebase)) {
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc::ld32(tO + q * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 v = fmul2(make_float2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2);
+                            o[2 * i] = __float_as_uint(v.x);
+                            o[2 * i + 1] = __float_as_uint(v.y);
+                        }
+                        tc::st32(tO + q * 32, o);
+                    }
                 }
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::arrive(p_full + X);
             }
-            tc::wait_st();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::arrive(p_full + X);
-        }
-        const bool live = ntx > 0 && ok && warp_all(*abort_flag == 0);
-        if (live) ok = warp_all(tc::wait_spin(o_done + X, (ntx - 1) & 1));
-        if (live && ok) {
-            tc::fence_after();
-            const float inv = p.o_scale / l;
-            if constexpr (!kPrefix) {
-                typename T::storage* orow =
-                    reinterpret_cast<typename T::storage*>(p.out) +
-                    (static_cast<int64_t>(q0 + t0 + X * RQ + rq) * p.Hq + h * G + g) * D;
+            const bool live = ntx > 0 && ok && warp_all(*abort_flag == 0);
+            if (live) ok = warp_all(tc::wait_spin(o_done + X, (tp + ntx - 1) & 1));
+            if (live && ok) {
+                tc::fence_after();
+                const float inv = p.o_scale / l;
+                if constexpr (!kPrefix) {
+                    typename T::storage* orow =
+                        reinterpret_cast<typename T::storage*>(p.out) +
+                        (static_cast<int64_t>(u.q0 + u.t0 + X * RQ + rq) * p.Hq + h * G + g) * D;
 #pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    tc::ld32(tO + q * 32, o);
-                    tc::wait_ld();
-                    if (row_valid) {
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc::ld32(tO + q * 32, o);
+                        tc::wait_ld();
+                        if (row_valid) {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack2<kBF>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                            w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                            w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                            w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + q * 32 + v4 * 8) = w;
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                uint4 w;
+                                w.x = pack2<kBF>(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                                w.y = pack2<kBF>(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                                w.z = pack2<kBF>(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                                w.w = pack2<kBF>(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                                *reinterpret_cast<uint4*>(orow + q * 32 + v4 * 8) = w;
+                            }
+                        }
+                    }
+                } else {
+                    // partial of this prefix partition: reference maximum (log2
+                    // units), the sum relative to it, and O / l
+                    const int b = member_row >= 0 && member_row < p.S ? member_row : -1;
+                    const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + g) * p.NP + pp;
+                    if (b >= 0) {
+                        p.part_m[prow] = m_ref;
+                        p.part_l[prow] = l;
+                    }
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        tc::ld32(tO + q * 32, o);
+                        tc::wait_ld();
+                        if (b >= 0) {
+                            float4* po = reinterpret_cast<float4*>(p.part_o + prow * D + q * 32);
+#pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4)
+                                po[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
+                                                     __uint_as_float(o[4 * v4 + 2]) * inv,
+                                                     __uint_as_float(o[4 * v4 + 3]) * inv);
                         }
                     }
                 }
-            } else {
-                // partial of this prefix partition: reference maximum (log2
-                // units), the sum relative to it, and O / l
-                const int b = member_row >= 0 && member_row < p.S ? member_row : -1;
-                const int64_t prow = (static_cast<int64_t>(b) * p.Hq + h * G + g) * p.NP + pp;
-                if (b >= 0) {
-                    p.part_m[prow] = m_ref;
-                    p.part_l[prow] = l;
-                }
-#pragma unroll
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t o[32];
-                    tc::ld32(tO + q * 32, o);
-                    tc::wait_ld();
-                    if (b >= 0) {
-                        float4* po = reinterpret_cast<float4*>(p.part_o + prow * D + q * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            po[v4] = make_float4(__uint_as_float(o[4 * v4]) * inv, __uint_as_float(o[4 * v4 + 1]) * inv,
-                                                 __uint_as_float(o[4 * v4 + 2]) * inv,
-                                                 __uint_as_float(o[4 * v4 + 3]) * inv);
-                    }
+            } else if (!ok) {
+                if (lane == 0) {
+                    report(p.err, PKV_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
                 }
             }
-        } else if (!ok) {
-            if (lane == 0) {
-                report(p.err, PKV_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-            }
+            tp += ntx;
+            if (!ok || *abort_flag) break;
         }
     }
     tc::fence_before();
@@ -703,6 +884,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, 512);
+    }
+    if (!kPrefix && threadIdx.x == 0) {
+        // the last CTA to finish puts the launch's counters back to zero
+        __threadfence();
+        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(sched, 0u);
+            atomicExch(sched + 1, 0u);
+            __threadfence();
+        }
     }
 }
 
@@ -725,11 +915,15 @@ cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq
     return cudaGetLastError();
 }
 
+// Persistent prefill: one CTA per SM (one CTA fits an SM), or one per unit
+// when there are fewer; the launch takes the next counter slot.
 template <typename T>
-cudaError_t launch_prefill(const PrefillParams& p, int D, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_prefill(PrefillParams p, int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, cudaStream_t st) {
+    static std::atomic<uint32_t> next_slot{0};
+    p.sched_slot = static_cast<int32_t>(next_slot.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
     const int64_t units = p.work ? p.num_work : static_cast<int64_t>(p.num_qtiles) * p.S;
-    const dim3 grid(static_cast<unsigned>(units * p.Hkv));
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(units * p.Hkv, num_sms())));
     return D == 64 ? launch_tile<T, 64, false>(p, grid, tq, tk, tv, st)
                    : launch_tile<T, 128, false>(p, grid, tq, tk, tv, st);
 }
