@@ -331,6 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         pre.kv_end[1] = 0;
         pre.bt = p.block_tables + static_cast<int64_t>(seq0) * p.MB + b0;
     }
+    // unit k for a reading role: 1 = a unit, 0 = the list has ended, -1 =
+    // timeout.  The prefix pass has its one unit and uses no ring.
+    auto next_unit = [&](int k, bool whole_warp, Unit& u) -> int {
+        if constexpr (kPrefix) {
+            u = pre;
+            return k == 0 ? 1 : 0;
+        } else {
+            if (!take_unit(u_full, u_empty, unit_ring, k, whole_warp, u)) return -1;
+            return u.h >= 0 ? 1 : 0;
+        }
+    };
     unsigned int* sched = g_prefill_sched + 2 * p.sched_slot;
     const int64_t total = kPrefix ? 1
                           : (p.work ? static_cast<int64_t>(p.num_work) * p.Hkv
@@ -387,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // unit k is claimed once the S MMAs of unit k - 1 are issued (that
             // unit is in its last key tile), so a CTA holds at most one unit
             // ahead and the list stays longest first across the SMs
-            if (k > 0 && !done && !__all_sync(0xffffffffu, mbar_wait(q_empty, (k - 1) & 1))) {
+            if (!kPrefix && k > 0 && !done && !__all_sync(0xffffffffu, mbar_wait(q_empty, (k - 1) & 1))) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
@@ -415,14 +426,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const int slot = k % kUnitSlots;
-            if (k >= kUnitSlots && !__all_sync(0xffffffffu, mbar_wait(u_empty + slot, ((k / kUnitSlots) + 1) & 1))) {
+            if (kPrefix) {
+                if (u.h < 0) break;
+            } else if (k >= kUnitSlots &&
+                       !__all_sync(0xffffffffu, mbar_wait(u_empty + slot, ((k / kUnitSlots) + 1) & 1))) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
                 break;
             }
-            if (lane == 0) {
+            if (!kPrefix && lane == 0) {
                 unit_ring[slot] = u;
                 tc::arrive(u_full + slot);
             }
@@ -488,14 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool run = true;
         for (int k = 0; run; ++k) {
             Unit u;
-            if (!take_unit(u_full, u_empty, unit_ring, k, true, u)) {
+            const int r = next_unit(k, true, u);
+            if (r < 0) {
                 if (lane == 0) {
                     report(p.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
                 break;
             }
-            if (u.h < 0) break;
+            if (r == 0) break;
             const int kv_max = max(u.kv_end[0], u.kv_end[1]);
             const int nkt = (kv_max + kTileN - 1) / kTileN;
             const int nblk = (kv_max + kBlockSize - 1) / kBlockSize;
@@ -633,8 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int tp0 = 0, tp1 = 0;  // tiles of Q tiles A and B in the finished units
             for (int k = 0;; ++k) {
                 Unit u;
-                ok = take_unit(u_full, u_empty, unit_ring, k, false, u);
-                if (!ok || u.h < 0) break;
+                const int r = next_unit(k, false, u);
+                ok = r >= 0;
+                if (r <= 0) break;
                 const int nt0 = (u.kv_end[0] + kTileN - 1) / kTileN;
                 const int nt1 = (u.kv_end[1] + kTileN - 1) / kTileN;
                 const int nkt = max(nt0, nt1);
@@ -726,8 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tp = 0;  // tiles of this Q tile in the finished units
         for (int k = 0;; ++k) {
             Unit u;
-            ok = take_unit(u_full, u_empty, unit_ring, k, true, u);
-            if (!ok || u.h < 0) break;
+            const int r = next_unit(k, true, u);
+            ok = r >= 0;
+            if (r <= 0) break;
             const int h = u.h;
             const int ntx = ((X ? u.kv_end[1] : u.kv_end[0]) + kTileN - 1) / kTileN;
             bool row_valid;
