@@ -311,3 +311,55 @@ def test_prefill_sharp_softmax(lib, dtype, G):
     vmax = float(np.max(np.abs(orc.dequantize(np.concatenate([wl.v_pool.ravel(), wl.v_new.ravel()]), dtype))))
     extra = p_rounding_allowance(dtype, vmax)
     assert err <= TOL[dtype] + extra, (err, mx, extra)
+
+
+def test_prefill_persistent_grid_counters_graphs_and_streams(lib):
+    """The persistent prefill takes units from a per-call device counter that
+    its last CTA puts back to zero.  More calls in a row than there are
+    counters, replays of a captured call, and two calls running at once on two
+    streams all reproduce the eager result bit for bit."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import PrefillStep
+    wl = workloads.prefill("prefill_persist", 2500, [700, 0, 40, 2000, 5], [300, 600, 129, 77, 1000], 32, 8)
+    st = run(wl)
+    assert lib.get_device_error() == 0
+    err, mx = check_full(st)
+    assert err <= TOL["bf16"], (err, mx)
+    eager = host_bits(st.out).copy()
+    for _ in range(1100):  # wraps the library's 1024 counters
+        st.attend()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    assert np.array_equal(host_bits(st.out), eager)
+    # a captured call, replayed
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.attend(stream=side)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        st.attend()
+    for _ in range(3):
+        st.out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert lib.get_device_error() == 0
+        assert np.array_equal(host_bits(st.out), eager)
+    # two calls at once on two streams (each holds its own counter)
+    st2 = PrefillStep(wl, device="cuda")
+    st2.run()
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    st.out.zero_()
+    st2.out.zero_()
+    torch.cuda.synchronize()
+    for _ in range(20):
+        with torch.cuda.stream(s1):
+            st.attend(stream=s1)
+        with torch.cuda.stream(s2):
+            st2.attend(stream=s2)
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    assert np.array_equal(host_bits(st.out), eager)
+    assert np.array_equal(host_bits(st2.out), eager)
