@@ -427,9 +427,9 @@ size_t pkv_prefill_workspace_bytes(int32_t kv_dtype, int32_t num_seqs, int32_t n
  * writes to units[0 .. *num_units) every non-empty unit s * nq + qt of the
  * batch (see work_units above), sorted by the causal key range of the
  * unit's last query row, longest first (ties: sequence, then query tile,
- * ascending), so that the last CTAs to start are the shortest.  The batch
+ * ascending), so that the last units to start are the shortest.  The batch
  * may mix chunks over contexts of any length; scheduling long units first
- * keeps the last wave short.
+ * keeps the tail short.
  * query_start [num_seqs + 1], seq_lens [num_seqs]: HOST copies of the
  *   prefill call's arrays.  max_query_len, num_q_heads, num_kv_heads: as
  *   passed to the prefill call.

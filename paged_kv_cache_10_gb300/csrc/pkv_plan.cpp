@@ -1,16 +1,17 @@
 // pkv_plan.cpp -- host-side work plan for the paged prefill attention.
 //
-// The prefill kernel runs one CTA per (sequence s, pair of 128-row query
-// tiles qt, KV head h); a CTA's work is its causal key range, which grows
-// with the sequence's context (tokens already in the pool) and with qt.  A
-// batch of chunks over contexts of different lengths ([P1] on chunked
+// The prefill kernel's work comes in units (sequence s, pair of 128-row
+// query tiles qt, KV head h); a unit's work is its causal key range, which
+// grows with the sequence's context (tokens already in the pool) and with
+// qt.  A batch of chunks over contexts of different lengths ([P1] on chunked
 // prefill: a long prompt is cut into chunks that each attend to the KV of
-// the earlier ones) gives CTAs of very different lengths, and CTAs start in
-// grid order.  The plan lists the units (s, qt) longest key range first, so
-// that the last CTAs to start are the shortest ones (longest-processing-time
-// first list scheduling).  The host knows the batch (it scheduled it), so
-// the plan is built here, in plain C++, and passed to the kernel as a short
-// device array.
+// the earlier ones) gives units of very different lengths, and the kernel's
+// persistent CTAs take units in list order as they become free.  The plan
+// lists the units (s, qt) longest key range first, so that the last units
+// to start are the shortest ones (longest-processing-time first list
+// scheduling).  The host knows the batch (it scheduled it), so the plan is
+// built here, in plain C++, and passed to the kernel as a short device
+// array.
 #include <algorithm>
 #include <cstdint>
 #include <vector>
