@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -61,10 +62,21 @@ def decode_kernel_kind(wl) -> str:
     return "tensor_core" if (wl.Hq // wl.Hkv >= 2 and wl.D == 128) else "cuda_core"
 
 
+def code_only(src: str) -> str:
+    """Source text without // comments, trailing blanks and empty lines, so
+    an edit to comments alone leaves the hash (and recorded counters) valid."""
+    out = []
+    for line in src.splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def kernel_hash(kind: str) -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:12]
 
 

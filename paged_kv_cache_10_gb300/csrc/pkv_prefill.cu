@@ -9,23 +9,24 @@
 // history in the paged pool -- earlier chunks and their own chunk up to
 // themselves -- gathered through the block table like decode.
 //
-// One CTA takes 128 query rows of one (sequence, KV head): 128 / G tokens x
-// the G query heads of the group, so every key / value tile feeds all heads
-// that read it.  Per 128-key tile (8 pool blocks):
+// A unit of work is two Q tiles of 128 query rows of one (sequence, KV
+// head), each 128 / G tokens x the G query heads of the group, so every
+// key / value tile feeds all heads that read it and both Q tiles.  Per
+// 128-key tile (8 pool blocks):
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, fp32 in tensor memory
 //   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
 //   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory
-// Warp roles: warp 0 loads Q (once, by a 3-D TMA map) and the key tiles,
-// warp 6 the value tiles (per pool block, by the pool's 2-D map), each
-// through a 3-stage ring; warp 1 issues the MMAs and owns the tensor memory;
-// warps 2-5 run the online softmax, the O corrections and the epilogue, one
-// thread per query row, with packed two-lane fp32 arithmetic.
-// S is double-buffered in tensor memory and P_j is written back over S_j,
-// where the P V MMA reads it as its A operand; Q K^T of the next tile and
-// P V of the previous one run while the softmax works.  The running max is
-// rebased only when it grows by more than 2^8, which keeps every
-// probability <= 256 and skips most O corrections; the final O / l is the
-// same softmax.
+// Warp roles: warp 3 claims units and loads their Q tiles (3-D TMA map);
+// warp 0 streams the key tiles through a 3-stage ring and warp 2 the value
+// tiles through a 2-stage ring (per pool block, by the pool's 2-D map);
+// warp 1 issues the MMAs and owns the tensor memory; warps 4-7 and 8-11 run
+// the online softmax, the O corrections and the epilogue of Q tiles A and
+// B, one thread per query row, with packed two-lane fp32 arithmetic.
+// P_j is written back over S_j, where the P V MMA reads it as its A
+// operand; the two Q tiles ping-pong, so one tile's MMAs run while the
+// other's softmax works.  The running max is rebased only when it grows by
+// more than 2^8, which keeps every probability <= 256 and skips most O
+// corrections; the final O / l is the same softmax.
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
@@ -389,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------- unit claims and Q loads (warp 3)
         // Claims the next unit with a row, publishes it to the other warps
         // and loads its Q tiles (the S MMAs of the unit before, which read
-        // the Q buffers, are complete by then).  A claim past the list
-        // publishes -1 (done).
+        // the Q buffers, are complete by then).  When the list is exhausted
+        // it publishes an end marker (a unit with h = -1).  The prefix pass
+        // publishes nothing: every warp uses the CTA's one unit.
         const uint64_t pol_q = policy_evict_first();
         int k = 0, qloads = 0;
         bool done = false;
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     report(p.err, PKV_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
-                done = true;  // publishes -1
+                done = true;  // publishes the end marker
             }
             Unit u{};
             u.h = -1;  // the end of the list unless a claim finds a unit
