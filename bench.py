@@ -707,6 +707,52 @@ def run_prefill(args, rank, world, local_rank):
     return line
 
 
+# ------------------------------------------- prefill per-unit cost sweep
+def run_prefill_unit_sweep(args, local_rank):
+    """Separates the prefill kernel's cost per key tile from its fixed cost
+    per unit: batches of equal units (each sequence appends 64 tokens, 32/8
+    heads, D 128, bf16, so one unit per (sequence, KV head)) with 0, 1024 or
+    3072 tokens of context (1, 9 or 25 key tiles per unit), sized to 2 and 4
+    units per SM; times the attention call with CUDA events.  A linear fit of
+    time per unit round against key tiles gives both costs."""
+    import numpy as np
+    from paged_kv_cache_10_gb300 import pagedkv as pk
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import PrefillStep
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    points = []
+    for rounds in (2, 4):
+        S = sms * rounds // 8
+        for ctx in (0, 1024, 3072):
+            wl = workloads.prefill(f"unit_sweep_{ctx}", 5000 + ctx, [ctx] * S, [64] * S, 32, 8)
+            st = PrefillStep(wl, device=dev)
+            st.run()
+            for _ in range(max(args.warmup, 3)):
+                st.attend()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = max(args.steps, 10)
+            e0.record()
+            for _ in range(reps):
+                st.attend()
+            e1.record()
+            torch.cuda.synchronize()
+            assert pk.get_device_error() == 0, "device error word set during the sweep"
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            tiles = -(-(ctx + 64) // 128)
+            points.append({"rounds": rounds, "context": ctx, "key_tiles": tiles, "us": round(us, 2),
+                           "us_per_round": round(us / rounds, 2)})
+            del st
+            torch.cuda.empty_cache()
+    big = [q for q in points if q["rounds"] == 4]
+    slope, icpt = np.polyfit([q["key_tiles"] for q in big], [q["us_per_round"] for q in big], 1)
+    return {"metric": "prefill cost per unit round (equal units)", "unit": "us", "points": points,
+            "fit_4_rounds": {"us_per_key_tile": round(float(slope), 3), "us_per_unit": round(float(icpt), 2)},
+            "sms": sms}
+
+
 # ------------------------------------------------------ prefix-cache timing
 def run_apc(args):
     """Host-side automatic prefix caching on a request stream: 16 system
@@ -911,6 +957,8 @@ def main(argv=None):
                          "and no blocks are shared)")
     ap.add_argument("--no-plan", action="store_true",
                     help="prefill: CTAs in grid order instead of the host plan's longest-first order")
+    ap.add_argument("--prefill-unit-sweep", action="store_true",
+                    help="prefill kernel cost per key tile and per unit, from batches of equal units")
     ap.add_argument("--profile", action="store_true",
                     help="timed steps only (no e2e loop, clock-window extension or CPU baseline): for ncu runs")
     args = ap.parse_args(argv)
@@ -922,6 +970,8 @@ def main(argv=None):
         line = run_apc(args) if rank == 0 else None
     elif args.swap:
         line = run_swap(args, local_rank) if rank == 0 else None
+    elif args.prefill_unit_sweep:
+        line = run_prefill_unit_sweep(args, local_rank) if rank == 0 else None
     elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
