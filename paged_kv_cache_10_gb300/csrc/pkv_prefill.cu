@@ -97,6 +97,7 @@ struct PrefillParams {
     int32_t num_work;
     float qk_scale;              // scale * log2(e) (* k_scale for a staged fp8 pool)
     float o_scale = 1.f;         // factor on O / l: v_scale for a staged fp8 pool
+    int32_t out_v8 = 0;          // out is 32-byte aligned: 32-byte stores in the epilogue
     unsigned int* err;
     // cascade prefix pass only
     const int32_t* group_offsets;  // [groups + 1]
@@ -119,6 +120,13 @@ constexpr int kSchedSlots = 1024;
 __device__ unsigned int g_prefill_sched[2 * kSchedSlots];
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// One 32-byte store (p 32-byte aligned): a whole L2 sector per thread.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 
 // Two-lane fp32 arithmetic (one instruction, each lane rounded as the scalar
 // operation) and a three-input maximum.
@@ -852,7 +860,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t o[32];
                         tc::ld32(tO + q * 32, o);
                         tc::wait_ld();
-                        if (row_valid) {
+                        if (row_valid && p.out_v8) {
+#pragma unroll
+                            for (int v8 = 0; v8 < 2; ++v8) {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    w[i] = pack2<kBF>(__uint_as_float(o[16 * v8 + 2 * i]) * inv,
+                                                      __uint_as_float(o[16 * v8 + 2 * i + 1]) * inv);
+                                st_global_v8(orow + q * 32 + v8 * 16, w);
+                            }
+                        } else if (row_valid) {
 #pragma unroll
                             for (int v4 = 0; v4 < 4; ++v4) {
                                 uint4 w;
@@ -1154,6 +1172,7 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
     p.max_query_len = max_query_len;
     p.qk_scale = scale * (fp8 ? desc->k_scale : 1.f) * 1.4426950408889634f;
     p.o_scale = fp8 ? desc->v_scale : 1.f;
+    p.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;  // rows are multiples of 128 bytes
     p.err = err;
 
     CUtensorMap tq, tk, tv;

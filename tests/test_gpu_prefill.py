@@ -346,6 +346,16 @@ def test_prefill_persistent_grid_counters_graphs_and_streams(lib):
         torch.cuda.synchronize()
         assert lib.get_device_error() == 0
         assert np.array_equal(host_bits(st.out), eager)
+    # an output 16 bytes (not 32) into its buffer takes the 16-byte stores
+    buf = torch.zeros(st.out.numel() + 8, dtype=torch.uint16, device="cuda")
+    out16 = buf[8:].view(st.out.shape)
+    assert out16.data_ptr() % 32 == 16
+    lib.paged_attention_prefill(st.q, st.k_cache, st.v_cache, st.desc, st.d_query_start, wl.max_query_len,
+                                st.d_tables, st.d_lens, wl.scale, out16, q_dtype="bf16", work_units=st.work)
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    assert np.array_equal(host_bits(out16), eager)
+    assert np.all(host_bits(buf[:8]) == 0)
     # two calls at once on two streams (each holds its own counter)
     st2 = PrefillStep(wl, device="cuda")
     st2.run()
