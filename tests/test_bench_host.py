@@ -83,3 +83,14 @@ def test_prefill_flops_count_every_causal_pair():
     # brute force: each new row at position p sees keys 0..p; 4 * D flops per key and head
     pairs = sum(c + j + 1 for c, n in zip(WL.ctx, WL.qlens) for j in range(n))
     assert bench.prefill_flops(WL()) == 4.0 * 128 * 8 * pairs
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    """Recorded DRAM traffic is keyed by a hash of the kernel sources; an edit
+    to // comments or blank lines must keep the key, any code edit must not."""
+    import bench
+    src = "int a = 1;  // one\n\n// a comment line\nint b = 2;\n"
+    assert bench.code_only(src) == bench.code_only("int a = 1;\nint b = 2;  // two, reworded\n")
+    assert bench.code_only(src) != bench.code_only("int a = 1;\nint b = 3;\n")
+    for kind in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_hash(kind)) == 12
