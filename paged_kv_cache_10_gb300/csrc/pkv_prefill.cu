@@ -389,6 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Prefill launches as a programmatic dependent of the kernel before it
+    // (the fp8 staging pass, or the append): the setup above overlaps that
+    // kernel's last CTAs, and nothing here reads global memory before it has
+    // completed and its writes are visible.
+    if constexpr (!kPrefix) wait_primary_grid();
     // tensor-memory columns: S of Q tile X at X * 128 (its first 64 columns
     // then hold that tile's P, two 16-bit probabilities per column); O of Q
     // tile X at 256 + X * 128
@@ -948,6 +953,22 @@ cudaError_t launch_tile(const PrefillParams& p, dim3 grid, const CUtensorMap& tq
                                     kSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
+    if constexpr (!kPrefix) {
+        // a programmatic dependent of the kernel before it on the stream
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        la[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = la;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<T, D, kPrefix>, p, tq, tk, tv);
+        if (e != cudaErrorNotSupported && e != cudaErrorInvalidValue) return e;
+        (void)cudaGetLastError();  // a driver that refuses the attribute gets a plain launch
+    }
     prefill_tc_kernel<T, D, kPrefix><<<grid, kThreads, kSmemBytes, st>>>(p, tq, tk, tv);
     return cudaGetLastError();
 }
@@ -1010,6 +1031,8 @@ __global__ void __launch_bounds__(256) stage_fp8_kernel(const uint8_t* __restric
                                                         uint4* __restrict__ v_copy, int32_t* __restrict__ table_copy,
                                                         unsigned int* err) {
     constexpr bool kBF = std::is_same<T, BF16>::value;
+    // the attention kernel may start its setup once every CTA here has begun
+    allow_dependent_launch();
     const int j = blockIdx.x, s = blockIdx.y, z = blockIdx.z;
     const int L = __ldg(seq_lens + s);  // the attention pass reports a bad length
     const int nblk = L <= 0 ? 0 : min((L + kBlockSize - 1) / kBlockSize, MB);
