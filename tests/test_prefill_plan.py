@@ -106,3 +106,31 @@ def test_decode_plan_lists_every_unit_longest_first(pk):
     st = pk.lib().pkv_decode_plan(pk._np_ptr(lens), lens.size, 8, int(lens.max()), P, pk._np_ptr(out), 1,
                                   ctypes.byref(n))
     assert st == 5 and n.value == len(want)
+
+
+def test_fp8_prefill_workload_codes_and_scales():
+    """The fp8 prefill workload stores E4M3 codes under per-tensor scales
+    max|x| / 448 of each pool's N(0,1) source: finite codes only (no NaN,
+    0x7f / 0xff), the largest magnitude code reached, the same context
+    lengths and queries as the bf16 batch of the same seed, and a staging
+    workspace sized for its tables."""
+    import oracle
+    from paged_kv_cache_10_gb300 import pagedkv as pk, workloads
+    wl = workloads.PREFILL["prefill_chunked_gqa_fp8"]()
+    ref = workloads.PREFILL["prefill_chunked_gqa"]()
+    assert wl.kv_dtype == "e4m3" and wl.dtype == "bf16"
+    assert wl.ctx == ref.ctx and wl.qlens == ref.qlens
+    assert np.array_equal(wl.q, ref.q)
+    for pool, scale in ((wl.k_pool, wl.k_scale), (wl.v_pool, wl.v_scale)):
+        assert pool.dtype == np.uint8
+        assert not np.any((pool & 0x7f) == 0x7f)
+        vals = oracle.dequantize(pool.ravel()[:1 << 20], "e4m3")
+        assert np.all(np.isfinite(vals))
+        assert np.max(np.abs(vals)) <= 448.0
+        assert scale > 0
+    assert np.max(np.abs(oracle.dequantize(wl.k_pool, "e4m3"))) == 448.0
+    assert wl.k_scale != wl.v_scale
+    need = pk.prefill_workspace_bytes("e4m3", wl.S, wl.Hkv, wl.D, wl.max_blocks)
+    copy = wl.S * wl.max_blocks * wl.Hkv * 16 * wl.D * 2
+    assert need >= 2 * copy + wl.S * wl.max_blocks * 4
+    assert pk.prefill_workspace_bytes("bf16", wl.S, wl.Hkv, wl.D, wl.max_blocks) == 0
