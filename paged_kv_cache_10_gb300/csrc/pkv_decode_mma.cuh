@@ -8,9 +8,13 @@
 // heads of the group on the MMA's N = 8 columns:
 //
 //   S   [16 tok x 8 heads]  = K   [16 x 128] . Q^T [128 x 8]   (8 MMAs)
-//   O^T [128 d  x 8 heads] += V^T [128 x 16] . P^T [16 x 8]     (8 MMAs)
+//   O^T [128 d  x 8 heads] += V^T [128 x 16] . P^T [16 x 8]     (2 x 8 MMAs)
 //
-// with mma.m16n8k16 and fp32 accumulation.  For G = 8 every column is used
+// with mma.m16n8k16 and fp32 accumulation.  P enters the second product as
+// a 16-bit head and a 16-bit tail (its rounding error), one MMA each into the
+// same accumulator, so the probabilities keep 16 (bf16) or 22 (f16)
+// significant bits: rounded once to bf16 they alone could move an output by
+// 2^-9 of max|V|.  For G = 8 every column is used
 // (G = 4 / 2: half / a quarter).  The newer 5th-generation MMA needs M >= 64
 // and would round-trip the scores through tensor memory for the online
 // softmax every block; this path keeps scores, probabilities and output in
@@ -119,6 +123,25 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
+}
+
+// Two floats as a 16-bit pair (head) and the rounding error of that pair as a
+// second 16-bit pair (tail): head + tail carries 16 (bf16) or 22 (f16)
+// significant bits of each value.  The difference x - head is exact in
+// float32, so the tail is x - head rounded once.
+template <bool BF>
+__device__ __forceinline__ void pack2_split(float lo, float hi, uint32_t& head, uint32_t& tail) {
+    head = pack2<BF>(lo, hi);
+    float rl, rh;
+    if constexpr (BF) {
+        rl = __uint_as_float(head << 16);
+        rh = __uint_as_float(head & 0xffff0000u);
+    } else {
+        const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&head));
+        rl = r.x;
+        rh = r.y;
+    }
+    tail = pack2<BF>(lo - rl, hi - rh);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-row tile landed
@@ -380,9 +403,15 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                     o[i][3] *= alB;
                 }
             }
-            // P^T fragments: transpose the (token, head) 8x8 tiles of P
-            const uint32_t pb0 = movmatrix_t(pack2<kBF>(p0, p1));  // tokens 0..7
-            const uint32_t pb1 = movmatrix_t(pack2<kBF>(p2, p3));  // tokens 8..15
+            // P^T fragments: transpose the (token, head) 8x8 tiles of P.  P
+            // enters the product as a 16-bit head plus a 16-bit tail (two
+            // MMAs into the same float32 accumulator), so the probabilities
+            // keep 16 (bf16) or 22 (f16) significant bits, not 8 or 11.
+            uint32_t h01, t01, h23, t23;
+            pack2_split<kBF>(p0, p1, h01, t01);
+            pack2_split<kBF>(p2, p3, h23, t23);
+            const uint32_t pb0 = movmatrix_t(h01), pt0 = movmatrix_t(t01);  // tokens 0..7
+            const uint32_t pb1 = movmatrix_t(h23), pt1 = movmatrix_t(t23);  // tokens 8..15
             // ---- O^T += V^T P^T
             if constexpr (!kFP8) {
                 const int mat = lane >> 3, rr = lane & 7;
@@ -393,6 +422,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_t(vts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
                     mma16816a<kBF>(o[i], a0, a1, a2, a3, pb0, pb1);
+                    mma16816a<kBF>(o[i], a0, a1, a2, a3, pt0, pt1);
                 }
             } else {
                 const uint32_t wa[4] = {va[0].x, va[0].y, va[0].z, va[0].w};
@@ -407,6 +437,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                     e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), a01, a23);
                     e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), a45, a67);
                     mma16816a<false>(o[i], a01, a23, a45, a67, pb0, pb1);
+                    mma16816a<false>(o[i], a01, a23, a45, a67, pt0, pt1);
                 }
             }
         }

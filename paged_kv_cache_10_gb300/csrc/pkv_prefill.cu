@@ -15,14 +15,16 @@
 // 128-key tile (8 pool blocks):
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, fp32 in tensor memory
 //   P = exp2(S * scale * log2 e - m)    one thread per row, from tensor memory
-//   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory
+//   O += P V     tcgen05.mma with P from tensor memory, O in tensor memory;
+//                P as a 16-bit head plus a 16-bit tail (two MMAs into O), so
+//                the probabilities keep 16 (bf16) or 22 (f16) significant bits
 // Warp roles: warp 3 claims units and loads their Q tiles (3-D TMA map);
 // warp 0 streams the key tiles through a 3-stage ring and warp 2 the value
 // tiles through a 2-stage ring (per pool block, by the pool's 2-D map);
 // warp 1 issues the MMAs and owns the tensor memory; warps 4-7 and 8-11 run
 // the online softmax, the O corrections and the epilogue of Q tiles A and
 // B, one thread per query row, with packed two-lane fp32 arithmetic.
-// P_j is written back over S_j, where the P V MMA reads it as its A
+// P_j (head and tail) is written back over S_j, where the P V MMAs read it as their A
 // operand; the two Q tiles ping-pong, so one tile's MMAs run while the
 // other's softmax works.  The running max is rebased only when it grows by
 // more than 2^8, which keeps every probability <= 256 and skips most O
@@ -48,10 +50,10 @@ constexpr int kBlockTileBytes = kBlockSize * 128;  // 16 rows x 128 bytes
 // Three warpgroups: warps 0-3 load (0: Q and keys, 2: values), issue the
 // MMAs (1) or idle (3); warps 4-7 run the softmax of Q tile A, warps 8-11 of
 // Q tile B.  setmaxnreg moves registers from the first to the other two:
-// 128 x 88 + 256 x 208 = 384 x 168, the launch's allocation.
+// 128 x 104 + 256 x 192 <= 384 x 168, the launch's allocation.
 constexpr int kThreads = 384;
-constexpr int kLoadRegs = 88;
-constexpr int kSoftmaxRegs = 208;
+constexpr int kLoadRegs = 104;
+constexpr int kSoftmaxRegs = 192;
 static_assert(128 * kLoadRegs + 256 * kSoftmaxRegs <= kThreads * (65536 / kThreads / 8 * 8), "register split");
 constexpr int kSoftmaxWarps = 4;  // per Q tile
 constexpr float kRebase = 8.0f;   // log2 units
@@ -158,6 +160,27 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// Two probabilities as a 16-bit head pair and a 16-bit tail pair (the
+// head's remainder, rounded once): head + tail keeps 16 (bf16) or 22 (f16)
+// significant bits.  bf16: the head is the top half of each float32 (a
+// truncation: one byte permute), so the remainder x - head is the exact low
+// half; f16: the head is rounded to nearest and the remainder taken exactly.
+template <bool BF>
+__device__ __forceinline__ void split2(float2 a, uint32_t& head, uint32_t& tail) {
+    float2 t;
+    if constexpr (BF) {
+        const uint32_t ux = __float_as_uint(a.x), uy = __float_as_uint(a.y);
+        head = __byte_perm(ux, uy, 0x7632);
+        t = fadd2(a, make_float2(__uint_as_float((ux & 0xffff0000u) ^ 0x80000000u),
+                                 __uint_as_float((uy & 0xffff0000u) ^ 0x80000000u)));
+    } else {
+        head = pack2<false>(a.x, a.y);
+        const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&head));
+        t = fadd2(a, make_float2(-r.x, -r.y));
+    }
+    tail = pack2<BF>(t.x, t.y);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -652,10 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int X, int j, int g) {
                 const uint64_t v = (g % kVStages) ? dV1 : dV0;
                 const uint32_t d = tmem + 256 + X * kTileN, pa = tmem + X * kTileN;
+                // P's head (columns 0-63), then its tail (64-127), into the same O
 #pragma unroll
                 for (int kk = 0; kk < kTileN / 16; ++kk)
                     mma_f16_tmem_a(d, pa + kk * 8, v + static_cast<uint64_t>((kk * kBlockTileBytes) >> 4), idO,
                                    j > 0 || kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < kTileN / 16; ++kk)
+                    mma_f16_tmem_a(d, pa + 64 + kk * 8, v + static_cast<uint64_t>((kk * kBlockTileBytes) >> 4), idO,
+                                   true);
                 tc::commit(o_done + X);
             };
             bool ok = true;
@@ -815,21 +843,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float2 nm2 = make_float2(-m_ref, -m_ref);
                 float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                uint32_t pk[64];
+                // P as a 16-bit head (columns 0-63) and the head's rounding
+                // error as a 16-bit tail (columns 64-127, S's second half,
+                // already read): P V runs once on each, so the probabilities
+                // keep 16 (bf16) or 22 (f16) significant bits
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t pk[16], pl[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float2 a = ffma2(make_float2(__uint_as_float(x[q][2 * i]), __uint_as_float(x[q][2 * i + 1])), c2, nm2);
                         a.x = ex2(a.x);
                         a.y = ex2(a.y);
                         ls[i & 3] = fadd2(ls[i & 3], a);
-                        pk[q * 16 + i] = pack2<kBF>(a.x, a.y);
+                        split2<kBF>(a, pk[i], pl[i]);
                     }
+                    tc::st16(tS + q * 16, pk);
+                    tc::st16(tS + 64 + q * 16, pl);
+                }
                 const float2 lt = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
                 l = l * alpha + (lt.x + lt.y);
-                tc::st32(tS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-                tc::st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
                 if (j > 0 && __any_sync(0xffffffffu, rebase)) {
                     const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
