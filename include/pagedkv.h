@@ -216,9 +216,11 @@ pkv_status pkv_paged_attention_decode(const void* q, int32_t q_dtype, int32_t nu
  * GPU that loads it until the process exits).  A call whose scratch need,
  * pkv_decode_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len,
  * P) for the partition size P actually used, exceeds 32 MiB returns
- * PKV_ERR_WORKSPACE and launches nothing.  The first call on a device looks
- * up the array's device address (cudaGetSymbolAddress); make that first
- * call before any stream capture.  No cudaMalloc, cudaFree or allocating
+ * PKV_ERR_WORKSPACE and launches nothing.  Every call looks up the array's
+ * device address in the current context (cudaGetSymbolAddress, which
+ * allocates nothing); the first lookup on a device may load the library's
+ * device code, so make the first call on a device before any stream
+ * capture.  No cudaMalloc, cudaFree or allocating
  * routine is called.  All calls share the one array and it keeps whatever
  * the last call left there; nothing in it needs to start at zero (every
  * partial the merge reads is written first in the same call).  Calls whose
@@ -470,6 +472,19 @@ int32_t pkv_get_decode_path(void);
  * the given stream first.  *flags receives the bits.
  */
 pkv_status pkv_get_device_error(uint32_t* flags, void* stream);
+
+/*
+ * Check of the failure path of the kernels' bounded waits (no counterpart on
+ * the pages, which describe no device-side failure handling).  Enqueues one
+ * 32-thread CTA on `stream` that waits on a shared-memory mbarrier nothing
+ * ever arrives at and no copy feeds, with the wait routine of the decode
+ * kernels' copy pipelines (which = 0: at most 2^14 polls of up to 100 us
+ * each) or of the prefill's tensor-core pipeline (which = 1: 2 s of the
+ * global timer).  The wait gives up, PKV_DEVERR_TIMEOUT is set in the device
+ * error word and the kernel returns, leaving the context usable.  Expect the
+ * launch to take up to about 2 s.  PKV_ERR_INVALID for another `which`.
+ */
+pkv_status pkv_check_wait_timeout(int32_t which, void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* pkv_status_string(int32_t status);

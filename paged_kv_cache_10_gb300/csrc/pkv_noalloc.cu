@@ -14,7 +14,6 @@
 //
 // Nothing here calls cudaMalloc, cudaFree or any routine that allocates.
 #include <cstdint>
-#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -27,28 +26,21 @@ constexpr size_t kNoAllocScratchBytes = 32u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device.  In host code
+// Device address of g_noalloc_scratch in the current context.  In host code
 // the array's name is only a host-side handle, so the address is looked up
-// once per device with cudaGetSymbolAddress and cached.
+// with cudaGetSymbolAddress -- on every call, not cached: a cached address
+// would outlive a cudaDeviceReset or belong to another context of the same
+// device.  The lookup allocates nothing; the first one on a device may load
+// the library's device code, which is why the first call should come before
+// any stream capture.
 void* scratch_address(pkv_status* st) {
-    static void* cached[kMaxDevices] = {};
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
         *st = PKV_ERR_CUDA;
         return nullptr;
     }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cached[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-            *st = PKV_ERR_CUDA;
-            return nullptr;
-        }
-        cached[dev] = ptr;
-    }
     *st = PKV_OK;
-    return cached[dev];
+    return ptr;
 }
 
 }  // namespace

@@ -36,7 +36,7 @@ EXPORTED = [
     "pkv_paged_attention_prefill", "pkv_alloc_append_tokens", "pkv_block_hash", "pkv_prefix_block_hashes",
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
     "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
-    "pkv_prefill_plan", "pkv_decode_plan", "pkv_prefill_workspace_bytes",
+    "pkv_prefill_plan", "pkv_decode_plan", "pkv_prefill_workspace_bytes", "pkv_check_wait_timeout",
 ]
 
 
@@ -94,6 +94,7 @@ def lib():
                                                      P, i32, P]),
         "pkv_decode_auto_partition": (i32, [i32, i32, i32, i32, i32, i32]),
         "pkv_get_device_error": (i32, [u32p, P]),
+        "pkv_check_wait_timeout": (i32, [i32, P]),
         "pkv_set_decode_path": (i32, [i32]),
         "pkv_get_decode_path": (i32, []),
         "pkv_status_string": (ctypes.c_char_p, [i32]),
@@ -462,6 +463,14 @@ def get_device_error(stream=None) -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().pkv_get_device_error(ctypes.byref(flags), _stream(stream)), "get_device_error")
     return int(flags.value)
+
+
+def check_wait_timeout(which: int, stream=None) -> None:
+    """Enqueues the library's check of its bounded waits: one CTA waits on a
+    barrier nothing arrives at (which 0: the decode copy-pipeline wait, 1:
+    the prefill tensor-core pipeline wait) until the wait gives up and sets
+    DEVERR_TIMEOUT."""
+    _check(lib().pkv_check_wait_timeout(int(which), _stream(stream)), "check_wait_timeout")
 
 
 # ------------------------------------------------------------ host allocator

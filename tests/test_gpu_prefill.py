@@ -1,9 +1,8 @@
 """Paged (chunked) prefill attention on the GPU against the float64 oracle:
 every output element on small mixed batches (several query and key tiles,
 ragged tails, empty chunks, all group sizes, both 16-bit types, fp8 E4M3
-pools with per-tensor scales), sampled rows
-of the full-size workloads (each sampled token is one decode row of the
-oracle at its own position), the appended pool bytes, and the error paths."""
+pools with per-tensor scales), every token of the full-size workloads, the
+appended pool bytes, and the error paths."""
 import numpy as np
 import pytest
 import torch
@@ -162,37 +161,16 @@ def test_prefill_fp8_cache_errors(lib):
 
 @pytest.mark.parametrize("name", ["prefill_chunked_gqa", "prefill_prompt_gqa", "prefill_prompt_mha",
                                   "prefill_chunked_gqa_fp8"])
-def test_prefill_full_size_sampled_rows(lib, name):
+def test_prefill_full_size_every_token(lib, name):
+    """The full-size prefill workloads in the launch configuration the
+    benchmark times: every token and head against the oracle's causal
+    prefill, the appended pool bytes bit for bit."""
     from paged_kv_cache_10_gb300 import workloads
     wl = workloads.PREFILL[name]()
     st = run(wl)
     assert lib.get_device_error() == 0
-    slots, tables, lens = model(wl)
-    assert np.array_equal(st.slots, slots) and np.array_equal(st.tables, tables)
-    kp, vp = oracle_pools(wl, slots)
-    # sampled tokens: first and last of every chunk plus a stride through it
-    rows, seqs, pos = [], [], []
-    qs = st.query_start
-    for s in range(wl.S):
-        n = wl.qlens[s]
-        for j in sorted({0, n - 1, *range(0, n, 97)}):
-            rows.append(qs[s] + j)
-            seqs.append(s)
-            pos.append(int(lens[s]) - n + j)
-    rows = np.array(rows)
-    # one decode row of the oracle per sampled token: its own position is the
-    # last key it may see
-    ref = oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.dtype, kp, vp, wl.kv_dtype,
-                              np.ascontiguousarray(tables[seqs]), np.array(pos, np.int32) + 1, wl.scale,
-                              wl.k_scale, wl.v_scale)
-    got = oracle.dequantize(host_bits(st.out)[rows], wl.dtype)
-    assert np.all(np.isfinite(got))
-    err = max_error(got, ref, wl.dtype, TOL[wl.kv_dtype])
-    assert err <= TOL[wl.kv_dtype], err
-    # every row was written (finite) and the appended pool bytes match
-    assert np.all(np.isfinite(oracle.dequantize(host_bits(st.out), wl.dtype)))
-    assert np.array_equal(host_bits(st.k_cache), kp)
-    assert np.array_equal(host_bits(st.v_cache), vp)
+    err, mx = check_full(st)
+    assert err <= TOL[wl.kv_dtype], (err, mx)
 
 
 def test_prefill_ignores_nan_bytes_past_the_sequence_end(lib):
