@@ -17,16 +17,45 @@ namespace pkv {
 // Device error word: the OR of PKV_DEVERR_* bits reported by the kernels.
 __device__ unsigned int g_device_error = 0;
 
+namespace {
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no libcuda link).
+CtxGetCurrent ctx_get_current() {
+    static CtxGetCurrent fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrent>(f);
+    });
+    return fn;
+}
+}  // namespace
+
+// The error word's device address is cached per device together with the
+// context it was looked up in, and looked up again whenever the current
+// context differs (after a cudaDeviceReset, or under another context of the
+// same device), so a stale address is never handed to a kernel.
 unsigned int* error_word() {
+    static CUcontext ctxs[kMaxDevices] = {};
     static unsigned int* ptrs[kMaxDevices] = {};
     static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const CtxGetCurrent get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
+    if (!ptrs[dev] || !ctx || ctx != ctxs[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
         ptrs[dev] = static_cast<unsigned int*>(p);
+        CUcontext now = nullptr;  // the lookup may have made the primary context current
+        if (get && get(&now) != CUDA_SUCCESS) now = nullptr;
+        ctxs[dev] = now;
     }
     return ptrs[dev];
 }
