@@ -282,11 +282,68 @@ def barrier():
         dist.barrier()
 
 
-# ------------------------------------------------------------- oracle timing
+# ---------------------------------------------------------------- oracle leg
+# The float64 oracle runs only in this leg (and in the reference arm below):
+# it times the oracle on bounded samples of the workload (cpu_baseline) and,
+# outside every timed region, recomputes the whole measured step to report
+# the GPU output's error.  Nothing it computes feeds the GPU path.
+TOL = {"f16": 2e-3, "bf16": 1e-2, "e4m3": 1e-2}  # max-abs bounds on the attention output
+_MANT = {"f16": 10, "bf16": 7}
+FP32_TERM = 2.0 ** -14
+
+
+def error_bound(ref: np.ndarray, out_dtype: str, tol: float, vmax: float) -> np.ndarray:
+    """Per-element bound on |out - oracle|: `tol`, except where half a unit in
+    the last place of the 16-bit output format at the oracle value exceeds
+    it (bf16 |out| >= 4, f16 |out| >= 8), where no value of that format can
+    meet it: there half that unit plus twice the float32 term 2^-14 * max|V|."""
+    a = np.maximum(np.abs(ref), np.finfo(np.float64).tiny)
+    half = 0.5 * np.exp2(np.floor(np.log2(a)) - _MANT[out_dtype])
+    return np.where(half > tol, half + 2.0 * FP32_TERM * vmax, tol)
+
+
+def oracle_host_step(wl):
+    """Slots, copy-on-write pairs, block tables and lengths of the step from
+    the oracle's own allocator model (the workload's script replayed)."""
+    from oracle.allocator_model import AllocatorModel
+    m = AllocatorModel(wl.NB, wl.b, wl.free_order)
+    for op in wl.setup:
+        if op[0] == "new":
+            m.seq_new(op[1], op[2])
+        elif op[0] == "fork":
+            m.fork(op[1], op[2])
+        elif op[0] == "extend":
+            for _ in range(op[2]):
+                m.append_slot(op[1])
+        elif op[0] == "free":
+            m.free_seq(op[1])
+    slots = np.full(wl.S, -1, np.int64)
+    pairs = []
+    for s in wl.step_seqs:
+        slot, cow = m.append_slot(s)
+        slots[s] = slot
+        if cow:
+            pairs.append(cow)
+    tables = np.full((wl.S, wl.max_blocks), -1, np.int32)
+    lens = np.zeros(wl.S, np.int32)
+    for s in range(wl.S):
+        t = m.block_table(s)
+        tables[s, :len(t)] = t
+        lens[s] = m.lens[s]
+    return slots, np.array(pairs, np.int32).reshape(-1, 2), tables, lens
+
+
+class HostStep:
+    """The host bookkeeping of one decode step (no device state)."""
+
+    def __init__(self, wl, slots, pairs, tables, lens):
+        self.wl, self.slots, self.pairs, self.tables, self.seq_lens = wl, slots, pairs, tables, lens
+
+
 def oracle_rows_step(wl, step, rows, pools):
     """The float64 oracle on rows of the workload: their append and their
     decode (plus the copy-on-write copies of the step).  ``pools`` = (k, v)
-    numpy pools updated in place (idempotent)."""
+    numpy pools updated in place (idempotent).  Returns the decode output."""
     import oracle
     kp, vp = pools
     if len(step.pairs):
@@ -294,9 +351,9 @@ def oracle_rows_step(wl, step, rows, pools):
     sl = np.full(wl.S, -1, np.int64)
     sl[rows] = step.slots[rows]
     oracle.append(wl.k_new, wl.v_new, wl.in_dtype, sl, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
-    oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.q_dtype, kp, vp, wl.kv_dtype,
-                        np.ascontiguousarray(step.tables[rows]), np.ascontiguousarray(step.seq_lens[rows]),
-                        wl.scale, wl.k_scale, wl.v_scale)
+    return oracle.paged_decode(np.ascontiguousarray(wl.q[rows]), wl.q_dtype, kp, vp, wl.kv_dtype,
+                               np.ascontiguousarray(step.tables[rows]), np.ascontiguousarray(step.seq_lens[rows]),
+                               wl.scale, wl.k_scale, wl.v_scale)
 
 
 def rows_bytes(step, rows) -> int:
@@ -309,12 +366,9 @@ def rows_bytes(step, rows) -> int:
     return kv + other + app
 
 
-def cpu_baseline(wl, step, budget_s=10.0):
-    """The oracle on whole-sequence samples of the workload: as many
-    sequences as fit the budget, repeated over the batch until ~budget_s of
-    CPU time has been spent."""
-    import oracle
-    pools = (wl.k_pool.copy(), wl.v_pool.copy())
+def _time_oracle(wl, step, pools, budget_s):
+    """Whole sequences (all heads) through the oracle, repeated over the
+    batch until ~budget_s of CPU time: (GB/s, reps, sequences per rep, s)."""
     t = time.perf_counter()
     oracle_rows_step(wl, step, np.array([0]), pools)
     one = max(time.perf_counter() - t, 1e-3)
@@ -327,20 +381,111 @@ def cpu_baseline(wl, step, budget_s=10.0):
         dt += time.perf_counter() - t
         done += rows_bytes(step, rows)
         reps += 1
-    return {"value": done / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reps} x {n} of {wl.S} sequences of {wl.name} (all heads): their append + float64 "
-                      f"decode, {dt:.1f} s"}
+    return done / dt / 1e9, reps, n, dt
+
+
+def cpu_baseline(wl, step, budget_s=10.0, single_s=3.0):
+    """The oracle on whole-sequence samples of the workload, on all host
+    cores (about budget_s of CPU time) and on one core (about single_s)."""
+    import oracle
+    pools = (wl.k_pool.copy(), wl.v_pool.copy())
+    cores = oracle.num_threads()
+    gbs, reps, n, dt = _time_oracle(wl, step, pools, budget_s)
+    out = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+           "sample": f"{reps} x {n} of {wl.S} sequences of {wl.name} (all heads): their append + float64 "
+                     f"decode, {dt:.1f} s"}
+    if single_s > 0:
+        oracle.set_num_threads(1)
+        try:
+            g1, r1, n1, d1 = _time_oracle(wl, step, pools, single_s)
+        finally:
+            oracle.set_num_threads(cores)
+        out["single_thread"] = {"value": round(g1, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{r1} x {n1} sequences, {d1:.1f} s"}
+    return out
+
+
+def oracle_parity(step) -> dict:
+    """Untimed: the whole step (copy-on-write copies, appends, every row's
+    decode) recomputed by the oracle from its own allocator model, against
+    the GPU's host bookkeeping, pools and output."""
+    import oracle
+    wl = step.wl
+    t0 = time.perf_counter()
+    slots, pairs, tables, lens = oracle_host_step(wl)
+    host_ok = (np.array_equal(step.slots, slots) and np.array_equal(np.asarray(step.pairs).reshape(-1, 2), pairs)
+               and np.array_equal(step.tables, tables) and np.array_equal(step.seq_lens, lens))
+    hs = HostStep(wl, slots, pairs, tables, lens)
+    pools = (wl.k_pool.copy(), wl.v_pool.copy())
+    ref = oracle_rows_step(wl, hs, np.arange(wl.S), pools)
+
+    def bits(t):
+        t = t.detach().cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 else t.view(torch.uint8).numpy()
+
+    pools_ok = bool(np.array_equal(bits(step.k_cache), pools[0]) and np.array_equal(bits(step.v_cache), pools[1]))
+    got = oracle.dequantize(bits(step.out), wl.q_dtype)
+    tol = TOL[wl.kv_dtype]
+    vmax = float(np.max(np.abs(oracle.dequantize(pools[1], wl.kv_dtype)))) * (wl.v_scale if wl.kv_dtype == "e4m3"
+                                                                               else 1.0)
+    err = np.abs(got - ref)
+    over = float(np.max(err - error_bound(ref, wl.q_dtype, tol, vmax))) if ref.size else -tol
+    return {"rows": int(wl.S), "max_abs_err": float(err.max()) if ref.size else 0.0,
+            "max_abs_oracle": float(np.abs(ref).max()) if ref.size else 0.0, "tol": tol,
+            "within_tolerance": bool(over <= 0 and np.all(np.isfinite(got))),
+            "max_err_minus_bound": over, "pools_bit_exact": pools_ok, "host_bookkeeping_exact": bool(host_ok),
+            "oracle_s": round(time.perf_counter() - t0, 2),
+            "basis": "every row and head of the step against the float64 oracle; bound: max-abs tol, or half an "
+                     "ulp of the output format + 2^-13 max|V| where that half ulp exceeds tol"}
+
+
+def kv_utilisation(step) -> dict:
+    """Share of the block slots the batch holds that carry a token (distinct
+    blocks, a shared block counted once) and the largest per-sequence waste
+    (slots of its last block past its length; at most block_size - 1)."""
+    wl = step.wl
+    lens = step.seq_lens.astype(np.int64)
+    nb = (lens + wl.b - 1) // wl.b
+    ids, valid = [], []
+    for r in range(wl.S):
+        if nb[r]:
+            ids.append(step.tables[r, :nb[r]].astype(np.int64))
+            valid.append(np.minimum(wl.b, lens[r] - wl.b * np.arange(nb[r])))
+    if not ids:
+        return {"utilisation": 1.0, "max_waste_tokens_per_seq": 0, "distinct_blocks": 0}
+    ids, valid = np.concatenate(ids), np.concatenate(valid)
+    best = np.zeros(int(ids.max()) + 1, np.int64)
+    np.maximum.at(best, ids, valid)
+    used = np.unique(ids)
+    return {"utilisation": round(float(best[used].sum()) / (len(used) * wl.b), 5),
+            "max_waste_tokens_per_seq": int((nb * wl.b - lens).max()), "distinct_blocks": int(len(used)),
+            "bound": f"waste <= block_size - 1 = {wl.b - 1} tokens per sequence"}
 
 
 # ----------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+# every decode config of the benchmark, in the order the default run times them
+DECODE_CONFIGS = [
+    ("tiny_fp16", False, False),
+    ("llama7b_mha", False, False),
+    ("llama3_8b_gqa", False, False),
+    ("longctx_fp8", False, False),
+    ("prefix_share", False, False),
+    ("prefix_share", True, True),  # shared-prefix (cascade) decode, each step one CUDA-graph replay
+]
+
+
+def measure_decode(args, rank, world, local_rank, name, cascade=False, graph=False, steps=None, sampler=None,
+                   oracle_leg=True, cpu_budget=10.0):
+    """Times one decode workload (K device-timed steps, the decode call's
+    launches, the e2e loop) and, on rank 0 of a single-GPU run, the oracle
+    leg.  Returns the JSON line of the workload (rank 0) or None."""
     from paged_kv_cache_10_gb300 import workloads
     from paged_kv_cache_10_gb300.step import DecodeStep
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = workloads.NAMED[args.workload]()
-    step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=args.cascade,
+    wl = workloads.NAMED[name]()
+    step = DecodeStep(wl, device=dev, partition_tokens=args.partition, cascade=cascade,
                       fused=not args.unfused, plan={"auto": "auto", "on": True, "off": False}[args.decode_plan])
     nbytes = step_bytes(step)
     stream = torch.cuda.current_stream()
@@ -352,15 +497,14 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(max(args.warmup, 3)):
         step.run()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank) if rank == 0 else None
 
-    K = args.steps
+    K = steps or args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    graph = step.capture() if args.graph else None
-    if graph is not None:
+    g = step.capture() if graph else None
+    if g is not None:
         for _ in range(max(args.warmup, 3)):
-            graph.replay()
+            g.replay()
     barrier()
     torch.cuda.synchronize()
     t_load0 = time.monotonic()
@@ -369,8 +513,8 @@ def run_ours(args, rank, world, local_rank):
             flush_buf.zero_()
         a, b, c = ev[i]
         a.record(stream)
-        if graph is not None:
-            graph.replay()  # the whole step, one launch
+        if g is not None:
+            g.replay()  # the whole step, one launch
         else:
             step.copy()
             step.append()
@@ -385,7 +529,7 @@ def run_ours(args, rank, world, local_rank):
         total_ms = sum(step_ms)
     else:
         total_ms = ev[0][0].elapsed_time(ev[-1][2])
-    if graph is None:
+    if g is None:
         decode_ms = [b.elapsed_time(c) for _, b, c in ev]
     else:
         # kernel roofline from replays of a graph holding the decode call
@@ -455,8 +599,6 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     clocks = sampler.summary(t_load0, t_load1) if sampler else None
-    if sampler:
-        sampler.stop()
     peak, peak_kind = measured_peaks()
     dec_ms = statistics.mean(decode_ms)
     # Where sequences share blocks the kernel need only read each distinct
@@ -467,8 +609,9 @@ def run_ours(args, rank, world, local_rank):
     if step.fused:  # the timed decode launch also writes the step's new tokens and copy-on-write copies
         roof_bytes += nbytes["append"] + nbytes["copy"]
     achieved = roof_bytes / (dec_ms / 1e3) / 1e9
-    kind = decode_kernel_kind(wl) if not args.cascade else "cascade"
-    traffic = recorded_traffic(args.workload, kind)
+    kind = decode_kernel_kind(wl) if not cascade else "cascade"
+    traffic_name = name + ("_cascade" if cascade else "")
+    traffic = recorded_traffic(traffic_name, kind)
     ms_per_step = total_ms / K
     line = {
         "metric": METRIC,
@@ -499,7 +642,7 @@ def run_ours(args, rank, world, local_rank):
                                              f"inputs larger than L2 ({working_set / 2**20:.0f} MiB vs "
                                              f"{l2 / 2**20:.0f} MiB), no flush"),
             "parallelism": f"replicas x{world}",
-            "launch": ("CUDA graph replay per step" if args.graph else "eager launches")
+            "launch": ("CUDA graph replay per step" if graph else "eager launches")
                       + ("; append fused into the decode kernel" if step.fused else ""),
             "cta_order": ("host plan, longest unit first" if step.work is not None else "grid order"),
         },
@@ -507,7 +650,8 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": d2h, "steps": Ke, "copies": E2E_COPIES},
         "gpu_launches": K * step.kernel_launches(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4), "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": {"tensor_core": "decode_mma_kernel (+ merge when split)",
                                 "cuda_core": "decode_kernel (+ merge when split)",
                                 "cascade": "prefill_tc_kernel prefix pass + decode kernel + merge"}[kind]
@@ -515,16 +659,62 @@ def run_ours(args, rank, world, local_rank):
                      "kernel_sources_hash": kernel_hash(kind),
                      "mean_launch_us": round(dec_ms * 1e3, 2),
                      "median_launch_us": round(statistics.median(decode_ms) * 1e3, 2),
-                     "launch_timing": ("decode call replayed as a CUDA graph" if graph is not None
+                     "launch_timing": ("decode call replayed as a CUDA graph" if g is not None
                                        else "eager decode call inside the timed steps"),
                      "algorithmic_bytes_per_launch": roof_bytes,
                      "bytes_basis": ("distinct KV bytes (blocks shared between sequences counted once)" if shared
                                      else "KV bytes gathered through the block tables"),
                      "logical_gbs": round(nbytes["decode"] / (dec_ms / 1e3) / 1e9, 1)},
         "clocks": clocks,
+        "kv_utilisation": kv_utilisation(step),
     }
-    if world == 1 and not (args.no_cpu_baseline or args.profile):
-        line["cpu_baseline"] = cpu_baseline(wl, step)
+    if world == 1 and oracle_leg and not (args.no_cpu_baseline or args.profile):
+        line["parity"] = oracle_parity(step)
+        line["cpu_baseline"] = cpu_baseline(wl, step, budget_s=cpu_budget, single_s=min(3.0, cpu_budget))
+    del step, g
+    torch.cuda.empty_cache()
+    return line
+
+
+def config_summary(line) -> dict:
+    """The per-config fields of a workload's line."""
+    r = line["roofline"]
+    keep = ("us_per_step", "median_us_per_step", "tokens_per_s", "value", "unit", "pct_of_hbm_peak",
+            "pct_of_nominal_8tbs", "dtype", "steps", "gpu_launches", "clocks", "kv_utilisation", "parity",
+            "cpu_baseline")
+    out = {k: line[k] for k in keep if k in line}
+    out["kv_gbs"] = line["value"]
+    out["e2e"] = {k: line["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+    out["roofline"] = {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "frac_of_nominal_8tbs",
+                                        "traffic", "mean_launch_us", "median_launch_us", "kernel", "bytes_basis",
+                                        "logical_gbs", "algorithmic_bytes_per_launch")}
+    c = line["config"]
+    out["config"] = {k: c[k] for k in ("workload", "num_seqs", "q_heads", "kv_heads", "head_size", "kv_dtype",
+                                       "mean_seq_len", "partition_tokens", "cow_pairs", "decode", "l2", "launch",
+                                       "cta_order")}
+    return out
+
+
+def run_ours(args, rank, world, local_rank):
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    try:
+        line = measure_decode(args, rank, world, local_rank, args.workload, args.cascade, args.graph,
+                              sampler=sampler)
+        if args.configs == "all" and world == 1:
+            # every decode config timed in the same run (the headline's fields stay its own)
+            configs = {}
+            for name, casc, graph in DECODE_CONFIGS:
+                key = name + ("_cascade" if casc else "")
+                if (name, casc, graph) == (args.workload, args.cascade, args.graph):
+                    configs[key] = config_summary(line)
+                    continue
+                ln = measure_decode(args, rank, world, local_rank, name, casc, graph,
+                                    steps=min(args.steps, 100), sampler=sampler, cpu_budget=4.0)
+                configs[key] = config_summary(ln)
+            line["configs"] = configs
+    finally:
+        if sampler:
+            sampler.stop()
     return line
 
 
@@ -558,16 +748,31 @@ def measured_tensor_peak():
     return 1900.0, "fallback"
 
 
+def oracle_prefill_host(wl):
+    """Slots of the chunk's tokens, block tables and lengths of a prefill
+    step from the oracle's own allocator model."""
+    from oracle.allocator_model import AllocatorModel
+    m = AllocatorModel(wl.NB, wl.b, wl.free_order)
+    for s, c in enumerate(wl.ctx):
+        m.seq_new(s, int(c))
+    slots = []
+    for s, n in enumerate(wl.qlens):
+        for _ in range(int(n)):
+            slots.append(m.append_slot(s)[0])
+    tables = np.full((wl.S, wl.max_blocks), -1, np.int32)
+    lens = np.zeros(wl.S, np.int32)
+    for s in range(wl.S):
+        t = m.block_table(s)
+        tables[s, :len(t)] = t
+        lens[s] = m.lens[s]
+    return np.array(slots, np.int64), tables, lens
+
+
 def prefill_cpu_baseline(wl, budget_s=10.0):
     """The float64 oracle on the first tokens of each chunk in turn (all
     heads, each with every key it sees), about budget_s of CPU time."""
     import oracle
-    from paged_kv_cache_10_gb300.pagedkv import Allocator
-    a = Allocator(wl.NB, wl.b, wl.free_order)
-    for s, c in enumerate(wl.ctx):
-        a.seq_new(s, int(c))
-    slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
-    tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
+    slots, tables, lens = oracle_prefill_host(wl)
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
     oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
     qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
@@ -842,12 +1047,7 @@ def run_reference_prefill(args, wl):
     float64 causal attention of the first tokens of one chunk (all heads,
     every key they see), rotating through the sequences."""
     import oracle
-    from paged_kv_cache_10_gb300.pagedkv import Allocator
-    a = Allocator(wl.NB, wl.b, wl.free_order)
-    for s, c in enumerate(wl.ctx):
-        a.seq_new(s, int(c))
-    slots, _ = a.append_tokens(np.arange(wl.S), wl.qlens)
-    tables, lens = a.export(np.arange(wl.S), wl.max_blocks)
+    slots, tables, lens = oracle_prefill_host(wl)
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
     oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
     qs = np.concatenate([[0], np.cumsum(wl.qlens)]).astype(np.int64)
@@ -889,24 +1089,13 @@ def run_reference(args, rank, world):
         return None
     import oracle
     from paged_kv_cache_10_gb300 import workloads
-    from paged_kv_cache_10_gb300.pagedkv import Allocator, apply_setup
 
     oracle.build()
     if args.workload in workloads.PREFILL:
         return run_reference_prefill(args, workloads.PREFILL[args.workload]())
     wl = workloads.NAMED[args.workload]()
-
-    class HostStep:  # the host bookkeeping of the step, through the C++ allocator
-        pass
-
-    st = HostStep()
-    st.wl = wl
-    a = Allocator(wl.NB, wl.b, wl.free_order)
-    apply_setup(a, wl.setup)
-    appending = np.full(wl.S, -1, np.int64)
-    appending[np.asarray(wl.step_seqs)] = np.asarray(wl.step_seqs)
-    st.slots, st.pairs = a.append_batch(appending)
-    st.tables, st.seq_lens = a.export(np.arange(wl.S), wl.max_blocks)
+    # the host bookkeeping of the step from the oracle's allocator model
+    st = HostStep(wl, *oracle_host_step(wl))
     pools = (wl.k_pool.copy(), wl.v_pool.copy())
     K, W = args.steps, args.warmup
     # one sequence (all heads) per step, rotating through the batch
@@ -951,7 +1140,11 @@ def main(argv=None):
                     help="append with its own kernel before the decode (default: fused into the decode kernel)")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix decode: blocks shared by a group of sequences are read once per group")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle leg (cpu_baseline timing and the untimed parity check)")
+    ap.add_argument("--configs", choices=["all", "none"], default=None,
+                    help="also time every decode config in the same run and report each under 'configs' "
+                         "(default: all for the default workload on one GPU, none otherwise)")
     ap.add_argument("--decode-plan", choices=["auto", "on", "off"], default="auto",
                     help="decode: CTAs in the host plan's longest-first order (auto: when unit lengths differ "
                          "and no blocks are shared)")
@@ -963,6 +1156,9 @@ def main(argv=None):
                     help="timed steps only (no e2e loop, clock-window extension or CPU baseline): for ncu runs")
     args = ap.parse_args(argv)
 
+    if args.configs is None:
+        args.configs = ("all" if (args.workload == DEFAULT_WORKLOAD and not args.cascade and not args.graph
+                                  and not args.profile and args.partition is None) else "none")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

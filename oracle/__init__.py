@@ -80,6 +80,8 @@ def bind(lib):
         lib.pkvo_copy_blocks.restype = i32
         lib.pkvo_num_threads.argtypes = []
         lib.pkvo_num_threads.restype = i32
+        lib.pkvo_set_num_threads.argtypes = [i32]
+        lib.pkvo_set_num_threads.restype = None
     return lib
 
 
@@ -90,6 +92,11 @@ def _ptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().pkvo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (timing only)."""
+    _load().pkvo_set_num_threads(int(n))
 
 
 # ----------------------------------------------------------------- formats

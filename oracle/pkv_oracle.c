@@ -453,3 +453,13 @@ int pkvo_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Threads the OpenMP loops above use from now on (at least 1); timing aid
+ * only, the results do not depend on it. */
+void pkvo_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : 1);
+#else
+    (void)n;
+#endif
+}
