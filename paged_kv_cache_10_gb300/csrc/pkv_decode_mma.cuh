@@ -145,10 +145,22 @@ __device__ __forceinline__ void pack2_split(float lo, float hi, uint32_t& head, 
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a 128-byte-row tile landed
-// with the 128-byte swizzle.
+// with the 128-byte swizzle.  For even r: swz128(r, c ^ 1) = swz128(r, c) ^ 16,
+// swz128(r + 1, c) = (swz128(r, c) ^ 16) + 128, and swz128(r + 8, c) =
+// swz128(r, c) + 1024.
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// The online softmax's reference maximum is moved only when a block's
+// maximum exceeds it by more than this many log2 units (probabilities <= 2^8).
+constexpr float kRebaseLog2 = 8.0f;
 
 // Copy stages per warp and resident CTAs per SM: about 190 KB of tiles in
 // flight per SM either way; fp8 tiles are half the size, so twice the warps
@@ -235,13 +247,15 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
 
     int tbl = -1;
     int k_issue = 0;
+    int issue_stage = 0;  // k_issue % NST, kept incrementally
     auto issue_next = [&]() {  // warp-uniform call
         if ((k_issue & 31) == 0) {
             const int k = k_issue + lane;
             tbl = k < nb_w ? __ldg(bt + static_cast<int64_t>(k) * NW) : -1;
         }
         const int phys = __shfl_sync(kFull, tbl, k_issue & 31);
-        const int stage = k_issue % NST;
+        const int stage = issue_stage;
+        issue_stage = issue_stage + 1 == NST ? 0 : issue_stage + 1;
         if (append_here && k_issue == nb_w - 1) {
             fused_commit<KT>(p, h, frow);
             __syncwarp();
@@ -302,10 +316,21 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;  // heads 2qd (A), 2qd+1 (B)
 
+    // fp8 fragment offsets in a stage's tiles: K chunk 2qd of row g8, V chunk
+    // g8 of row 2qd (the stage bases are 1024-byte aligned)
+    const uint32_t koff = swz128(g8, 2 * qd), voff = swz128(2 * qd, g8);
     bool aborted = false;
+    int stage = 0;
+    uint32_t phase = 0;  // (k / NST) & 1
     for (int k = 0; k < nb_w; ++k) {
-        const int stage = k % NST;
-        if (!mbar_wait(&bars[stage], (k / NST) & 1)) {
+        if (k > 0) {
+            ++stage;
+            if (stage == NST) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!mbar_wait(&bars[stage], phase)) {
             if (lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
             aborted = true;
             break;
@@ -330,14 +355,15 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                 __syncwarp();
             }
             // fp8: value bytes loaded up front (chunk g8 of tokens 2qd, 2qd+1,
-            // 2qd+8, 2qd+9) so their latency hides behind K Q^T
+            // 2qd+8, 2qd+9) so their latency hides behind K Q^T; the four
+            // offsets follow from one lane constant (see swz128)
             uint4 va[4];
             if constexpr (kFP8) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tok = 2 * qd + (i & 1) + 8 * (i >> 1);
-                    va[i] = *reinterpret_cast<const uint4*>(vt + swz128(tok, g8));
-                }
+                const uint32_t v1 = (voff ^ 16u) + 128u;
+                va[0] = lds128(vts + voff);
+                va[1] = lds128(vts + v1);
+                va[2] = lds128(vts + voff + 1024u);
+                va[3] = lds128(vts + v1 + 1024u);
             }
             // ---- S = K Q^T, two accumulators (even / odd k-steps) to halve the chain
             float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -354,10 +380,10 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
             } else {
                 uint32_t w0[8], w1[8];
                 {
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(kt + swz128(g8, 2 * qd));
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(kt + swz128(g8, 2 * qd + 1));
-                    const uint4 c2 = *reinterpret_cast<const uint4*>(kt + swz128(g8 + 8, 2 * qd));
-                    const uint4 c3 = *reinterpret_cast<const uint4*>(kt + swz128(g8 + 8, 2 * qd + 1));
+                    const uint4 c0 = lds128(kts + koff);
+                    const uint4 c1 = lds128(kts + (koff ^ 16u));
+                    const uint4 c2 = lds128(kts + koff + 1024u);
+                    const uint4 c3 = lds128(kts + (koff ^ 16u) + 1024u);
                     w0[0] = c0.x; w0[1] = c0.y; w0[2] = c0.z; w0[3] = c0.w;
                     w0[4] = c1.x; w0[5] = c1.y; w0[6] = c1.z; w0[7] = c1.w;
                     w1[0] = c2.x; w1[1] = c2.y; w1[2] = c2.z; w1[3] = c2.w;
@@ -386,15 +412,23 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
                 bA = fmaxf(bA, __shfl_xor_sync(kFull, bA, mask));
                 bB = fmaxf(bB, __shfl_xor_sync(kFull, bB, mask));
             }
-            const float nA = fmaxf(mA, bA), nB = fmaxf(mB, bB);
-            const float alA = nA == mA ? 1.f : ex2(mA - nA);
-            const float alB = nB == mB ? 1.f : ex2(mB - nB);
+            // Lazy reference maximum: the probabilities are taken against a
+            // reference that moves only when a block's maximum exceeds it by
+            // more than 2^kRebaseLog2, so every p stays <= 2^kRebaseLog2 (exact
+            // range for f16 / bf16) and O is rescaled only on those rare
+            // moves, not whenever one of the group's heads sees a new maximum.
+            // The partials carry the reference, and the merges use it as the
+            // row's maximum; the result is the same softmax.
+            const bool rbA = bA > mA + kRebaseLog2, rbB = bB > mB + kRebaseLog2;
+            const float nA = rbA ? bA : mA, nB = rbB ? bB : mB;
+            const float alA = rbA ? ex2(mA - nA) : 1.f;  // 0 on the first block (mA = -inf)
+            const float alB = rbB ? ex2(mB - nB) : 1.f;
             mA = nA;
             mB = nB;
             const float p0 = ex2(sv[0] - nA), p1 = ex2(sv[1] - nB), p2 = ex2(sv[2] - nA), p3 = ex2(sv[3] - nB);
             lA = lA * alA + (p0 + p2);
             lB = lB * alB + (p1 + p3);
-            if (__any_sync(kFull, alA != 1.f || alB != 1.f)) {  // skip when no head's max moved
+            if (__any_sync(kFull, rbA || rbB)) {  // skip when no head's reference moved
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     o[i][0] *= alA;

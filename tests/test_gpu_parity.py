@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL, check_step, host_bits, max_error, p_rounding_allowance
+from parity_util import TOL, check_step, host_bits, max_error
 
 pytestmark = pytest.mark.gpu
 
@@ -395,11 +395,9 @@ def _scale_q(wl, factor):
 def test_sharp_softmax_matches_oracle(lib, kv, G, partition):
     """q scaled by 30: scores spread over ~150 log2 units, so the running
     maximum moves by large steps inside blocks, across warps and across
-    split-K partitions (merge weights underflow to 0).  Few keys dominate
-    each row, so the bound adds the rounding of the probabilities to the
-    tensor-core operand type (bf16 for bf16 pools, f16 for f16 and fp8
-    pools; the CUDA-core kernel at G = 1 keeps them in fp32)."""
-    import oracle
+    split-K partitions (merge weights underflow to 0), and few keys dominate
+    each row.  The tensor-core kernels carry the probabilities as a 16-bit
+    head plus a 16-bit tail, so the plain bound holds here too."""
     from paged_kv_cache_10_gb300 import workloads
     Hkv = 2
     wl = workloads.custom(f"sharp_{kv}", 111 + G, [1, 17, 200, 1500, 3000], Hkv * G, Hkv, 128, kv_dtype=kv,
@@ -408,10 +406,7 @@ def test_sharp_softmax_matches_oracle(lib, kv, G, partition):
     st = run(wl)
     assert lib.get_device_error() == 0
     err, mx = check_step(st)
-    vmax = max(float(np.max(np.abs(oracle.dequantize(wl.v_pool, kv)))) * (wl.v_scale if kv == "e4m3" else 1.0),
-               float(np.max(np.abs(oracle.dequantize(wl.v_new, wl.in_dtype)))))
-    extra = 0.0 if G == 1 else p_rounding_allowance("bf16" if kv == "bf16" else "f16", vmax)
-    assert err <= TOL[kv] + extra, (err, mx, extra)
+    assert err <= TOL[kv], (err, mx)
 
 
 @pytest.mark.parametrize("kv,G,partition", [("bf16", 1, 64), ("bf16", 4, 0), ("e4m3", 8, 256), ("f16", 2, 16)])

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from oracle.allocator_model import AllocatorModel
-from parity_util import TOL, host_bits, max_error, p_rounding_allowance
+from parity_util import TOL, host_bits, max_error
 
 pytestmark = pytest.mark.gpu
 
@@ -274,8 +274,8 @@ def test_prefill_rejects_bad_arguments(lib):
 def test_prefill_sharp_softmax(lib, dtype, G):
     """q scaled by 30: the row maximum jumps by far more than the lazy
     rebase threshold (2^8) between key tiles, in prompts and in chunks over
-    earlier context.  Few keys dominate each row, so the bound adds the
-    rounding of the probabilities to the operand type of P V."""
+    earlier context, and few keys dominate each row; with the probabilities
+    carried as a 16-bit head plus tail the plain bound holds."""
     import oracle as orc
     from paged_kv_cache_10_gb300 import workloads
     Hkv = 2
@@ -286,9 +286,7 @@ def test_prefill_sharp_softmax(lib, dtype, G):
     st = run(wl)
     assert lib.get_device_error() == 0
     err, mx = check_full(st)
-    vmax = float(np.max(np.abs(orc.dequantize(np.concatenate([wl.v_pool.ravel(), wl.v_new.ravel()]), dtype))))
-    extra = p_rounding_allowance(dtype, vmax)
-    assert err <= TOL[dtype] + extra, (err, mx, extra)
+    assert err <= TOL[dtype], (err, mx)
 
 
 def test_prefill_persistent_grid_counters_graphs_and_streams(lib):
