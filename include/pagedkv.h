@@ -319,11 +319,17 @@ pkv_status pkv_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t nu
  *     rows of each group;
  *   max_group_members, max_group_blocks: host bounds of the two (size the
  *     launch).
- * workspace must hold pkv_decode_cascade_workspace_bytes(...) bytes.
+ * workspace must hold pkv_decode_cascade_workspace_bytes(...) bytes, plus,
+ * for an fp8 pool, pkv_decode_cascade_staging_bytes(...) more: there the
+ * prefix pass first copies every group's shared blocks once into q's 16-bit
+ * type (exact: every E4M3 value is an f16 and a bf16 value) in the
+ * workspace, after the partials at the next 256-byte boundary, and reads
+ * that copy, with k_scale in the score scale and v_scale on the output.
  * scale must be finite and > 0 (else PKV_ERR_INVALID).
- * Implemented for f16 / bf16 pools (q of the same type), head_size 128,
- * num_q_heads / num_kv_heads in {1, 2, 4, 8}; fp8 pools return
- * PKV_ERR_UNSUPPORTED.  A member index or block count out of range sets
+ * Implemented for f16 / bf16 pools (q of the same type) and fp8 E4M3 pools
+ * (q f16 or bf16; k_scale, v_scale > 0), head_size 64 or 128, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8}.  The own tokens use the kernels plain decode
+ * uses.  A member index or block count out of range sets
  * PKV_DEVERR_SEQ_LEN and the offending rows are skipped.
  * Streams: the prefix pass runs on a stream the library owns (one per
  * device, created by the first call on it), forked from `stream` by an event
@@ -347,6 +353,14 @@ pkv_status pkv_paged_attention_decode_cascade(const void* q, int32_t q_dtype, in
 size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_size,
                                           int32_t max_seq_len, int32_t partition_tokens,
                                           int32_t max_group_blocks);
+
+/* Extra workspace bytes of pkv_paged_attention_decode_cascade over an fp8
+ * pool (the groups' 16-bit prefix copy and its block table): 0 for f16 / bf16
+ * pools, for no groups, or on invalid sizes.  The whole workspace is then
+ * round_up(pkv_decode_cascade_workspace_bytes(...), 256) + this. */
+size_t pkv_decode_cascade_staging_bytes(int32_t kv_dtype, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                        int32_t num_groups, int32_t max_group_blocks, int32_t num_kv_heads,
+                                        int32_t head_size);
 
 /*
  * Paged (chunked) prefill attention, causal, on the tensor cores.  Prefill

@@ -74,6 +74,17 @@ extern "C" size_t pkv_decode_cascade_workspace_bytes(int32_t num_seqs, int32_t n
     return partials_bytes(num_seqs, num_q_heads, head_size, NP);
 }
 
+extern "C" size_t pkv_decode_cascade_staging_bytes(int32_t kv_dtype, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                                   int32_t num_groups, int32_t max_group_blocks, int32_t num_kv_heads,
+                                                   int32_t head_size) {
+    if (kv_dtype != PKV_FP8_E4M3 || num_seqs <= 0 || max_blocks_per_seq <= 0 || num_groups <= 0 ||
+        max_group_blocks <= 0 || num_kv_heads <= 0 || head_size <= 0)
+        return 0;
+    return static_cast<size_t>(
+        cascade_stage_layout(num_seqs, max_blocks_per_seq, num_groups, max_group_blocks, num_kv_heads, head_size)
+            .bytes);
+}
+
 extern "C" pkv_status pkv_paged_attention_decode_cascade(
     const void* q, int32_t q_dtype, int32_t num_seqs, int32_t num_q_heads, const void* k_cache, const void* v_cache,
     const pkv_cache_desc* d, const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -92,8 +103,10 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * d->block_size)
         return PKV_ERR_INVALID;
     if (max_group_blocks > max_blocks_per_seq || partition_tokens % kBlockSize) return PKV_ERR_INVALID;
-    if (d->kv_dtype == PKV_FP8_E4M3 || q_dtype != d->kv_dtype) return PKV_ERR_UNSUPPORTED;
-    if (d->block_size != kBlockSize || d->head_size != 128) return PKV_ERR_UNSUPPORTED;
+    const bool fp8 = d->kv_dtype == PKV_FP8_E4M3;
+    if (!fp8 && q_dtype != d->kv_dtype) return PKV_ERR_UNSUPPORTED;
+    if (d->block_size != kBlockSize || (d->head_size != 64 && d->head_size != 128)) return PKV_ERR_UNSUPPORTED;
+    if (fp8 && !(d->k_scale > 0.f && d->v_scale > 0.f)) return PKV_ERR_INVALID;
     const int G = num_q_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || d->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
@@ -110,7 +123,17 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     const int64_t NP = npp + nps;
     const int64_t row_chunks = cdiv(static_cast<int64_t>(max_group_members) * G, 128);  // one 128-row Q tile per CTA
     if (NP > 0x7fffffff || static_cast<int64_t>(num_groups) * row_chunks > 65535) return PKV_ERR_UNSUPPORTED;
-    const size_t need = partials_bytes(num_seqs, num_q_heads, d->head_size, NP);
+    const size_t part_bytes = partials_bytes(num_seqs, num_q_heads, d->head_size, NP);
+    // an fp8 pool's staged 16-bit prefix copy follows the partials
+    const size_t stage_off = (part_bytes + 255) / 256 * 256;
+    const int64_t stage_rows = static_cast<int64_t>(num_groups) * max_group_blocks * d->num_kv_heads * kBlockSize;
+    const bool staged = fp8 && num_groups > 0 && max_group_blocks > 0 && row_chunks > 0;
+    if (staged && stage_rows > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
+    const size_t need =
+        staged ? stage_off + static_cast<size_t>(cascade_stage_layout(num_seqs, max_blocks_per_seq, num_groups,
+                                                                      max_group_blocks, d->num_kv_heads, d->head_size)
+                                                     .bytes)
+               : part_bytes;
     if (!workspace || ws_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
     unsigned int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
@@ -130,8 +153,9 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     p.MB = max_blocks_per_seq;
     p.P = P;
     p.NP = static_cast<int32_t>(NP);
-    p.qk_scale = scale * 1.4426950408889634f;
-    p.v_scale = 1.f;
+    const float log2e = 1.4426950408889634f;
+    p.qk_scale = scale * log2e * (fp8 ? d->k_scale : 1.f);
+    p.v_scale = fp8 ? d->v_scale : 1.f;
     p.err = err;
     p.seq_group = seq_group;
     p.group_blocks = group_blocks;
@@ -139,9 +163,14 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     p.cascade = 1;
     partials_layout(p, workspace);
 
-    CUtensorMap tk, tv, tq;
-    if (!encode_pool_map(&tk, k_cache, 2, pool_rows, d->head_size) ||
-        !encode_pool_map(&tv, v_cache, 2, pool_rows, d->head_size) ||
+    // The own-token decode: the kernels plain decode would use (tensor cores
+    // for grouped heads at head_size 128, CUDA cores otherwise), on the pool
+    // itself.
+    const bool use_mma = d->head_size == 128 && G >= 2;
+    const int eb = fp8 ? 1 : 2;
+    CUtensorMap tk, tv, tq, tpk, tpv;
+    if ((use_mma && (!encode_pool_map(&tk, k_cache, eb, pool_rows, d->head_size) ||
+                     !encode_pool_map(&tv, v_cache, eb, pool_rows, d->head_size))) ||
         !encode_token_head_map(&tq, q, d->head_size, num_q_heads, num_seqs, G, 1))
         return PKV_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -151,12 +180,34 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     SideStream* ss = nullptr;
     // 1. shared prefixes, on the side stream, after everything before this call
     if (prefix) {
+        CascadeParams cp{p, group_offsets, group_members, G, static_cast<int32_t>(row_chunks), npp,
+                         block_tables, d->num_blocks, p.qk_scale, 1.f};
+        void* staging = static_cast<unsigned char*>(workspace) + stage_off;
+        if (staged) {
+            // the prefix pass reads a 16-bit copy (q's type) of the groups' blocks
+            const CascadeStage lay = cascade_stage_layout(num_seqs, max_blocks_per_seq, num_groups, max_group_blocks,
+                                                          d->num_kv_heads, d->head_size);
+            unsigned char* sw = static_cast<unsigned char*>(staging);
+            cp.prefix_tables = reinterpret_cast<const int32_t*>(sw + lay.table_off);
+            cp.prefix_nb = num_groups * max_group_blocks;
+            cp.prefix_o_scale = d->v_scale;
+            if (!encode_pool_map(&tpk, sw + lay.k_off, 2, stage_rows, d->head_size) ||
+                !encode_pool_map(&tpv, sw + lay.v_off, 2, stage_rows, d->head_size))
+                return PKV_ERR_CUDA;
+        } else if (!use_mma) {
+            if (!encode_pool_map(&tpk, k_cache, 2, pool_rows, d->head_size) ||
+                !encode_pool_map(&tpv, v_cache, 2, pool_rows, d->head_size))
+                return PKV_ERR_CUDA;
+        }
+        const CUtensorMap& pk = (staged || !use_mma) ? tpk : tk;
+        const CUtensorMap& pv = (staged || !use_mma) ? tpv : tv;
         lock.lock();
         if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
         if (cudaEventRecord(ss->fork, st) != cudaSuccess || cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
             return PKV_ERR_CUDA;
-        CascadeParams cp{p, group_offsets, group_members, G, static_cast<int32_t>(row_chunks), npp};
-        e = launch_cascade_prefix_tc(cp, num_groups, d->kv_dtype, tq, tk, tv, ss->stream);
+        if (staged) e = launch_cascade_stage_fp8(cp, num_groups, max_group_blocks, q_dtype, k_cache, v_cache, staging,
+                                                 ss->stream);
+        if (e == cudaSuccess) e = launch_cascade_prefix_tc(cp, num_groups, q_dtype, d->head_size, tq, pk, pv, ss->stream);
         if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->stream);
         if (e != cudaSuccess) {
             (void)cudaStreamWaitEvent(st, ss->join, 0);  // keep the caller's stream behind what was enqueued
@@ -164,10 +215,23 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
         }
     }
     // 2. each sequence's own tokens, meanwhile on the caller's stream
-    if (G >= 2) {
-        e = d->kv_dtype == PKV_BF16 ? launch_decode_mma_bf16(p, G, tk, tv, st) : launch_decode_mma_f16(p, G, tk, tv, st);
+    if (use_mma) {
+        if (d->kv_dtype == PKV_BF16)
+            e = launch_decode_mma_bf16(p, G, tk, tv, st);
+        else if (d->kv_dtype == PKV_F16)
+            e = launch_decode_mma_f16(p, G, tk, tv, st);
+        else if (q_dtype == PKV_BF16)
+            e = launch_decode_mma_fp8_bf16q(p, G, tk, tv, st);
+        else
+            e = launch_decode_mma_fp8_f16q(p, G, tk, tv, st);
+    } else if (d->kv_dtype == PKV_BF16) {
+        e = launch_decode_bf16(p, G, st);
+    } else if (d->kv_dtype == PKV_F16) {
+        e = launch_decode_f16(p, G, st);
+    } else if (q_dtype == PKV_BF16) {
+        e = launch_decode_fp8_bf16q(p, G, st);
     } else {
-        e = d->kv_dtype == PKV_BF16 ? launch_decode_bf16(p, G, st) : launch_decode_f16(p, G, st);
+        e = launch_decode_fp8_f16q(p, G, st);
     }
     // join before the merge reads the prefix partials
     if (prefix && cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess) return PKV_ERR_CUDA;

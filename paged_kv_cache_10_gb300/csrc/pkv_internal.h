@@ -111,10 +111,29 @@ struct CascadeParams {
     int32_t G;
     int32_t row_chunks;  // CTAs per (group, KV head, prefix partition) along rows (128 rows each)
     int32_t npp;         // prefix partitions (partition indices [0, npp))
+    // The 16-bit pool the prefix pass reads (the caller's pool, or the
+    // staged copy of an fp8 pool): its block table (rows of the groups'
+    // first members), block count and scales.
+    const int32_t* prefix_tables;
+    int32_t prefix_nb;
+    float prefix_qk_scale;  // scale * log2(e) (* k_scale for a staged copy)
+    float prefix_o_scale;   // 1, or v_scale for a staged copy
 };
-// tq: q as [S][Hq][128] with a box of 64 x G x 1 (encode_token_head_map).
-cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int kv_dtype, const CUtensorMap& tq,
+// tq: q as [S][Hq][D] with a box of 64 x G x 1 (encode_token_head_map); tk,
+// tv: the 16-bit pool the prefix pass reads, in q's type.
+cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int q_dtype, int D, const CUtensorMap& tq,
                                      const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st);
+
+// Cascade decode over an fp8 E4M3 pool: the tcgen05 prefix pass reads a
+// 16-bit copy (q's type) of every group's shared blocks, made first by
+// launch_cascade_stage_fp8: copy block g * MGB + j holds block j of group g's
+// prefix, and the first member's row of the copy's [S][MB] table names it.
+struct CascadeStage {
+    int64_t table_off, k_off, v_off, bytes;  // from the start of the staging area
+};
+CascadeStage cascade_stage_layout(int64_t S, int64_t MB, int64_t num_groups, int64_t MGB, int64_t Hkv, int64_t D);
+cudaError_t launch_cascade_stage_fp8(const CascadeParams& cp, int num_groups, int MGB, int q_dtype,
+                                     const void* k_cache, const void* v_cache, void* staging, cudaStream_t st);
 
 // Log-sum-exp merge of split-K partials into out (q dtype).
 cudaError_t launch_merge(const DecodeParams& p, int q_dtype, cudaStream_t st);

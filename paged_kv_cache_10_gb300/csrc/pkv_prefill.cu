@@ -1055,26 +1055,46 @@ StageLayout stage_layout(int64_t S, int64_t MB, int64_t Hkv, int64_t D) {
 // its copy zeroed (the attention pass then reads zeros, not stale bytes).
 constexpr int kStageUnroll = 8;
 
-template <typename T>
+// kGroups = false (prefill): CTA (j, s, z) copies sequence s's logical block
+// j into copy block s * MB + j, for the blocks its seq_lens[s] reaches.
+// kGroups = true (cascade decode): CTA (j, g, z) copies block j of group g's
+// shared prefix (group_blocks[g] blocks, read through the block table of
+// the group's first member) into copy block g * MGB + j, and that member's
+// row of the copy's table names it; the prefix pass reads only those rows.
+template <typename T, bool kGroups>
 __global__ void __launch_bounds__(256) stage_fp8_kernel(const uint8_t* __restrict__ k_cache,
                                                         const uint8_t* __restrict__ v_cache,
                                                         const int32_t* __restrict__ block_tables,
                                                         const int32_t* __restrict__ seq_lens, int MB, int NB,
                                                         int block_vecs, uint4* __restrict__ k_copy,
                                                         uint4* __restrict__ v_copy, int32_t* __restrict__ table_copy,
-                                                        unsigned int* err) {
+                                                        unsigned int* err, const int32_t* __restrict__ group_blocks,
+                                                        const int32_t* __restrict__ group_offsets,
+                                                        const int32_t* __restrict__ group_members, int S, int MGB) {
     constexpr bool kBF = std::is_same<T, BF16>::value;
     // the attention kernel may start its setup once every CTA here has begun
     allow_dependent_launch();
-    const int j = blockIdx.x, s = blockIdx.y, z = blockIdx.z;
-    const int L = __ldg(seq_lens + s);  // the attention pass reports a bad length
-    const int nblk = L <= 0 ? 0 : min((L + kBlockSize - 1) / kBlockSize, MB);
-    if (j >= nblk) return;
-    const int64_t dst = static_cast<int64_t>(s) * MB + j;
-    const int id = __ldg(block_tables + dst);
+    const int j = blockIdx.x, z = blockIdx.z;
+    int64_t row, dst;  // table entry read (and written in the copy), copy block
+    if constexpr (kGroups) {
+        const int g = blockIdx.y;
+        const int nb = min(max(__ldg(group_blocks + g), 0), MB);  // the prefix pass reports a bad count
+        const int s0 = __ldg(group_members + __ldg(group_offsets + g));
+        if (j >= nb || s0 < 0 || s0 >= S) return;  // ... and a bad member
+        row = static_cast<int64_t>(s0) * MB + j;
+        dst = static_cast<int64_t>(g) * MGB + j;
+    } else {
+        const int s = blockIdx.y;
+        const int L = __ldg(seq_lens + s);  // the attention pass reports a bad length
+        const int nblk = L <= 0 ? 0 : min((L + kBlockSize - 1) / kBlockSize, MB);
+        if (j >= nblk) return;
+        row = static_cast<int64_t>(s) * MB + j;
+        dst = row;
+    }
+    const int id = __ldg(block_tables + row);
     const bool bad = id < 0 || id >= NB;
     if (threadIdx.x == 0 && z == 0) {
-        table_copy[dst] = static_cast<int32_t>(dst);
+        table_copy[row] = static_cast<int32_t>(dst);
         if (bad) report(err, PKV_DEVERR_BLOCK_ID);
     }
     // block_vecs: 16-byte output vectors per block and pool (Hkv * 16 * D / 8)
@@ -1111,19 +1131,20 @@ __global__ void __launch_bounds__(256) stage_fp8_kernel(const uint8_t* __restric
 
 int prefix_partitions(int blocks) { return (blocks + kPrefixPartitionBlocks - 1) / kPrefixPartitionBlocks; }
 
-cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int kv_dtype, const CUtensorMap& tq,
+cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, int q_dtype, int D, const CUtensorMap& tq,
                                      const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
     const DecodeParams& b = cp.base;
     PrefillParams p{};
-    p.block_tables = b.block_tables;
+    p.block_tables = cp.prefix_tables;
     p.S = b.S;
     p.Hq = b.Hq;
     p.Hkv = b.Hkv;
     p.MB = b.MB;
-    p.NB = b.NB;
+    p.NB = cp.prefix_nb;
     p.G = cp.G;
     p.TT = kTileM / cp.G;
-    p.qk_scale = b.qk_scale;
+    p.qk_scale = cp.prefix_qk_scale;
+    p.o_scale = cp.prefix_o_scale;
     p.err = b.err;
     p.group_offsets = cp.group_offsets;
     p.group_members = cp.group_members;
@@ -1134,8 +1155,46 @@ cudaError_t launch_cascade_prefix_tc(const CascadeParams& cp, int num_groups, in
     p.NP = b.NP;
     p.row_chunks = cp.row_chunks;
     const dim3 grid(cp.npp, b.Hkv, num_groups * cp.row_chunks);
-    return kv_dtype == PKV_BF16 ? launch_tile<BF16, 128, true>(p, grid, tq, tk, tv, st)
-                                : launch_tile<F16, 128, true>(p, grid, tq, tk, tv, st);
+    if (q_dtype == PKV_BF16)
+        return D == 64 ? launch_tile<BF16, 64, true>(p, grid, tq, tk, tv, st)
+                       : launch_tile<BF16, 128, true>(p, grid, tq, tk, tv, st);
+    return D == 64 ? launch_tile<F16, 64, true>(p, grid, tq, tk, tv, st)
+                   : launch_tile<F16, 128, true>(p, grid, tq, tk, tv, st);
+}
+
+CascadeStage cascade_stage_layout(int64_t S, int64_t MB, int64_t num_groups, int64_t MGB, int64_t Hkv, int64_t D) {
+    const auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+    const int64_t copy = num_groups * MGB * Hkv * kBlockSize * D * 2;
+    CascadeStage l{};
+    l.table_off = 0;
+    l.k_off = up(S * MB * 4);
+    l.v_off = l.k_off + up(copy);
+    l.bytes = l.v_off + up(copy);
+    return l;
+}
+
+cudaError_t launch_cascade_stage_fp8(const CascadeParams& cp, int num_groups, int MGB, int q_dtype,
+                                     const void* k_cache, const void* v_cache, void* staging, cudaStream_t st) {
+    const DecodeParams& b = cp.base;
+    if (num_groups == 0 || MGB == 0) return cudaSuccess;
+    const CascadeStage lay = cascade_stage_layout(b.S, b.MB, num_groups, MGB, b.Hkv, b.D);
+    unsigned char* ws = static_cast<unsigned char*>(staging);
+    int32_t* table_copy = reinterpret_cast<int32_t*>(ws + lay.table_off);
+    uint4* k_copy = reinterpret_cast<uint4*>(ws + lay.k_off);
+    uint4* v_copy = reinterpret_cast<uint4*>(ws + lay.v_off);
+    const int block_vecs = b.Hkv * kBlockSize * b.D / 8;
+    const dim3 grid(static_cast<unsigned>(MGB), static_cast<unsigned>(num_groups), 2);
+    const auto* kc = static_cast<const uint8_t*>(k_cache);
+    const auto* vc = static_cast<const uint8_t*>(v_cache);
+    if (q_dtype == PKV_BF16)
+        stage_fp8_kernel<BF16, true><<<grid, 256, 0, st>>>(kc, vc, b.block_tables, b.seq_lens, b.MB, b.NB, block_vecs,
+                                                           k_copy, v_copy, table_copy, b.err, b.group_blocks,
+                                                           cp.group_offsets, cp.group_members, b.S, MGB);
+    else
+        stage_fp8_kernel<F16, true><<<grid, 256, 0, st>>>(kc, vc, b.block_tables, b.seq_lens, b.MB, b.NB, block_vecs,
+                                                          k_copy, v_copy, table_copy, b.err, b.group_blocks,
+                                                          cp.group_offsets, cp.group_members, b.S, MGB);
+    return cudaGetLastError();
 }
 
 }  // namespace pkv
@@ -1195,11 +1254,13 @@ extern "C" pkv_status pkv_paged_attention_prefill(const void* q, int32_t q_dtype
         const auto* kc = static_cast<const uint8_t*>(k_cache);
         const auto* vc = static_cast<const uint8_t*>(v_cache);
         if (q_dtype == PKV_BF16)
-            stage_fp8_kernel<BF16><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
-                                                         desc->num_blocks, block_vecs, k_copy, v_copy, table_copy, err);
+            stage_fp8_kernel<BF16, false><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
+                                                                desc->num_blocks, block_vecs, k_copy, v_copy,
+                                                                table_copy, err, nullptr, nullptr, nullptr, 0, 0);
         else
-            stage_fp8_kernel<F16><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
-                                                        desc->num_blocks, block_vecs, k_copy, v_copy, table_copy, err);
+            stage_fp8_kernel<F16, false><<<grid, 256, 0, st>>>(kc, vc, block_tables, seq_lens, max_blocks_per_seq,
+                                                               desc->num_blocks, block_vecs, k_copy, v_copy,
+                                                               table_copy, err, nullptr, nullptr, nullptr, 0, 0);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
         block_tables = table_copy;
         k_pool = k_copy;

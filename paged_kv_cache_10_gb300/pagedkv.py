@@ -37,6 +37,7 @@ EXPORTED = [
     "pkv_alloc_lookup", "pkv_alloc_seq_new_prefix", "pkv_alloc_commit", "pkv_alloc_num_cached",
     "pkv_alloc_block_hash_of", "pkv_alloc_reset_prefix_cache", "pkv_paged_attention_decode_append",
     "pkv_prefill_plan", "pkv_decode_plan", "pkv_prefill_workspace_bytes", "pkv_check_wait_timeout",
+    "pkv_decode_cascade_staging_bytes",
 ]
 
 
@@ -117,6 +118,7 @@ def lib():
         "pkv_paged_attention_decode_cascade": (i32, [P, i32, i32, i32, P, P, D, P, i32, P, i32, P, P, P, P, i32, i32,
                                                      i32, ctypes.c_float, P, P, ctypes.c_size_t, i32, P]),
         "pkv_decode_cascade_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32, i32]),
+        "pkv_decode_cascade_staging_bytes": (ctypes.c_size_t, [i32, i32, i32, i32, i32, i32, i32]),
         "pkv_alloc_prefix_groups": (i32, [P, P, i32, i32, P, P, P, P, P, P, P]),
         "pkv_swap_blocks": (i32, [P, P, D, P, P, i32, P, i32, i32, P]),
         "pkv_alloc_swap_out": (i32, [P, P, i64, P, i32, P]),
@@ -292,6 +294,24 @@ def decode_cascade_workspace_bytes(num_seqs: int, num_q_heads: int, head_size: i
                                    partition_tokens: int, max_group_blocks: int) -> int:
     return int(lib().pkv_decode_cascade_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len,
                                                         partition_tokens, max_group_blocks))
+
+
+def decode_cascade_staging_bytes(kv_dtype: str, num_seqs: int, max_blocks_per_seq: int, num_groups: int,
+                                 max_group_blocks: int, num_kv_heads: int, head_size: int) -> int:
+    return int(lib().pkv_decode_cascade_staging_bytes(DTYPE_CODE[kv_dtype], num_seqs, max_blocks_per_seq, num_groups,
+                                                      max_group_blocks, num_kv_heads, head_size))
+
+
+def decode_cascade_total_workspace_bytes(kv_dtype: str, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                         head_size: int, max_seq_len: int, max_blocks_per_seq: int,
+                                         partition_tokens: int, num_groups: int, max_group_blocks: int) -> int:
+    """Whole workspace of a cascade decode call: the partials, then (fp8 pools)
+    the groups' 16-bit prefix copy at the next 256-byte boundary."""
+    part = decode_cascade_workspace_bytes(num_seqs, num_q_heads, head_size, max_seq_len, partition_tokens,
+                                          max_group_blocks)
+    stage = decode_cascade_staging_bytes(kv_dtype, num_seqs, max_blocks_per_seq, num_groups, max_group_blocks,
+                                         num_kv_heads, head_size)
+    return (-(-part // 256) * 256 + stage) if stage else part
 
 
 @dataclass

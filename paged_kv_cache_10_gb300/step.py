@@ -81,8 +81,9 @@ class DecodeStep:
             self.d_group_blocks = torch.from_numpy(g.group_blocks).to(dev)
             self.d_group_offsets = torch.from_numpy(g.group_offsets).to(dev)
             self.d_group_members = torch.from_numpy(g.group_members).to(dev)
-            ws = pk.decode_cascade_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens,
-                                                   g.max_blocks)
+            ws = pk.decode_cascade_total_workspace_bytes(wl.kv_dtype, wl.S, wl.Hq, wl.Hkv, wl.D, self.max_seq_len,
+                                                         self.max_blocks, self.partition_tokens, g.num_groups,
+                                                         g.max_blocks)
         else:
             ws = pk.decode_workspace_bytes(wl.S, wl.Hq, wl.D, self.max_seq_len, self.partition_tokens)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev) if ws else None
@@ -129,7 +130,8 @@ class DecodeStep:
         if len(self.pairs) and not self.fused:
             n += 1
         if self.cascade:
-            n += 1 + (1 if self.groups.num_groups else 0)  # merge, prefix
+            # merge, prefix pass (and the 16-bit staging of an fp8 pool's prefixes)
+            n += 1 + ((2 if self.wl.kv_dtype == "e4m3" else 1) if self.groups.num_groups else 0)
             return n
         P = self.effective_partition()
         if self.max_seq_len > P:

@@ -204,14 +204,16 @@ def longctx_fp8(seed=1004) -> Workload:
                  partition_tokens=512)
 
 
-def prefix_share(seed=1005, pairs=64, prefix=2048, literal=False) -> Workload:
+def prefix_share(seed=1005, pairs=64, prefix=2048, literal=False, kv_dtype="bf16") -> Workload:
     """Parallel sampling over one shared prefix.
 
     Default: ``pairs`` pairs (2j, 2j+1); both members share the prefix and a
     pair suffix of U[0,512] tokens, so the first member's append hits a shared
     partial block (copy-on-write) unless the suffix is a whole number of
     blocks.  ``literal=True``: 2*pairs sequences with independent suffixes
-    (no block but the prefix is shared, so no copy-on-write)."""
+    (no block but the prefix is shared, so no copy-on-write).  kv_dtype:
+    the pool's element type (queries stay bf16; an fp8 pool takes per-tensor
+    scales from its values)."""
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(7)[6]))
     S = 2 * pairs
     T = 1 << 30  # template sequence id, freed before the step
@@ -231,8 +233,8 @@ def prefix_share(seed=1005, pairs=64, prefix=2048, literal=False) -> Workload:
         nblk = _blocks(prefix) + sum(_blocks(x) + 2 for x in suf)
     setup.append(("free", T))
     NB = nblk + math.ceil(0.10 * nblk)
-    name = "prefix_share_literal" if literal else "prefix_share"
-    return build(name, seed, S, 32, 8, 128, NB, "bf16", "bf16", setup, list(range(S)), lens)
+    name = ("prefix_share_literal" if literal else "prefix_share") + ("" if kv_dtype == "bf16" else "_" + kv_dtype)
+    return build(name, seed, S, 32, 8, 128, NB, "bf16", kv_dtype, setup, list(range(S)), lens)
 
 
 def custom(name, seed, lens, Hq, Hkv, D, kv_dtype="bf16", q_dtype=None, NB=None,
@@ -252,7 +254,8 @@ def custom(name, seed, lens, Hq, Hkv, D, kv_dtype="bf16", q_dtype=None, NB=None,
                  partition_tokens=partition_tokens)
 
 
-def fork_groups(name, seed, groups, singles, Hq, Hkv, D=128, kv_dtype="bf16", partition_tokens=0) -> Workload:
+def fork_groups(name, seed, groups, singles, Hq, Hkv, D=128, kv_dtype="bf16", partition_tokens=0,
+                q_dtype=None) -> Workload:
     """Fork trees: for each (prefix_tokens, members) in ``groups`` a template
     sequence of prefix_tokens (a multiple of 16) is forked into ``members``
     sequences, each extended by its own U[0, 300] tokens; ``singles``
@@ -280,7 +283,8 @@ def fork_groups(name, seed, groups, singles, Hq, Hkv, D=128, kv_dtype="bf16", pa
         need += _blocks(L) + 1
         s += 1
     NB = need + math.ceil(0.25 * need)
-    return build(name, seed, s, Hq, Hkv, D, NB, kv_dtype, kv_dtype, setup, list(range(s)), lens,
+    q_dtype = q_dtype or ("bf16" if kv_dtype == "e4m3" else kv_dtype)
+    return build(name, seed, s, Hq, Hkv, D, NB, q_dtype, kv_dtype, setup, list(range(s)), lens,
                  partition_tokens=partition_tokens)
 
 

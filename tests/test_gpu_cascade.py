@@ -75,12 +75,80 @@ def test_cascade_without_groups_is_plain_decode(lib):
     assert np.all(host_bits(st.out)[3] == 0)
 
 
-def test_cascade_rejects_fp8(lib):
+@pytest.mark.parametrize("qd", ["bf16", "f16"])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_cascade_fp8_fork_trees_match_oracle(lib, qd, G):
+    """fp8 E4M3 pools: the prefix pass reads a 16-bit copy of every group's
+    shared blocks (made by the call), the own tokens use the fp8 decode
+    kernels; judged against the oracle on the dequantised codes."""
     from paged_kv_cache_10_gb300 import workloads
-    wl = workloads.custom("fp8c", 73, [40, 50], 16, 2, 128, kv_dtype="e4m3")
+    Hkv = 2
+    wl = workloads.fork_groups("forks_fp8", 160 + G, [(32, 3), (320, 5), (528, 4), (96, 1)], 3, Hkv * G, Hkv,
+                               kv_dtype="e4m3", q_dtype=qd)
+    assert wl.k_scale != wl.v_scale
+    st = run(wl, cascade=True, cascade_min_blocks=1)
+    assert lib.get_device_error() == 0
+    assert st.groups.num_groups >= 3 and st.kernel_launches() == 5  # append, staging, prefix, decode, merge
+    err, mx = check_step(st)
+    assert err <= TOL["e4m3"], (err, mx)
+
+
+@pytest.mark.parametrize("kv,qd", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "bf16")])
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_cascade_head_size_64_matches_oracle(lib, kv, qd, G):
+    from paged_kv_cache_10_gb300 import workloads
+    Hkv = 2
+    wl = workloads.fork_groups("forks_d64", 260 + G, [(64, 4), (400, 6), (1040, 3)], 2, Hkv * G, Hkv, D=64,
+                               kv_dtype=kv, q_dtype=qd)
+    st = run(wl, cascade=True, cascade_min_blocks=1)
+    assert lib.get_device_error() == 0
+    assert st.groups.num_groups >= 3
+    err, mx = check_step(st)
+    assert err <= TOL[kv], (err, mx)
+
+
+def test_cascade_fp8_prefix_share_full_size(lib):
+    """prefix_share over an fp8 pool at full size: 128 rows, one group of a
+    2048-token prefix read once per KV head through the staged copy; every
+    row against the oracle and equal, within the bound, to plain decode."""
+    import oracle
+    from paged_kv_cache_10_gb300 import workloads
+    wl = workloads.prefix_share(kv_dtype="e4m3")
+    st = run(wl, cascade=True)
+    assert lib.get_device_error() == 0
+    assert st.groups.num_groups == 1 and st.groups.max_blocks == 128
+    err, mx = check_step(st)
+    assert err <= TOL["e4m3"], (err, mx)
+    plain = run(wl)
+    fa = oracle.dequantize(host_bits(st.out), "bf16")
+    fb = oracle.dequantize(host_bits(plain.out), "bf16")
+    assert np.max(np.abs(fa - fb)) <= TOL["e4m3"]
+
+
+def test_cascade_fp8_workspace_must_hold_the_staging(lib):
+    """The staged prefix copy follows the partials in the workspace; a
+    workspace of the partials alone is refused before any launch."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.fork_groups("fp8_ws", 171, [(320, 4)], 1, 16, 2, kv_dtype="e4m3")
+    st = DecodeStep(wl, device="cuda", cascade=True, cascade_min_blocks=1)
+    g = st.groups
+    part = lib.decode_cascade_workspace_bytes(wl.S, wl.Hq, wl.D, st.max_seq_len, st.partition_tokens, g.max_blocks)
+    stage = lib.decode_cascade_staging_bytes("e4m3", wl.S, st.max_blocks, g.num_groups, g.max_blocks, wl.Hkv, wl.D)
+    assert stage > 0 and lib.decode_cascade_staging_bytes("bf16", wl.S, st.max_blocks, g.num_groups, g.max_blocks,
+                                                          wl.Hkv, wl.D) == 0
+    short = torch.empty(part, dtype=torch.uint8, device="cuda")
     with pytest.raises(lib.PagedKVError) as e:
-        run(wl, cascade=True)
-    assert e.value.status == lib.ERR_UNSUPPORTED
+        lib.paged_attention_decode_cascade(st.q, st.k_cache, st.v_cache, st.desc, st.d_tables, st.d_lens,
+                                           st.max_seq_len, wl.scale, st.out, st.d_seq_group, st.d_group_blocks,
+                                           st.d_group_offsets, st.d_group_members, g.max_members, g.max_blocks,
+                                           short, partition_tokens=st.partition_tokens, q_dtype="bf16")
+    assert e.value.status == lib.ERR_WORKSPACE
+    st.run()
+    torch.cuda.synchronize()
+    assert lib.get_device_error() == 0
+    err, mx = check_step(st)
+    assert err <= TOL["e4m3"], (err, mx)
 
 
 def test_cascade_graph_replay_and_stream_order(lib):
