@@ -123,6 +123,14 @@ namespace {
 std::atomic<int> g_decode_path{0};  // 0 auto, 1 CUDA cores, 2 tensor cores
 }  // namespace
 
+cudaError_t launch_decode_gqa(const DecodeParams& p, int G, int kv_dtype, int q_dtype, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t st) {
+    if (kv_dtype == PKV_F16) return launch_decode_mma_f16(p, G, tk, tv, st);
+    if (kv_dtype == PKV_BF16) return launch_decode_mma_bf16(p, G, tk, tv, st);
+    return q_dtype == PKV_BF16 ? launch_decode_mma_fp8_bf16q(p, G, tk, tv, st)
+                               : launch_decode_mma_fp8_f16q(p, G, tk, tv, st);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -355,14 +363,7 @@ pkv_status decode_common(const void* q, int32_t q_dtype, int32_t num_seqs, int32
         if (!encode_pool_map(&tk, k_cache, eb, pool_rows, d->head_size) ||
             !encode_pool_map(&tv, v_cache, eb, pool_rows, d->head_size))
             return PKV_ERR_CUDA;
-        if (d->kv_dtype == PKV_F16)
-            e = launch_decode_mma_f16(p, G, tk, tv, st);
-        else if (d->kv_dtype == PKV_BF16)
-            e = launch_decode_mma_bf16(p, G, tk, tv, st);
-        else if (q_dtype == PKV_BF16)
-            e = launch_decode_mma_fp8_bf16q(p, G, tk, tv, st);
-        else
-            e = launch_decode_mma_fp8_f16q(p, G, tk, tv, st);
+        e = launch_decode_gqa(p, G, d->kv_dtype, q_dtype, tk, tv, st);
     } else if (d->kv_dtype == PKV_F16) {
         e = launch_decode_f16(p, G, st);
     } else if (d->kv_dtype == PKV_BF16) {

@@ -216,14 +216,7 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     }
     // 2. each sequence's own tokens, meanwhile on the caller's stream
     if (use_mma) {
-        if (d->kv_dtype == PKV_BF16)
-            e = launch_decode_mma_bf16(p, G, tk, tv, st);
-        else if (d->kv_dtype == PKV_F16)
-            e = launch_decode_mma_f16(p, G, tk, tv, st);
-        else if (q_dtype == PKV_BF16)
-            e = launch_decode_mma_fp8_bf16q(p, G, tk, tv, st);
-        else
-            e = launch_decode_mma_fp8_f16q(p, G, tk, tv, st);
+        e = launch_decode_gqa(p, G, d->kv_dtype, q_dtype, tk, tv, st);
     } else if (d->kv_dtype == PKV_BF16) {
         e = launch_decode_bf16(p, G, st);
     } else if (d->kv_dtype == PKV_F16) {

@@ -96,6 +96,10 @@ cudaError_t launch_decode_mma_fp8_bf16q(const DecodeParams& p, int G, const CUte
                                         cudaStream_t st);
 cudaError_t launch_decode_mma_fp8_f16q(const DecodeParams& p, int G, const CUtensorMap& tk, const CUtensorMap& tv,
                                        cudaStream_t st);
+// Tensor-core decode of grouped heads at head_size 128 for the pool type
+// (the warp-level MMA kernel).
+cudaError_t launch_decode_gqa(const DecodeParams& p, int G, int kv_dtype, int q_dtype, const CUtensorMap& tk,
+                              const CUtensorMap& tv, cudaStream_t st);
 
 // Shared-prefix (cascade) decode: the prefix pass over each group's shared
 // leading blocks, kPrefixPartitionBlocks blocks per prefix partition.  Wide
