@@ -162,14 +162,18 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // maximum exceeds it by more than this many log2 units (probabilities <= 2^8).
 constexpr float kRebaseLog2 = 8.0f;
 
-// Copy stages per warp and resident CTAs per SM: about 190 KB of tiles in
-// flight per SM either way; fp8 tiles are half the size, so twice the warps
-// share the same bytes (its per-block instruction count is higher).
+// Copy stages per warp and resident CTAs per SM.  Two stages keep a block
+// in flight while one is attended (a third measured no faster on either
+// type).  A CTA's start (its first copies' latency) is a fixed cost of each
+// short partition, so more resident CTAs hide more of it: fp8 CTAs keep
+// their Q^T fragments in shared memory and load the value bytes late, which
+// fits five of them per SM in the register file (longctx_fp8 decode call
+// 104.5 -> 102.4 us against four; six spill and lose).
 template <typename KT>
 struct MmaCfg {
     static constexpr int kWarps = 4;
-    static constexpr int kStages = KT::bytes == 1 ? 3 : 2;
-    static constexpr int kCtasPerSm = KT::bytes == 1 ? 4 : 3;
+    static constexpr int kStages = 2;
+    static constexpr int kCtasPerSm = KT::bytes == 1 ? 5 : 3;
 };
 
 template <typename KT, int NW, int NST>
@@ -180,8 +184,188 @@ struct MmaSmem {
     static constexpr int kPhysOffset = kBarOffset + NW * NST * 8;
     // merge weights: [NW][8] per-warp scale factors, [8] 1/denominator, [8] denominator
     static constexpr int kMergeOffset = kPhysOffset + NW * NST * 4;
-    static constexpr int kBytes = kMergeOffset + (NW * 8 + 16) * 4 + 1024;  // + alignment slack
+    // fp8: the Q^T B fragments, [8 k-steps][32 lanes] pairs (16-bit pools keep them in registers)
+    static constexpr int kQOffset = kMergeOffset + (NW * 8 + 16) * 4;
+    static constexpr int kBytes = kQOffset + (KT::bytes == 1 ? 8 * 32 * 8 : 0) + 1024;  // + alignment slack
 };
+
+// B fragments of Q^T for (sequence s, KV head h): column n = head g8 of the
+// group (heads >= G zero); fp8 pools take q as f16 (exact in the normal range).
+template <int G, typename KT, typename QT>
+__device__ __forceinline__ void load_qb(const void* q, int Hq, int s, int h, uint32_t (&qb)[8][2]) {
+    constexpr int D = 128;
+    const int lane = threadIdx.x & 31;
+    const int g8 = lane >> 2, qd = lane & 3;
+    const int g = g8 < G ? g8 : 0;
+    const int64_t row = static_cast<int64_t>(s) * Hq + h * G + g;
+    const unsigned char* qrow = static_cast<const unsigned char*>(q) + row * D * 2;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        if constexpr (KT::bytes != 1) {
+            qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * qd) * 2);
+            qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 8 + 2 * qd) * 2);
+        } else {
+            uint32_t w[2];
+            load_words<8>(qrow + (32 * qd + 4 * kk) * 2, w);
+            float f[4];
+            Unpack<QT, 4>::run(w, f);
+            qb[kk][0] = pack2<false>(f[0], f[1]);
+            qb[kk][1] = pack2<false>(f[2], f[3]);
+        }
+        if (g8 >= G) qb[kk][0] = qb[kk][1] = 0u;
+    }
+}
+
+// One 16-token block of the decode: S = K Q^T for the G heads on the MMA's
+// N columns, the online-softmax update of (m, l) per head with the lazy
+// reference maximum, and O^T += V^T P^T.  kt: the block's K tile (V tile
+// TILE bytes after it) in the 128-byte-swizzled layout the TMA lands;
+// nvalid: tokens of the block inside the sequence (value rows past it are
+// zeroed first).  Warp-uniform call.
+template <int G, typename KT, typename QT>
+__device__ __forceinline__ void mma_block(unsigned char* kt, int nvalid, const uint32_t (&qb)[8][2],
+                                          const uint2* qsm, float (&o)[8][4], float& mA, float& mB, float& lA,
+                                          float& lB, float qk_scale, uint32_t koff, uint32_t voff) {
+    constexpr bool kFP8 = KT::bytes == 1;
+    constexpr bool kBF = std::is_same<KT, BF16>::value;
+    constexpr int TILE = kBlockSize * 128 * KT::bytes;
+    const int lane = threadIdx.x & 31;
+    const int g8 = lane >> 2;
+    unsigned char* vt = kt + TILE;
+    const uint32_t kts = smem_addr(kt), vts = smem_addr(vt);
+    if (nvalid < kBlockSize) {
+        // zero the value rows past the sequence end (stale pool bytes
+        // must not reach the MMA: 0 * NaN is NaN)
+        constexpr int kChunksPerRow = kFP8 ? 8 : 16;
+        const int nz = (kBlockSize - nvalid) * kChunksPerRow;
+        for (int i = lane; i < nz; i += 32) {
+            const int row = nvalid + i / kChunksPerRow, c = i % kChunksPerRow;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+    }
+    // ---- S = K Q^T, two accumulators (even / odd k-steps) to halve the chain
+    float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (!kFP8) {
+        const int mat = lane >> 3, rr = lane & 7;
+        const int tok = rr + 8 * (mat & 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int chunk = 2 * kk + (mat >> 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
+            mma16816a<kBF>(sa[kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+    } else {
+        uint32_t w0[8], w1[8];
+        {
+            const uint4 c0 = lds128(kts + koff);
+            const uint4 c1 = lds128(kts + (koff ^ 16u));
+            const uint4 c2 = lds128(kts + koff + 1024u);
+            const uint4 c3 = lds128(kts + (koff ^ 16u) + 1024u);
+            w0[0] = c0.x; w0[1] = c0.y; w0[2] = c0.z; w0[3] = c0.w;
+            w0[4] = c1.x; w0[5] = c1.y; w0[6] = c1.z; w0[7] = c1.w;
+            w1[0] = c2.x; w1[1] = c2.y; w1[2] = c2.z; w1[3] = c2.w;
+            w1[4] = c3.x; w1[5] = c3.y; w1[6] = c3.z; w1[7] = c3.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a01, a45, a23, a67;
+            e4m3x4_to_f16x4(w0[kk], a01, a45);
+            e4m3x4_to_f16x4(w1[kk], a23, a67);
+            const uint2 qf = qsm[kk * 32 + lane];
+            mma16816a<false>(sa[kk & 1], a01, a23, a45, a67, qf.x, qf.y);
+        }
+    }
+    // ---- online softmax: s0 (tok g8, head A), s1 (tok g8, head B),
+    //      s2 (tok g8+8, head A), s3 (tok g8+8, head B)
+    float sv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sv[c] = (sa[0][c] + sa[1][c]) * qk_scale;
+    if (nvalid < kBlockSize) {
+        if (g8 >= nvalid) sv[0] = sv[1] = -INFINITY;
+        if (g8 + 8 >= nvalid) sv[2] = sv[3] = -INFINITY;
+    }
+    float bA = fmaxf(sv[0], sv[2]), bB = fmaxf(sv[1], sv[3]);
+#pragma unroll
+    for (int mask = 4; mask < 32; mask <<= 1) {
+        bA = fmaxf(bA, __shfl_xor_sync(kFull, bA, mask));
+        bB = fmaxf(bB, __shfl_xor_sync(kFull, bB, mask));
+    }
+    // Lazy reference maximum: the probabilities are taken against a
+    // reference that moves only when a block's maximum exceeds it by
+    // more than 2^kRebaseLog2, so every p stays <= 2^kRebaseLog2 (exact
+    // range for f16 / bf16) and O is rescaled only on those rare
+    // moves, not whenever one of the group's heads sees a new maximum.
+    // The partials carry the reference, and the merges use it as the
+    // row's maximum; the result is the same softmax.
+    const bool rbA = bA > mA + kRebaseLog2, rbB = bB > mB + kRebaseLog2;
+    const float nA = rbA ? bA : mA, nB = rbB ? bB : mB;
+    const float alA = rbA ? ex2(mA - nA) : 1.f;  // 0 on the first block (mA = -inf)
+    const float alB = rbB ? ex2(mB - nB) : 1.f;
+    mA = nA;
+    mB = nB;
+    const float p0 = ex2(sv[0] - nA), p1 = ex2(sv[1] - nB), p2 = ex2(sv[2] - nA), p3 = ex2(sv[3] - nB);
+    lA = lA * alA + (p0 + p2);
+    lB = lB * alB + (p1 + p3);
+    if (__builtin_expect(__any_sync(kFull, rbA || rbB), 0)) {  // skip when no head's reference moved
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= alA;
+            o[i][1] *= alB;
+            o[i][2] *= alA;
+            o[i][3] *= alB;
+        }
+    }
+    // P^T fragments: transpose the (token, head) 8x8 tiles of P.  P
+    // enters the product as a 16-bit head plus a 16-bit tail (two
+    // MMAs into the same float32 accumulator), so the probabilities
+    // keep 16 (bf16) or 22 (f16) significant bits, not 8 or 11.
+    uint32_t h01, t01, h23, t23;
+    pack2_split<kBF>(p0, p1, h01, t01);
+    pack2_split<kBF>(p2, p3, h23, t23);
+    const uint32_t pb0 = movmatrix_t(h01), pt0 = movmatrix_t(t01);  // tokens 0..7
+    const uint32_t pb1 = movmatrix_t(h23), pt1 = movmatrix_t(t23);  // tokens 8..15
+    // ---- O^T += V^T P^T
+    if constexpr (!kFP8) {
+        const int mat = lane >> 3, rr = lane & 7;
+        const int tok = rr + 8 * (mat >> 1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int chunk = 2 * i + (mat & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
+            mma16816a<kBF>(o[i], a0, a1, a2, a3, pb0, pb1);
+            mma16816a<kBF>(o[i], a0, a1, a2, a3, pt0, pt1);
+        }
+    } else {
+        // value bytes: chunk g8 of tokens 2qd, 2qd+1, 2qd+8, 2qd+9; the four
+        // offsets follow from one lane constant (see swz128)
+        uint4 va[4];
+        {
+            const uint32_t v1 = (voff ^ 16u) + 128u;
+            va[0] = lds128(vts + voff);
+            va[1] = lds128(vts + v1);
+            va[2] = lds128(vts + voff + 1024u);
+            va[3] = lds128(vts + v1 + 1024u);
+        }
+        const uint32_t wa[4] = {va[0].x, va[0].y, va[0].z, va[0].w};
+        const uint32_t wb[4] = {va[1].x, va[1].y, va[1].z, va[1].w};
+        const uint32_t wc[4] = {va[2].x, va[2].y, va[2].z, va[2].w};
+        const uint32_t wd[4] = {va[3].x, va[3].y, va[3].z, va[3].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int w = i >> 1;
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2i, 2i+1 of the chunk
+            uint32_t a01, a23, a45, a67;
+            e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), a01, a23);
+            e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), a45, a67);
+            mma16816a<false>(o[i], a01, a23, a45, a67, pb0, pb1);
+            mma16816a<false>(o[i], a01, a23, a45, a67, pt0, pt1);
+        }
+    }
+}
 
 template <int G, typename KT, typename QT, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
@@ -247,15 +431,12 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
 
     int tbl = -1;
     int k_issue = 0;
-    int issue_stage = 0;  // k_issue % NST, kept incrementally
-    auto issue_next = [&]() {  // warp-uniform call
+    auto issue_next = [&](const int stage) {  // warp-uniform call; stage = k_issue % NST
         if ((k_issue & 31) == 0) {
             const int k = k_issue + lane;
             tbl = k < nb_w ? __ldg(bt + static_cast<int64_t>(k) * NW) : -1;
         }
         const int phys = __shfl_sync(kFull, tbl, k_issue & 31);
-        const int stage = issue_stage;
-        issue_stage = issue_stage + 1 == NST ? 0 : issue_stage + 1;
         if (append_here && k_issue == nb_w - 1) {
             fused_commit<KT>(p, h, frow);
             __syncwarp();
@@ -284,30 +465,24 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
         ++k_issue;
     };
 
-    // ---- B fragments of Q^T (column n = head g8 of the group; heads >= G zero)
     uint32_t qb[8][2];
-    {
-        const int g = g8 < G ? g8 : 0;
-        const int64_t row = static_cast<int64_t>(s) * p.Hq + h * G + g;
-        const unsigned char* qrow = static_cast<const unsigned char*>(p.q) + row * D * 2;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            if constexpr (!kFP8) {
-                qb[kk][0] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 2 * qd) * 2);
-                qb[kk][1] = *reinterpret_cast<const uint32_t*>(qrow + (16 * kk + 8 + 2 * qd) * 2);
-            } else {
-                uint32_t w[2];
-                load_words<8>(qrow + (32 * qd + 4 * kk) * 2, w);
-                float f[4];
-                Unpack<QT, 4>::run(w, f);
-                qb[kk][0] = pack2<false>(f[0], f[1]);
-                qb[kk][1] = pack2<false>(f[2], f[3]);
-            }
-            if (g8 >= G) qb[kk][0] = qb[kk][1] = 0u;
-        }
-    }
+    uint2* qsm = reinterpret_cast<uint2*>(smem + SM::kQOffset);
+    if constexpr (!kFP8) load_qb<G, KT, QT>(p.q, p.Hq, s, h, qb);
 
-    for (int i = 0; i < NST && k_issue < nb_w; ++i) issue_next();
+#pragma unroll
+    for (int i = 0; i < NST; ++i)
+        if (k_issue < nb_w) issue_next(i);
+
+    if constexpr (kFP8) {
+        // the CTA's warps share one copy of the fragments (registers for a
+        // fifth resident CTA); warp w writes k-steps 2w, 2w + 1
+        uint32_t qt[8][2];
+        load_qb<G, KT, QT>(p.q, p.Hq, s, h, qt);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            if ((kk >> 1) == warp % 4) qsm[kk * 32 + lane] = make_uint2(qt[kk][0], qt[kk][1]);
+        __syncthreads();
+    }
 
     // O^T accumulators: m-tile i, c0/c1 = (row g8, heads 2qd, 2qd+1),
     // c2/c3 = (row g8 + 8, heads 2qd, 2qd+1).
@@ -320,163 +495,28 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     // g8 of row 2qd (the stage bases are 1024-byte aligned)
     const uint32_t koff = swz128(g8, 2 * qd), voff = swz128(2 * qd, g8);
     bool aborted = false;
-    int stage = 0;
     uint32_t phase = 0;  // (k / NST) & 1
-    for (int k = 0; k < nb_w; ++k) {
-        if (k > 0) {
-            ++stage;
-            if (stage == NST) {
-                stage = 0;
-                phase ^= 1u;
+    int tok0 = (j0 + warp) * kBlockSize;
+    // unrolled by the ring depth: each stage's addresses are constants
+    for (int k0 = 0; k0 < nb_w && !aborted; k0 += NST) {
+#pragma unroll
+        for (int st = 0; st < NST; ++st) {
+            if (k0 + st >= nb_w) break;
+            if (!mbar_wait(&bars[st], phase)) {
+                if (lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
+                aborted = true;
+                break;
             }
+            const int phys = stage_phys[st];
+            const int nvalid = min(kBlockSize, t1 - tok0);
+            tok0 += NW * kBlockSize;
+            if (phys >= 0 && phys < p.NB) {
+                mma_block<G, KT, QT>(wbase + st * STAGE, nvalid, qb, qsm, o, mA, mB, lA, lB, p.qk_scale, koff, voff);
+            }
+            __syncwarp();
+            if (k_issue < nb_w) issue_next(st);
         }
-        if (!mbar_wait(&bars[stage], phase)) {
-            if (lane == 0) report(p.err, PKV_DEVERR_TIMEOUT);
-            aborted = true;
-            break;
-        }
-        const int phys = stage_phys[stage];
-        const int tok0 = (j0 + warp + k * NW) * kBlockSize;
-        const int nvalid = min(kBlockSize, t1 - tok0);
-        if (phys >= 0 && phys < p.NB) {
-            unsigned char* kt = wbase + stage * STAGE;
-            unsigned char* vt = kt + TILE;
-            const uint32_t kts = smem_addr(kt), vts = smem_addr(vt);
-            if (nvalid < kBlockSize) {
-                // zero the value rows past the sequence end (stale pool bytes
-                // must not reach the MMA: 0 * NaN is NaN)
-                constexpr int kChunksPerRow = kFP8 ? 8 : 16;
-                const int nz = (kBlockSize - nvalid) * kChunksPerRow;
-                for (int i = lane; i < nz; i += 32) {
-                    const int row = nvalid + i / kChunksPerRow, c = i % kChunksPerRow;
-                    *reinterpret_cast<uint4*>(vt + (c >> 3) * 2048 + row * 128 + (c & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                __syncwarp();
-            }
-            // fp8: value bytes loaded up front (chunk g8 of tokens 2qd, 2qd+1,
-            // 2qd+8, 2qd+9) so their latency hides behind K Q^T; the four
-            // offsets follow from one lane constant (see swz128)
-            uint4 va[4];
-            if constexpr (kFP8) {
-                const uint32_t v1 = (voff ^ 16u) + 128u;
-                va[0] = lds128(vts + voff);
-                va[1] = lds128(vts + v1);
-                va[2] = lds128(vts + voff + 1024u);
-                va[3] = lds128(vts + v1 + 1024u);
-            }
-            // ---- S = K Q^T, two accumulators (even / odd k-steps) to halve the chain
-            float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            if constexpr (!kFP8) {
-                const int mat = lane >> 3, rr = lane & 7;
-                const int tok = rr + 8 * (mat & 1);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int chunk = 2 * kk + (mat >> 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
-                    mma16816a<kBF>(sa[kk & 1], a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-                }
-            } else {
-                uint32_t w0[8], w1[8];
-                {
-                    const uint4 c0 = lds128(kts + koff);
-                    const uint4 c1 = lds128(kts + (koff ^ 16u));
-                    const uint4 c2 = lds128(kts + koff + 1024u);
-                    const uint4 c3 = lds128(kts + (koff ^ 16u) + 1024u);
-                    w0[0] = c0.x; w0[1] = c0.y; w0[2] = c0.z; w0[3] = c0.w;
-                    w0[4] = c1.x; w0[5] = c1.y; w0[6] = c1.z; w0[7] = c1.w;
-                    w1[0] = c2.x; w1[1] = c2.y; w1[2] = c2.z; w1[3] = c2.w;
-                    w1[4] = c3.x; w1[5] = c3.y; w1[6] = c3.z; w1[7] = c3.w;
-                }
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    uint32_t a01, a45, a23, a67;
-                    e4m3x4_to_f16x4(w0[kk], a01, a45);
-                    e4m3x4_to_f16x4(w1[kk], a23, a67);
-                    mma16816a<false>(sa[kk & 1], a01, a23, a45, a67, qb[kk][0], qb[kk][1]);
-                }
-            }
-            // ---- online softmax: s0 (tok g8, head A), s1 (tok g8, head B),
-            //      s2 (tok g8+8, head A), s3 (tok g8+8, head B)
-            float sv[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sv[c] = (sa[0][c] + sa[1][c]) * p.qk_scale;
-            if (nvalid < kBlockSize) {
-                if (g8 >= nvalid) sv[0] = sv[1] = -INFINITY;
-                if (g8 + 8 >= nvalid) sv[2] = sv[3] = -INFINITY;
-            }
-            float bA = fmaxf(sv[0], sv[2]), bB = fmaxf(sv[1], sv[3]);
-#pragma unroll
-            for (int mask = 4; mask < 32; mask <<= 1) {
-                bA = fmaxf(bA, __shfl_xor_sync(kFull, bA, mask));
-                bB = fmaxf(bB, __shfl_xor_sync(kFull, bB, mask));
-            }
-            // Lazy reference maximum: the probabilities are taken against a
-            // reference that moves only when a block's maximum exceeds it by
-            // more than 2^kRebaseLog2, so every p stays <= 2^kRebaseLog2 (exact
-            // range for f16 / bf16) and O is rescaled only on those rare
-            // moves, not whenever one of the group's heads sees a new maximum.
-            // The partials carry the reference, and the merges use it as the
-            // row's maximum; the result is the same softmax.
-            const bool rbA = bA > mA + kRebaseLog2, rbB = bB > mB + kRebaseLog2;
-            const float nA = rbA ? bA : mA, nB = rbB ? bB : mB;
-            const float alA = rbA ? ex2(mA - nA) : 1.f;  // 0 on the first block (mA = -inf)
-            const float alB = rbB ? ex2(mB - nB) : 1.f;
-            mA = nA;
-            mB = nB;
-            const float p0 = ex2(sv[0] - nA), p1 = ex2(sv[1] - nB), p2 = ex2(sv[2] - nA), p3 = ex2(sv[3] - nB);
-            lA = lA * alA + (p0 + p2);
-            lB = lB * alB + (p1 + p3);
-            if (__any_sync(kFull, rbA || rbB)) {  // skip when no head's reference moved
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    o[i][0] *= alA;
-                    o[i][1] *= alB;
-                    o[i][2] *= alA;
-                    o[i][3] *= alB;
-                }
-            }
-            // P^T fragments: transpose the (token, head) 8x8 tiles of P.  P
-            // enters the product as a 16-bit head plus a 16-bit tail (two
-            // MMAs into the same float32 accumulator), so the probabilities
-            // keep 16 (bf16) or 22 (f16) significant bits, not 8 or 11.
-            uint32_t h01, t01, h23, t23;
-            pack2_split<kBF>(p0, p1, h01, t01);
-            pack2_split<kBF>(p2, p3, h23, t23);
-            const uint32_t pb0 = movmatrix_t(h01), pt0 = movmatrix_t(t01);  // tokens 0..7
-            const uint32_t pb1 = movmatrix_t(h23), pt1 = movmatrix_t(t23);  // tokens 8..15
-            // ---- O^T += V^T P^T
-            if constexpr (!kFP8) {
-                const int mat = lane >> 3, rr = lane & 7;
-                const int tok = rr + 8 * (mat >> 1);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int chunk = 2 * i + (mat & 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(vts + (chunk >> 3) * 2048 + swz128(tok, chunk & 7), a0, a1, a2, a3);
-                    mma16816a<kBF>(o[i], a0, a1, a2, a3, pb0, pb1);
-                    mma16816a<kBF>(o[i], a0, a1, a2, a3, pt0, pt1);
-                }
-            } else {
-                const uint32_t wa[4] = {va[0].x, va[0].y, va[0].z, va[0].w};
-                const uint32_t wb[4] = {va[1].x, va[1].y, va[1].z, va[1].w};
-                const uint32_t wc[4] = {va[2].x, va[2].y, va[2].z, va[2].w};
-                const uint32_t wd[4] = {va[3].x, va[3].y, va[3].z, va[3].w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int w = i >> 1;
-                    const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2i, 2i+1 of the chunk
-                    uint32_t a01, a23, a45, a67;
-                    e4m3x4_to_f16x4(__byte_perm(wa[w], wb[w], sel), a01, a23);
-                    e4m3x4_to_f16x4(__byte_perm(wc[w], wd[w], sel), a45, a67);
-                    mma16816a<false>(o[i], a01, a23, a45, a67, pb0, pb1);
-                    mma16816a<false>(o[i], a01, a23, a45, a67, pt0, pt1);
-                }
-            }
-        }
-        __syncwarp();
-        if (k_issue < nb_w) issue_next();
+        phase ^= 1u;
     }
 
     if (aborted) {
@@ -531,33 +571,61 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
-        const int g = idx / D, d = idx % D;
-        // inverse of the fragment layout: head g, head dimension d
-        int i, upper, gl;
-        if constexpr (kFP8) {
-            gl = d >> 4;
-            i = (d & 15) >> 1;
-            upper = d & 1;
-        } else {
-            i = d >> 4;
-            upper = (d >> 3) & 1;
-            gl = d & 7;
-        }
-        const int c = 2 * upper + (g & 1);
-        const int frag = 16 + (4 * i + c) * 33 + 4 * gl + (g >> 1);
-        float num = 0.f;
+    // ---- output: thread t writes head g = t / TPH, head dimensions
+    // [DPT (t % TPH), DPT (t % TPH + 1)) in one vector store
+    constexpr int TPH = NW * 32 / G;  // threads per head
+    constexpr int DPT = D / TPH;      // head dimensions per thread (G)
+    static_assert(TPH * G == NW * 32 && DPT * TPH == D, "output split");
+    {
+        const int g = threadIdx.x / TPH;
+        const int d0 = (threadIdx.x % TPH) * DPT;
+        float sc[NW];
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-            num = fmaf(msc[w * 8 + g], reinterpret_cast<float*>(smem + w * NST * STAGE)[frag], num);
-        const float out = num * minv[g] * p.v_scale;
+        for (int w = 0; w < NW; ++w) sc[w] = msc[w * 8 + g];
+        const float inv = minv[g];
+        float r[DPT];
+#pragma unroll
+        for (int j = 0; j < DPT; ++j) {
+            const int d = d0 + j;
+            // inverse of the fragment layout: head g, head dimension d
+            int i, upper, gl;
+            if constexpr (kFP8) {
+                gl = d >> 4;
+                i = (d & 15) >> 1;
+                upper = d & 1;
+            } else {
+                i = d >> 4;
+                upper = (d >> 3) & 1;
+                gl = d & 7;
+            }
+            const int frag = 16 + (4 * i + 2 * upper + (g & 1)) * 33 + 4 * gl + (g >> 1);
+            float num = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) num = fmaf(sc[w], reinterpret_cast<float*>(smem + w * NST * STAGE)[frag], num);
+            r[j] = num * inv * p.v_scale;
+        }
         const int64_t row = static_cast<int64_t>(s) * p.Hq + h * G + g;
         if (nparts == 1 && !p.cascade) {
-            reinterpret_cast<typename QT::storage*>(p.out)[row * D + d] = from_float<QT>(out);
+            constexpr bool kBFq = std::is_same<QT, BF16>::value;
+            uint32_t w[DPT / 2];
+#pragma unroll
+            for (int j = 0; j < DPT / 2; ++j) w[j] = pack2<kBFq>(r[2 * j], r[2 * j + 1]);
+            unsigned char* dst = static_cast<unsigned char*>(p.out) + (row * D + d0) * 2;
+            if constexpr (DPT == 8) {
+                *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else if constexpr (DPT == 4) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+            } else {
+                *reinterpret_cast<uint32_t*>(dst) = w[0];
+            }
         } else {
             const int64_t prow = row * p.NP + p.part_base + part;
-            p.part_o[prow * D + d] = out;
-            if (d == 0) {
+            float* dst = p.part_o + prow * D + d0;
+#pragma unroll
+            for (int j = 0; j + 4 <= DPT; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+            if constexpr (DPT == 2) *reinterpret_cast<float2*>(dst) = make_float2(r[0], r[1]);
+            if (d0 == 0) {
                 float M = -INFINITY;
 #pragma unroll
                 for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<float*>(smem + w * NST * STAGE)[g]);
