@@ -32,7 +32,9 @@
 // keys, contraction column k of lane quad member q covers head dimensions
 // 32q + 4k .. 32q + 4k + 3; for values, row g / g + 8 of m-tile i is head
 // dimension 16g + 2i / 16g + 2i + 1.  q is converted to f16 (exact in the
-// normal range).
+// normal range), and the CTA keeps one copy of its Q^T fragments in shared
+// memory rather than one per warp in registers, which fits a fifth CTA per
+// SM.
 #pragma once
 
 #include <cuda.h>
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(NW * 32, MmaCfg<KT>::kCtasPerSm)
 
     if constexpr (kFP8) {
         // the CTA's warps share one copy of the fragments (registers for a
-        // fifth resident CTA); warp w writes k-steps 2w, 2w + 1
+        // fifth resident CTA); warp w of the four writes k-steps 2w, 2w + 1
         uint32_t qt[8][2];
         load_qb<G, KT, QT>(p.q, p.Hq, s, h, qt);
 #pragma unroll
