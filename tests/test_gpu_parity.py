@@ -41,6 +41,7 @@ CASES = [
     ("f16", "f16", 128),
     ("bf16", "bf16", 64),
     ("e4m3", "f16", 64),
+    ("e4m3", "f16", 128),
 ]
 
 
