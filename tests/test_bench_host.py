@@ -94,3 +94,32 @@ def test_kernel_hash_ignores_comments_but_not_code():
     assert bench.code_only(src) != bench.code_only("int a = 1;\nint b = 3;\n")
     for kind in bench.KERNEL_SOURCES:
         assert len(bench.kernel_hash(kind)) == 12
+
+
+def test_kv_utilisation_counts_distinct_blocks_and_the_last_block_waste():
+    """The b - 1 waste bound of the paged pool ("vLLM 高性能大语言模型推理引擎深度技术评估与分布式架构展望",
+    physical blocks and the paging analogy): every sequence wastes at most the
+    slots of its last block, and a block several sequences share counts once."""
+    from types import SimpleNamespace
+    import bench
+    wl = SimpleNamespace(b=16, S=4)
+    lens = np.array([1, 16, 33, 20], np.int32)
+    tables = np.array([[3, -1, -1], [7, -1, -1], [4, 5, 6], [7, 9, -1]], np.int32)  # rows 1 and 3 share block 7
+    got = bench.kv_utilisation(SimpleNamespace(wl=wl, seq_lens=lens, tables=tables))
+    # distinct blocks 3, 7, 4, 5, 6, 9 hold 1, 16, 16, 16, 1, 4 tokens
+    assert got["distinct_blocks"] == 6
+    assert got["utilisation"] == round(54 / (6 * 16), 5)
+    assert got["max_waste_tokens_per_seq"] == 15  # the 1-token row and the 33-token row
+    assert 0 <= got["max_waste_tokens_per_seq"] <= wl.b - 1
+
+
+def test_bench_parity_bound_is_the_tests_bound():
+    """bench.py reports each config's error against the same per-element
+    bound the parity tests assert (its own copy, since bench.py imports
+    nothing from tests/)."""
+    import bench
+    from parity_util import relaxed_bound
+    rng = np.random.default_rng(5)
+    ref = np.concatenate([rng.normal(0, 3, 4000), rng.uniform(-20, 20, 4000), [0.0, 1e-30, 3.99, 4.0, 8.0]])
+    for dt, tol in (("bf16", 1e-2), ("f16", 2e-3)):
+        np.testing.assert_array_equal(bench.error_bound(ref, dt, tol, 7.5), relaxed_bound(ref, dt, tol, 7.5))
