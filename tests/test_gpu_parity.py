@@ -45,16 +45,18 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("kv,qd,D", CASES)
-@pytest.mark.parametrize("G", [1, 2, 4, 8])
+# path 0: the automatic choice (tensor cores for G >= 2 at D = 128); path 1:
+# the CUDA-core kernel forced, only where the automatic choice differs
+SMALL = [(kv, qd, D, G, path) for kv, qd, D in CASES for G in (1, 2, 4, 8) for path in (0, 1)
+         if path == 0 or (G > 1 and D == 128)]
+
+
+@pytest.mark.parametrize("kv,qd,D,G,path", SMALL)
 @pytest.mark.parametrize("partition", [0, 16, 64, 512])
-@pytest.mark.parametrize("path", [0, 1])
 def test_small_cases_match_oracle(lib, kv, qd, D, G, partition, path):
-    """path 0: automatic choice (tensor cores for G >= 2 at D = 128);
-    path 1: the CUDA-core kernel for every case."""
+    """Every element of a small edge-length batch against the oracle, for
+    each dtype / head size / group size / partition size and kernel."""
     from paged_kv_cache_10_gb300 import workloads
-    if path == 1 and (G == 1 or D != 128):
-        pytest.skip("automatic choice already is the CUDA-core kernel")
     Hkv = 2
     wl = workloads.custom(f"edge_{kv}_{D}_{G}", 7 + G + D, EDGE_LENS, Hkv * G, Hkv, D, kv_dtype=kv,
                           q_dtype=qd, partition_tokens=partition)
