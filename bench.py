@@ -405,6 +405,12 @@ def cpu_baseline(wl, step, budget_s=10.0, single_s=3.0):
     return out
 
 
+def _host_bits(t) -> np.ndarray:
+    """A device tensor's raw bits on the host (uint16 or uint8)."""
+    t = t.detach().cpu()
+    return t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 else t.view(torch.uint8).numpy()
+
+
 def oracle_parity(step) -> dict:
     """Untimed: the whole step (copy-on-write copies, appends, every row's
     decode) recomputed by the oracle from its own allocator model, against
@@ -419,12 +425,9 @@ def oracle_parity(step) -> dict:
     pools = (wl.k_pool.copy(), wl.v_pool.copy())
     ref = oracle_rows_step(wl, hs, np.arange(wl.S), pools)
 
-    def bits(t):
-        t = t.detach().cpu()
-        return t.view(torch.int16).numpy().view(np.uint16) if t.element_size() == 2 else t.view(torch.uint8).numpy()
-
-    pools_ok = bool(np.array_equal(bits(step.k_cache), pools[0]) and np.array_equal(bits(step.v_cache), pools[1]))
-    got = oracle.dequantize(bits(step.out), wl.q_dtype)
+    pools_ok = bool(np.array_equal(_host_bits(step.k_cache), pools[0])
+                    and np.array_equal(_host_bits(step.v_cache), pools[1]))
+    got = oracle.dequantize(_host_bits(step.out), wl.q_dtype)
     tol = TOL[wl.kv_dtype]
     vmax = float(np.max(np.abs(oracle.dequantize(pools[1], wl.kv_dtype)))) * (wl.v_scale if wl.kv_dtype == "e4m3"
                                                                                else 1.0)
@@ -712,6 +715,7 @@ def run_ours(args, rank, world, local_rank):
                                     steps=min(args.steps, 100), sampler=sampler, cpu_budget=4.0)
                 configs[key] = config_summary(ln)
             line["configs"] = configs
+            line["next"] = measure_next(args, rank, world, local_rank, sampler=sampler)
     finally:
         if sampler:
             sampler.stop()
@@ -799,13 +803,25 @@ def prefill_cpu_baseline(wl, budget_s=10.0):
 
 
 def run_prefill(args, rank, world, local_rank):
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    try:
+        return measure_prefill(args, rank, world, local_rank, args.workload, sampler=sampler)
+    finally:
+        if sampler:
+            sampler.stop()
+
+
+def measure_prefill(args, rank, world, local_rank, name, steps=None, sampler=None, cpu_budget=10.0):
+    """Times one prefill workload (K device-timed steps, the attention call,
+    the e2e loop) and, on rank 0 of a single-GPU run, the oracle leg.
+    Returns the JSON line of the workload (rank 0) or None."""
     from paged_kv_cache_10_gb300 import pagedkv as pk
     from paged_kv_cache_10_gb300 import workloads
     from paged_kv_cache_10_gb300.step import PrefillStep
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = workloads.PREFILL[args.workload]()
+    wl = workloads.PREFILL[name]()
     step = PrefillStep(wl, device=dev, plan=not args.no_plan)
     flops = prefill_flops(wl)
     nbytes = prefill_bytes(wl)
@@ -816,8 +832,7 @@ def run_prefill(args, rank, world, local_rank):
     for _ in range(max(args.warmup, 3)):
         step.run()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    K = args.steps
+    K = steps or args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     barrier()
     torch.cuda.synchronize()
@@ -873,8 +888,6 @@ def run_prefill(args, rank, world, local_rank):
     if rank != 0:
         return None
     clocks = sampler.summary(t_load0, t_load1) if sampler else None
-    if sampler:
-        sampler.stop()
     peak, peak_kind = measured_tensor_peak()
     a_ms = statistics.mean(attn_ms)
     achieved = flops / (a_ms / 1e3) / 1e12
@@ -908,8 +921,45 @@ def run_prefill(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if world == 1 and not (args.no_cpu_baseline or args.profile):
-        line["cpu_baseline"] = prefill_cpu_baseline(wl)
+        line["parity"] = prefill_parity(step)
+        line["cpu_baseline"] = prefill_cpu_baseline(wl, budget_s=cpu_budget)
+    del step
+    torch.cuda.empty_cache()
     return line
+
+
+def prefill_summary(line) -> dict:
+    """The per-workload fields of a prefill line."""
+    r = line["roofline"]
+    keep = ("metric", "us_per_step", "median_us_per_step", "tokens_per_s", "value", "unit", "dtype", "steps",
+            "gpu_launches", "clocks", "parity", "cpu_baseline")
+    out = {k: line[k] for k in keep if k in line}
+    out["e2e"] = {k: line["e2e"][k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+    out["roofline"] = {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "peak_kind",
+                                        "kernel", "mean_launch_us", "median_launch_us",
+                                        "algorithmic_flops_per_launch")}
+    c = line["config"]
+    out["config"] = {k: c[k] for k in ("workload", "num_seqs", "q_heads", "kv_heads", "head_size", "kv_dtype",
+                                       "new_tokens", "l2", "cta_order")}
+    return out
+
+
+# the rows beyond the decode configs that the default run also measures
+NEXT_PREFILL = ("prefill_chunked_gqa", "prefill_chunked_gqa_fp8")
+
+
+def measure_next(args, rank, world, local_rank, sampler=None) -> dict:
+    """Chunked prefill over a bf16 and an fp8 pool (device-timed, with e2e,
+    sampled oracle parity and the oracle's timing), the host prefix cache on
+    a request stream, and block swap to and from a pinned host pool."""
+    out = {}
+    for name in NEXT_PREFILL:
+        ln = measure_prefill(args, rank, world, local_rank, name, steps=min(args.steps, 50), sampler=sampler,
+                             cpu_budget=4.0)
+        out[name] = prefill_summary(ln)
+    out["prefix_cache_host"] = run_apc(argparse.Namespace(steps=50))
+    out["swap_blocks"] = run_swap(argparse.Namespace(workload="llama3_8b_gqa", steps=20, warmup=3), local_rank)
+    return out
 
 
 # ------------------------------------------- prefill per-unit cost sweep
@@ -956,6 +1006,54 @@ def run_prefill_unit_sweep(args, local_rank):
     return {"metric": "prefill cost per unit round (equal units)", "unit": "us", "points": points,
             "fit_4_rounds": {"us_per_key_tile": round(float(slope), 3), "us_per_unit": round(float(icpt), 2)},
             "sms": sms}
+
+
+def prefill_parity(step, per_seq=8) -> dict:
+    """Untimed: the step's host bookkeeping and pools against the oracle's
+    own allocator model and append, and the first and last ``per_seq`` new
+    tokens of every chunk (all heads, every key each sees) against the
+    float64 oracle."""
+    import oracle
+    wl = step.wl
+    t0 = time.perf_counter()
+    slots, tables, lens = oracle_prefill_host(wl)
+    host_ok = (np.array_equal(step.slots, slots) and np.array_equal(step.tables, tables)
+               and np.array_equal(step.seq_lens, lens))
+    kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.append(wl.k_new, wl.v_new, wl.dtype, slots, kp, vp, wl.kv_dtype, wl.k_scale, wl.v_scale)
+    pools_ok = bool(np.array_equal(_host_bits(step.k_cache), kp) and np.array_equal(_host_bits(step.v_cache), vp))
+    got_all = oracle.dequantize(_host_bits(step.out), wl.dtype)
+    tol = TOL[wl.kv_dtype]
+    vmax = float(np.max(np.abs(oracle.dequantize(vp, wl.kv_dtype)))) * (wl.v_scale if wl.kv_dtype == "e4m3" else 1.0)
+    qs = step.query_start
+    err_max = ref_max = 0.0
+    over = -tol
+    tokens = 0
+    finite = True
+    for s in range(wl.S):
+        n = int(wl.qlens[s])
+        ctx = int(lens[s]) - n
+        spans = sorted({(0, min(per_seq, n)), (max(0, n - per_seq), n)})
+        for a, b in spans:
+            if b <= a:
+                continue
+            # the oracle takes the rows as the last b - a tokens of a sequence of ctx + b
+            ref = oracle.paged_prefill(np.ascontiguousarray(wl.q[qs[s] + a:qs[s] + b]), wl.dtype,
+                                       np.array([0, b - a], np.int32), kp, vp, wl.kv_dtype, tables[s:s + 1],
+                                       np.array([ctx + b], np.int32), wl.scale, wl.k_scale, wl.v_scale)
+            got = got_all[qs[s] + a:qs[s] + b]
+            err = np.abs(got - ref)
+            finite = finite and bool(np.all(np.isfinite(got)))
+            err_max = max(err_max, float(err.max()))
+            ref_max = max(ref_max, float(np.abs(ref).max()))
+            over = max(over, float(np.max(err - error_bound(ref, wl.dtype, tol, vmax))))
+            tokens += b - a
+    return {"tokens": tokens, "of_tokens": int(wl.T), "max_abs_err": err_max, "max_abs_oracle": ref_max, "tol": tol,
+            "within_tolerance": bool(over <= 0 and finite), "max_err_minus_bound": over,
+            "pools_bit_exact": pools_ok, "host_bookkeeping_exact": bool(host_ok),
+            "oracle_s": round(time.perf_counter() - t0, 2),
+            "basis": f"first and last {per_seq} new tokens of every chunk (all heads) against the float64 oracle "
+                     "(every token at full size in the GPU tests); bound as for the decode"}
 
 
 # ------------------------------------------------------ prefix-cache timing
