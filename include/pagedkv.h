@@ -331,11 +331,11 @@ pkv_status pkv_decode_plan(const int32_t* seq_lens, int32_t num_seqs, int32_t nu
  * num_kv_heads in {1, 2, 4, 8}.  The own tokens use the kernels plain decode
  * uses.  A member index or block count out of range sets
  * PKV_DEVERR_SEQ_LEN and the offending rows are skipped.
- * Streams: the prefix pass runs on a stream the library owns (one per
- * device, created by the first call on it), forked from `stream` by an event
- * and joined back before the merge, so it overlaps the own-token decode.
- * The call is ordered on `stream` like any other and can be captured into a
- * CUDA graph (make the first call on a device outside a capture).
+ * Streams: every launch goes to `stream`.  The own-token decode is a
+ * programmatic dependent of the prefix pass and runs beside it; one extra
+ * CTA of its grid waits for the prefix pass, and the merge waits for that
+ * grid.  The call is ordered on `stream` like any other and can be captured
+ * into a CUDA graph.  num_seqs above 65534 returns PKV_ERR_UNSUPPORTED.
  */
 pkv_status pkv_paged_attention_decode_cascade(const void* q, int32_t q_dtype, int32_t num_seqs,
                                               int32_t num_q_heads, const void* k_cache, const void* v_cache,

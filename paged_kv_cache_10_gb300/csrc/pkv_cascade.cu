@@ -17,9 +17,16 @@
 //      the end of its group's prefix), partials at indices NPP + p;
 //   3. the merge kernel combines prefix and own partials of every row.
 //
+// The three run in this order on the caller's stream, each later one a
+// programmatic dependent of the one before.  The prefix pass lets the
+// own-token decode start at once (it reads the pool and writes other
+// partials), so the two run side by side; one extra CTA of the decode grid
+// waits for the prefix pass to complete, so the merge, which waits for the
+// decode grid, sees both.  No second stream or event is involved, and the
+// call can be captured into a CUDA graph.
+//
 // The result is the same function as pkv_paged_attention_decode.
 #include <cstdint>
-#include <mutex>
 
 #include "pkv_internal.h"
 
@@ -28,35 +35,6 @@ namespace pkv {
 namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// The prefix pass and the own-token decode read the pool and write disjoint
-// partials, so they may run at the same time: the prefix pass goes to a
-// library-owned stream forked from the caller's (an event), and the caller's
-// stream waits for it (a second event) before the merge.  The call stays
-// ordered on the caller's stream and can be captured into a CUDA graph.
-// One side stream and event pair per device; the mutex keeps the record /
-// wait pairs of concurrent callers from interleaving.
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex side_mu;
-
-cudaError_t side_stream(SideStream** out) {
-    static SideStream per_dev[kMaxDevices];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    SideStream& ss = per_dev[dev];
-    if (!ss.stream) {
-        if ((e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-        if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-    }
-    *out = &ss;
-    return cudaSuccess;
-}
 }  // namespace
 
 }  // namespace pkv
@@ -109,7 +87,7 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     if (fp8 && !(d->k_scale > 0.f && d->v_scale > 0.f)) return PKV_ERR_INVALID;
     const int G = num_q_heads / d->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs > 65535 || d->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65534 || d->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;  // + the decode's join layer
     if (num_seqs == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out || !seq_group) return PKV_ERR_INVALID;
     if (num_groups > 0 && (!group_blocks || !group_offsets || !group_members)) return PKV_ERR_INVALID;
@@ -176,9 +154,7 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     const bool prefix = npp > 0 && row_chunks > 0;
-    std::unique_lock<std::mutex> lock(side_mu, std::defer_lock);
-    SideStream* ss = nullptr;
-    // 1. shared prefixes, on the side stream, after everything before this call
+    // 1. shared prefixes, after everything before this call
     if (prefix) {
         CascadeParams cp{p, group_offsets, group_members, G, static_cast<int32_t>(row_chunks), npp,
                          block_tables, d->num_blocks, p.qk_scale, 1.f};
@@ -201,20 +177,12 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
         }
         const CUtensorMap& pk = (staged || !use_mma) ? tpk : tk;
         const CUtensorMap& pv = (staged || !use_mma) ? tpv : tv;
-        lock.lock();
-        if (side_stream(&ss) != cudaSuccess) return PKV_ERR_CUDA;
-        if (cudaEventRecord(ss->fork, st) != cudaSuccess || cudaStreamWaitEvent(ss->stream, ss->fork, 0) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        if (staged) e = launch_cascade_stage_fp8(cp, num_groups, max_group_blocks, q_dtype, k_cache, v_cache, staging,
-                                                 ss->stream);
-        if (e == cudaSuccess) e = launch_cascade_prefix_tc(cp, num_groups, q_dtype, d->head_size, tq, pk, pv, ss->stream);
-        if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->stream);
-        if (e != cudaSuccess) {
-            (void)cudaStreamWaitEvent(st, ss->join, 0);  // keep the caller's stream behind what was enqueued
-            return PKV_ERR_CUDA;
-        }
+        if (staged) e = launch_cascade_stage_fp8(cp, num_groups, max_group_blocks, q_dtype, k_cache, v_cache, staging, st);
+        if (e == cudaSuccess) e = launch_cascade_prefix_tc(cp, num_groups, q_dtype, d->head_size, tq, pk, pv, st);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        p.join_primary = 1;
     }
-    // 2. each sequence's own tokens, meanwhile on the caller's stream
+    // 2. each sequence's own tokens, beside the prefix pass
     if (use_mma) {
         e = launch_decode_gqa(p, G, d->kv_dtype, q_dtype, tk, tv, st);
     } else if (d->kv_dtype == PKV_BF16) {
@@ -226,10 +194,8 @@ extern "C" pkv_status pkv_paged_attention_decode_cascade(
     } else {
         e = launch_decode_fp8_f16q(p, G, st);
     }
-    // join before the merge reads the prefix partials
-    if (prefix && cudaStreamWaitEvent(st, ss->join, 0) != cudaSuccess) return PKV_ERR_CUDA;
     if (e != cudaSuccess) return PKV_ERR_CUDA;
-    // 3. merge every row
+    // 3. merge every row, once the decode grid (and with it the prefix pass) is complete
     e = launch_merge(p, q_dtype, st);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -83,12 +83,16 @@ struct DecodeSmem {
 // This CTA's (partition, KV head, sequence): from the grid, or from the
 // host's work list (unit = s * (NP - part_base) + partition, KV head
 // fastest).  A unit outside the batch sets PKV_DEVERR_SEQ_LEN; false: skip.
+// With join_primary the grid's extra z-layer holds no units: its CTA
+// (0, 0, S) waits there for the programmatic primary grid to complete.
 __device__ __forceinline__ bool decode_unit(const DecodeParams& p, int& part, int& h, int& s) {
     if (!p.work) {
         part = blockIdx.x;
         h = blockIdx.y;
         s = blockIdx.z;
-        return true;
+        if (s < p.S) return true;
+        if (part == 0 && h == 0) wait_primary_grid();
+        return false;
     }
     const int64_t lin = blockIdx.x;
     const int u = __ldg(p.work + lin / p.Hkv);
@@ -420,9 +424,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t st) {
         configured[dev] = true;
     }
     const dim3 grid = p.work ? dim3(static_cast<unsigned>(static_cast<int64_t>(p.num_work) * p.Hkv))
-                             : dim3(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
-    kern<<<grid, NW * 32, SMEM, st>>>(p);
-    return cudaGetLastError();
+                             : dim3(p.NP - p.part_base, p.Hkv, p.S + (p.join_primary ? 1 : 0));  // this launch's partitions
+    return launch_maybe_pdl(p.join_primary != 0 && !p.work, kern, grid, dim3(NW * 32), SMEM, st, p);
 }
 
 template <typename KT, typename QT>

@@ -657,9 +657,8 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, const CUtensorMap& tk, co
         configured[dev] = true;
     }
     const dim3 grid = p.work ? dim3(static_cast<unsigned>(static_cast<int64_t>(p.num_work) * p.Hkv))
-                             : dim3(p.NP - p.part_base, p.Hkv, p.S);  // this launch's partitions
-    kern<<<grid, NW * 32, SMEM, st>>>(p, tk, tv);
-    return cudaGetLastError();
+                             : dim3(p.NP - p.part_base, p.Hkv, p.S + (p.join_primary ? 1 : 0));  // this launch's partitions
+    return launch_maybe_pdl(p.join_primary != 0 && !p.work, kern, grid, dim3(NW * 32), SMEM, st, p, tk, tv);
 }
 
 template <typename KT, typename QT>

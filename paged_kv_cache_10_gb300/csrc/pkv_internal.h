@@ -57,7 +57,36 @@ struct DecodeParams {
     // (partition, KV head, sequence).
     const int32_t* work = nullptr;
     int32_t num_work = 0;
+    // Cascade decode: this launch is a programmatic dependent of the prefix
+    // pass before it on the stream.  The grid gets one more z-layer; its CTA
+    // (0, 0, S) waits for the prefix pass to complete, so this grid completes
+    // after it and a programmatic dependent of this grid (the merge) sees both.
+    int32_t join_primary = 0;
 };
+
+// Launches kern on st, as a programmatic dependent of the kernel before it
+// when pdl is set (a plain launch where the driver refuses the attribute).
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+    if (pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute la[1];
+        la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        la[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = la;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+        if (e != cudaErrorNotSupported && e != cudaErrorInvalidValue) return e;
+        (void)cudaGetLastError();
+    }
+    kern<<<grid, block, smem, st>>>(args...);
+    return cudaGetLastError();
+}
 
 // First token of a sequence's own (non-shared) attention range, clamped
 // into [0, L] on whole blocks; out-of-range group data reports

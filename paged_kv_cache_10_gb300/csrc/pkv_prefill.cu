@@ -293,6 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                       const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr bool kBF = std::is_same<T, BF16>::value;
+    // cascade decode: the own-token decode after this grid reads nothing it
+    // writes and may start at once
+    if constexpr (kPrefix) allow_dependent_launch();
     using TL = Tile<D>;
     constexpr int kOffQ = TL::kOffQ, kOffK = TL::kOffK, kOffV = TL::kOffV, kOffMisc = TL::kOffMisc;
     constexpr int kOpBytes = TL::kOp, kDB = TL::kDB;

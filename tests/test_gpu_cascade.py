@@ -152,10 +152,10 @@ def test_cascade_fp8_workspace_must_hold_the_staging(lib):
 
 
 def test_cascade_graph_replay_and_stream_order(lib):
-    """The prefix pass runs on the library's own stream, forked from the
-    caller's and joined before the merge: captured into a CUDA graph the step
-    replays to the same bits as eager, and on a non-default caller stream the
-    eager result is the same too."""
+    """The prefix pass, the own-token decode (its programmatic dependent)
+    and the merge all run on the caller's stream: captured into a CUDA graph
+    the step replays to the same bits as eager, and on a non-default caller
+    stream the eager result is the same too."""
     from paged_kv_cache_10_gb300 import workloads
     from paged_kv_cache_10_gb300.step import DecodeStep
     wl = workloads.fork_groups("cgraph", 74, [(320, 5), (96, 3)], 2, 32, 8)
