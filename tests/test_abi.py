@@ -127,6 +127,34 @@ def test_prefill_validation_rejects_before_any_launch(pk):
         assert call(desc=bad, ws=fake, ws_bytes=need) == pk.ERR_INVALID
 
 
+def test_cascade_validation_rejects_before_any_launch(pk):
+    L = pk.lib()
+    d = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="bf16").c()
+    d96 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=96, kv_dtype="bf16").c()
+    d8 = pk.CacheDesc(num_blocks=8, num_kv_heads=2, head_size=128, kv_dtype="e4m3", k_scale=0.0).c()
+    fake = 1 << 20  # never dereferenced: every call below fails validation first
+
+    def call(desc=d, q_dtype=1, S=2, Hq=8, mgb=2, part=16, ws=None, ws_bytes=0, q=fake):
+        return L.pkv_paged_attention_decode_cascade(q, q_dtype, S, Hq, fake, fake, ctypes.byref(desc), fake, 4,
+                                                    fake, 64, fake, fake, fake, fake, 1, 2, mgb, 0.1, fake, ws,
+                                                    ws_bytes, part, None)
+
+    assert call(S=0) == pk.OK                           # an empty batch needs no device
+    assert call(S=65535) == pk.ERR_UNSUPPORTED          # the decode grid's join layer needs one more z index
+    assert call(desc=d96) == pk.ERR_UNSUPPORTED         # head_size 96
+    assert call(q_dtype=0) == pk.ERR_UNSUPPORTED        # f16 q over a bf16 pool
+    assert call(Hq=6) == pk.ERR_UNSUPPORTED             # 3 query heads per KV head
+    assert call(Hq=5) == pk.ERR_INVALID                 # heads not a multiple
+    assert call(desc=d8) == pk.ERR_INVALID              # fp8 pool without a positive k_scale
+    assert call(mgb=5) == pk.ERR_INVALID                # shared prefix longer than the block table
+    assert call(part=24) == pk.ERR_INVALID              # partition not a multiple of the block size
+    assert call(q=fake + 2) == pk.ERR_INVALID           # q not 16-byte aligned
+    assert call() == pk.ERR_WORKSPACE                   # no workspace for the partials
+    need = L.pkv_decode_cascade_workspace_bytes(2, 8, 128, 64, 16, 2)
+    assert need > 0
+    assert call(ws=fake, ws_bytes=need - 1) == pk.ERR_WORKSPACE
+
+
 def test_prefill_workspace_bytes(pk):
     """0 for 16-bit pools (read in place); for fp8 pools a 4-byte table entry
     per (sequence, block) and two 16-bit copies of S * MB blocks, each part
