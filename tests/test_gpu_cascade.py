@@ -177,3 +177,47 @@ def test_cascade_graph_replay_and_stream_order(lib):
     torch.cuda.synchronize()
     assert lib.get_device_error() == 0
     assert np.array_equal(host_bits(st.out), eager)
+
+
+def test_cascade_merge_waits_for_the_prefix_pass(lib):
+    """The merge must see the prefix pass's partials, which only the decode
+    grid's join CTA orders before it.  The workspace is filled with NaN bits
+    before every call (so a partial read too early is wrong, not a stale
+    copy of the right one), on a batch whose prefix pass outlasts the
+    own-token decode (32 rows over an 8192-token shared prefix: 64 prefix
+    CTAs of 8 key tiles, one wave of short own-token CTAs).  Eager calls and
+    CUDA-graph replays of fill + call give the oracle-checked bits every
+    time."""
+    from paged_kv_cache_10_gb300 import workloads
+    from paged_kv_cache_10_gb300.step import DecodeStep
+    wl = workloads.fork_groups("cjoin", 75, [(8192, 32)], 0, 32, 8)
+    st = DecodeStep(wl, device="cuda", cascade=True)
+    assert st.groups.num_groups == 1 and st.workspace is not None
+    st.workspace.fill_(255)
+    st.run()
+    torch.cuda.synchronize()
+    err, mx = check_step(st)
+    assert err <= TOL["bf16"], (err, mx)
+    ref = host_bits(st.out).copy()
+
+    def call():
+        st.workspace.fill_(255)
+        st.decode()
+
+    for _ in range(30):
+        st.out.zero_()
+        call()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(st.out), ref)
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+    for _ in range(100):
+        st.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(st.out), ref)
+    assert lib.get_device_error() == 0
