@@ -613,8 +613,7 @@ def measure_decode(args, rank, world, local_rank, name, cascade=False, graph=Fal
         roof_bytes += nbytes["append"] + nbytes["copy"]
     achieved = roof_bytes / (dec_ms / 1e3) / 1e9
     kind = decode_kernel_kind(wl) if not cascade else "cascade"
-    traffic_name = name + ("_cascade" if cascade else "")
-    traffic = recorded_traffic(traffic_name, kind)
+    traffic = recorded_traffic(name, kind)  # the kind's source hash tells the cascade row from the plain one
     ms_per_step = total_ms / K
     line = {
         "metric": METRIC,

@@ -123,3 +123,22 @@ def test_bench_parity_bound_is_the_tests_bound():
     ref = np.concatenate([rng.normal(0, 3, 4000), rng.uniform(-20, 20, 4000), [0.0, 1e-30, 3.99, 4.0, 8.0]])
     for dt, tol in (("bf16", 1e-2), ("f16", 2e-3)):
         np.testing.assert_array_equal(bench.error_bound(ref, dt, tol, 7.5), relaxed_bound(ref, dt, tol, 7.5))
+
+
+def test_recorded_traffic_covers_every_reported_kernel():
+    """profiles/ncu_traffic.txt holds a row, for the current kernel sources,
+    for every workload whose line carries roofline.traffic: each decode
+    config (the cascade by its own source hash) and each prefill row."""
+    import types
+    import bench
+    heads = {"tiny_fp16": (4, 4, 64), "llama7b_mha": (32, 32, 128), "llama3_8b_gqa": (32, 8, 128),
+             "longctx_fp8": (64, 8, 128), "prefix_share": (32, 8, 128)}  # (query heads, KV heads, head size)
+    for name, cascade, _ in bench.DECODE_CONFIGS:
+        Hq, Hkv, D = heads[name]
+        kind = "cascade" if cascade else bench.decode_kernel_kind(types.SimpleNamespace(Hq=Hq, Hkv=Hkv, D=D))
+        t = bench.recorded_traffic(name, kind)
+        assert t is not None and t > 0, (name, kind)
+    for name in bench.NEXT_PREFILL + ("prefill_prompt_gqa", "prefill_prompt_mha"):
+        assert bench.recorded_traffic(name, "prefill"), name
+    # the plain and the cascade rows of prefix_share are told apart by their hash
+    assert bench.recorded_traffic("prefix_share", "cascade") != bench.recorded_traffic("prefix_share", "tensor_core")
