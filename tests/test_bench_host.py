@@ -138,7 +138,9 @@ def test_recorded_traffic_covers_every_reported_kernel():
         kind = "cascade" if cascade else bench.decode_kernel_kind(types.SimpleNamespace(Hq=Hq, Hkv=Hkv, D=D))
         t = bench.recorded_traffic(name, kind)
         assert t is not None and t > 0, (name, kind)
+    from paged_kv_cache_10_gb300 import workloads
     for name in bench.NEXT_PREFILL + ("prefill_prompt_gqa", "prefill_prompt_mha"):
+        assert name in workloads.PREFILL, name
         assert bench.recorded_traffic(name, "prefill"), name
     # the plain and the cascade rows of prefix_share are told apart by their hash
     assert bench.recorded_traffic("prefix_share", "cascade") != bench.recorded_traffic("prefix_share", "tensor_core")
