@@ -1,13 +1,17 @@
 """Host-side logic of bench.py without a GPU: the multi-rank aggregation
 (whole-job bytes summed over ranks, time = slowest rank) over a gloo process
-group of two CPU ranks, and the algorithmic byte count of a step."""
+group of two CPU ranks, the algorithmic byte count of a step, the
+recorded traffic rows, and the reference arm (the oracle) run on the CPU."""
 import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _free_port():
@@ -144,3 +148,27 @@ def test_recorded_traffic_covers_every_reported_kernel():
         assert bench.recorded_traffic(name, "prefill"), name
     # the plain and the cascade rows of prefix_share are told apart by their hash
     assert bench.recorded_traffic("prefix_share", "cascade") != bench.recorded_traffic("prefix_share", "tensor_core")
+
+
+@pytest.mark.parametrize("workload", ["tiny_fp16", "prefill_chunked_gqa"])
+def test_reference_arm_line_and_no_product_code(workload):
+    """bench.py --impl reference (the oracle as the reference arm) prints one
+    JSON line with the arm's contract fields, on the CPU, and its process
+    never loads the product library."""
+    import json
+    import subprocess
+    import sys
+    code = ("import json, sys, bench; bench.main(['--impl', 'reference', '--steps', '1', '--warmup', '1', "
+            f"'--workload', '{workload}']); "
+            "maps = open('/proc/self/maps').read(); "
+            "print('PRODUCT_LOADED' if 'libpagedkv' in maps else 'PRODUCT_NOT_LOADED')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert lines[-1] == "PRODUCT_NOT_LOADED"
+    line = json.loads(lines[-2])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["unit"] == line["e2e"]["unit"] and line["e2e"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["config"]["workload"] == workload
