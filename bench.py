@@ -14,7 +14,10 @@ copied from pinned host memory and the output copied back inside the timed
 region.  ``roofline`` is the decode kernel's achieved bandwidth against the
 measured HBM copy peak.  ``cpu_baseline`` times the float64 oracle on a
 bounded sample of the same workload.  ``--impl reference`` times that oracle
-alone, as the reference arm.
+alone, as the reference arm.  The default run (the Llama-7B-shaped MHA
+workload on one GPU) also times every other decode config under ``configs``
+and the chunked prefill (bf16 and fp8 pools), the host prefix cache and block
+swap under ``next``; ``--workload prefill_*`` times a prefill step instead.
 
 With ``--gpus N`` (torchrun) every rank runs its own replica of the workload
 on its own GPU (the path has no exchange step; no collective touches the
@@ -1240,7 +1243,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle leg (cpu_baseline timing and the untimed parity check)")
     ap.add_argument("--configs", choices=["all", "none"], default=None,
-                    help="also time every decode config in the same run and report each under 'configs' "
+                    help="also time every decode config in the same run and report each under 'configs', "
+                         "and the chunked prefill, prefix cache and block swap under 'next' "
                          "(default: all for the default workload on one GPU, none otherwise)")
     ap.add_argument("--decode-plan", choices=["auto", "on", "off"], default="auto",
                     help="decode: CTAs in the host plan's longest-first order (auto: when unit lengths differ "
